@@ -1,0 +1,338 @@
+#!/usr/bin/env python3
+"""Benchmark of libdspark's draft-sampling hot path on GB300.
+
+One step = one draft block (all gamma positions) of the workload: W1 gather, bias product,
+logits, temperature softmax normaliser, Philox Gumbel-max sampling, Eq 7 confidence and the
+prefix survival, all in libdspark's kernels.  The default workload is the Qwen3-4B-shaped
+latency regime (B=1, gamma=7, V=151936, r=256, d=2560, bf16).  The metric is draft tokens/s
+(B * gamma per block), plus the achieved HBM bandwidth of the draft kernel against the measured
+copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun), every rank drafts its own independent requests (weak scaling, no
+collective on the data path); value = all ranks' tokens / the slowest rank's time.
+``--impl reference`` times the CPU oracle (the plain fp64 restatement of the pages' equations)
+on the host cores, one draft position over the full vocabulary per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft tokens/sec (B×γ per block) and achieved HBM GB/s vs roofline, 1 GB300"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: every timed block starts with a cold L2
+
+# ncu DRAM traffic (read + write bytes) of one draft-kernel launch on the default workload,
+# with the sha256 prefix of the kernel source it was measured on.  A changed kernel reports null.
+TRAFFIC = {"source_sha": None, "bytes_per_launch": None}
+
+
+def _sha(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def algorithmic_bytes(wl) -> int:
+    """What one block must move: per step W2 once, U_k once, the target once, the gathered W1
+    rows and h_k; once per block the confidence weight w; outputs are negligible."""
+    es_w = 4 if wl.dtype == "f32" else 2
+    es_u = es_w
+    per_step = wl.V * wl.r * es_w + wl.B * wl.V * es_u + wl.B * wl.r * es_w + wl.B * wl.d * es_u
+    if wl.target_noise is not None:
+        per_step += wl.B * wl.V * 4
+    if wl.head == "rnn":
+        per_step += 3 * wl.r * (2 * wl.r + wl.d) * es_w
+    return wl.gamma * per_step + (wl.d + wl.r) * es_w
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_reference(args, wl):
+    """CPU oracle, one draft position (full vocabulary, all B requests) per step."""
+    import numpy as np
+
+    from oracle import oracle
+    from semi_autoregressive_drafting_gb300 import inputs
+
+    t = inputs.generate(wl)
+    O = inputs.to_oracle
+    cores = os.cpu_count() or 1
+    U = O(t["U"])
+    h = O(t["h"])
+
+    def one(k):
+        return oracle.draft(head=0 if wl.head == "markov" else 1, B=wl.B, gamma=1, V=wl.V,
+                            r=wl.r, d=wl.d, T=wl.T, seed=wl.seed, W1=O(t["W1"]), W2=O(t["W2"]),
+                            Wj=O(t.get("Wj")), U=np.ascontiguousarray(U[:, k:k + 1]),
+                            x0=O(t["x0"]), h=np.ascontiguousarray(h[:, k:k + 1]), w=O(t["w"]),
+                            nthreads=cores)
+
+    for i in range(args.warmup):
+        one(i % wl.gamma)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(i % wl.gamma)
+    dt = time.perf_counter() - t0
+    value = wl.B * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.name, "B": wl.B, "gamma": wl.gamma,
+                                        "V": wl.V, "r": wl.r, "d": wl.d},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "one draft position over the full vocabulary per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def cpu_baseline(wl, seconds: float = 15.0):
+    """The oracle as it stands on the host cores, on whole draft positions of the workload."""
+    import numpy as np
+
+    from oracle import oracle
+    from semi_autoregressive_drafting_gb300 import inputs
+
+    t = inputs.generate(wl)
+    O = inputs.to_oracle
+    cores = os.cpu_count() or 1
+    U, h = O(t["U"]), O(t["h"])
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        k = n % wl.gamma
+        oracle.draft(head=0 if wl.head == "markov" else 1, B=wl.B, gamma=1, V=wl.V, r=wl.r,
+                     d=wl.d, T=wl.T, seed=wl.seed, W1=O(t["W1"]), W2=O(t["W2"]),
+                     Wj=O(t.get("Wj")), U=np.ascontiguousarray(U[:, k:k + 1]), x0=O(t["x0"]),
+                     h=np.ascontiguousarray(h[:, k:k + 1]), w=O(t["w"]), nthreads=cores)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": wl.B * n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} draft positions x B={wl.B} over the full vocabulary ({dt:.1f} s)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3_4b_markov")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from semi_autoregressive_drafting_gb300 import inputs
+    wl = inputs.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, wl)
+        return
+
+    import torch
+
+    import semi_autoregressive_drafting_gb300 as ds
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    host = inputs.generate(wl)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    ws = ds.Workspace(0 if wl.head == "markov" else 1, wl.B, wl.gamma, wl.V, wl.r, wl.d)
+    stream = torch.cuda.current_stream()
+    B, G = wl.B, wl.gamma
+
+    def step(U, h, x0, out=None):
+        if wl.head == "markov":
+            return ds.markov_draft(dev["W1"], dev["W2"], U, x0, T=wl.T, seed=wl.seed, h=h,
+                                   w=dev["w"], target=dev.get("target"), workspace=ws, out=out)
+        return ds.rnn_draft(dev["W1"], dev["W2"], dev["Wj"], U, h, x0, T=wl.T, seed=wl.seed,
+                            w=dev["w"], target=dev.get("target"), workspace=ws, out=out)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    out = step(dev["U"], dev["h"], dev["x0"])
+    bufs = {"tokens": out.tokens, "lse": out.lse, "c": out.c, "S": out.S}
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(dev["U"], dev["h"], dev["x0"], out=bufs)
+    torch.cuda.synchronize()
+    assert ws.status() == 0, "draft kernel reported a device error during warm-up"
+
+    # ---- device-resident timing: CUDA events around each draft launch, L2 flushed between
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step(dev["U"], dev["h"], dev["x0"], out=bufs)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    times = [a.elapsed_time(b) for a, b in ev]   # ms per block
+    ms_step = sum(times) / len(times)
+    assert ws.status() == 0, "draft kernel reported a device error"
+
+    # ---- end to end through the public API: pinned host inputs in, results out, every step
+    hU = host["U"].pin_memory()
+    hh = host["h"].pin_memory()
+    hx = host["x0"].pin_memory()
+    dU, dh, dx = torch.empty_like(dev["U"]), torch.empty_like(dev["h"]), torch.empty_like(dev["x0"])
+    res = {k: torch.empty(B, G, dtype=torch.float32).pin_memory() for k in ("lse", "c", "S")}
+    res_tok = torch.empty(B, G, dtype=torch.int32).pin_memory()
+    h2d = hU.numel() * hU.element_size() + hh.numel() * hh.element_size() + hx.numel() * 4
+    d2h = res_tok.numel() * 4 + sum(v.numel() * 4 for v in res.values())
+    e2e_steps = min(args.steps, 500)
+    for _ in range(3):
+        dU.copy_(hU, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for i in range(e2e_steps):
+        flush.zero_()
+        e0.record(stream)
+        dU.copy_(hU, non_blocking=True)
+        dh.copy_(hh, non_blocking=True)
+        dx.copy_(hx, non_blocking=True)
+        o = step(dU, dh, dx, out=bufs)
+        res_tok.copy_(o.tokens, non_blocking=True)
+        res["lse"].copy_(o.lse, non_blocking=True)
+        res["c"].copy_(o.c, non_blocking=True)
+        res["S"].copy_(o.S, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_ms /= e2e_steps
+
+    # ---- max over ranks
+    if dist:
+        tt = torch.tensor([ms_step, e2e_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step, e2e_ms = tt.tolist()
+    value = world * B * G / (ms_step * 1e-3)
+    e2e_value = world * B * G / (e2e_ms * 1e-3)
+
+    if rank == 0:
+        peak, peak_kind = load_peaks()
+        alg = algorithmic_bytes(wl)
+        achieved = alg / (ms_step * 1e-3) / 1e9
+        src = os.path.join(ROOT, "semi_autoregressive_drafting_gb300", "csrc", "draft_cc.cu")
+        traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["source_sha"] == _sha(src) else None
+        launches = ds.draft_launches(0 if wl.head == "markov" else 1, B, wl.V, wl.r,
+                                     wl.dtype == "bf16")
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "B": B, "gamma": G, "V": wl.V, "r": wl.r, "d": wl.d,
+                       "T": wl.T, "l2": "flushed between timed blocks (512 MB write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                       "path": "cuda-core" if ds.draft_path(0, B, wl.V, wl.r) == 0 else "tcgen05"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_kind": f"{peak_kind} copy bandwidth",
+                         "algorithmic_bytes_per_launch": alg,
+                         "kernel": "draft_cc_kernel" if ds.draft_path(0, B, wl.V, wl.r) == 0
+                         else "draft_tc_kernel"},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": launches * args.steps,
+            "clocks": clk.summary(),
+            "wall_s": wall,
+            "ms_per_step_min": min(times), "ms_per_step_median": statistics.median(times),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(line))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+/*
+ * dspark.h -- C ABI of libdspark, the GB300 (sm_103a) draft-sampling hot path of DSpark
+ * (confidence-scheduled speculative decoding with semi-autoregressive generation).
+ *
+ * Sources cited below (page title, section / equation):
+ *   [P1] "DSpark -- paper verification": section 1 (Eqs 4-8), section 4 (delta table D7, D8).
+ *   [P2] "DSpark: 既要猜得连贯，也要把验证算力花在刀刃上": "设计" (Hardware-aware prefix scheduler).
+ *   [P3] "DSpark: Wait It's All Autoregressive?": "A parallel backbone with autoregressive
+ *        sampling", "How the Markov sampler works", "Training DSpark" (teacher forcing).
+ *   [P4] "Phase-Conditioned Speculative Decoding": section 3 (Eq 7, Eq 8, Theta = tau * SPS).
+ *
+ * Conventions shared by every call
+ *   - Pointers: every array argument is DEVICE memory owned by the caller, C-contiguous, and
+ *     16-byte aligned.  The library allocates nothing and keeps no per-call global state; the
+ *     only process-wide state is a per-device cache of SM count and occupancy.
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Calls are asynchronous: DSPARK_OK means "validated and enqueued".
+ *   - Errors: a host-detectable error returns at once with nothing enqueued.  CUDA launch
+ *     failures return DSPARK_ERR_CUDA; dspark_last_error() gives the text (thread-local).
+ *     Errors found on the device by the draft calls are written to a status word in the
+ *     workspace and read back with dspark_get_status().
+ *   - dtypes: `wdt` applies to the weights (W1, W2, w, Wj), `udt` to the activations (U, h).
+ *     DSPARK_BF16 arrays hold raw bfloat16; fp32 accumulation everywhere.
+ *   - Limits: 1 <= gamma <= 16, 2 <= V <= 2^24, r and d multiples of 8 (d may be 0 when the
+ *     confidence head is not used), 8 <= r <= 512, T finite and > 0.
+ *
+ * Layouts (row-major)
+ *   W1      [V][r]        embedding table of the sequential head (Eq 5 lookup)
+ *   W2      [V][r]        logit projection stored as a linear layer's weight: row v holds the
+ *                         r coefficients of vocab entry v, so B_k[v] = sum_j a_j * W2[v][j]
+ *   Wj      [3r][2r+d]    RNN joint projection, rows [gate; candidate; output], columns
+ *                         [s_{k-1}; W1[x_{k-1}]; h_k] (Eq 6, delta table D8); no bias
+ *   w       [d+r]         confidence weight: w[0:d] multiplies h_k, w[d:d+r] multiplies
+ *                         W1[x_{k-1}] (Eq 7); no bias
+ *   U       [B][gamma][V] base logits of the parallel backbone (Eq 4)
+ *   h       [B][gamma][d] backbone hidden states
+ *   target  [B][gamma][V] fp32 target-model logits (Eq 8), optional
+ *   x0      [B]           int32 anchor tokens (the target's last token)
+ *
+ * Sampling (a reading: the pages only say "sample left to right according to p_k")
+ *   p_k = softmax((U_k + B_k) / T).  x_k = argmax_v (y_v + g_v), y = (U_k + B_k) / T,
+ *   g_v = -ln(-ln u_v), ties to the smaller v.  u_v = (2*(bits >> 9) + 1) * 2^-24 where bits is
+ *   word (v mod 4) of Philox4x32-10 (Salmon et al., SC'11) with key (lo32(seed), hi32(seed))
+ *   and counter (floor(v/4), k-1, b, 0x44535052).  The same seed, shapes and inputs give the
+ *   same tokens on every run (no atomics decide a value; reductions run in a fixed order).
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSPARK_OK = 0,
+  DSPARK_ERR_INVALID = 1,     /* bad argument; on the device: a token or S out of range     */
+  DSPARK_ERR_WORKSPACE = 2,   /* workspace NULL, misaligned, or smaller than required        */
+  DSPARK_ERR_CUDA = 3,        /* a CUDA runtime call failed; see dspark_last_error()         */
+  DSPARK_ERR_TIMEOUT = 4,     /* a device-side wait between thread blocks ran out (device)   */
+  DSPARK_ERR_UNSUPPORTED = 5  /* valid arguments this build has no kernel for                */
+} dspark_status;
+
+typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
+
+typedef enum { DSPARK_HEAD_MARKOV = 0, DSPARK_HEAD_RNN = 1 } dspark_head;
+
+/*
+ * Bytes of workspace the draft calls need for this problem.  The workspace is caller-owned
+ * device memory, 256-byte aligned, that must be ZEROED ONCE before its first use; every
+ * successful call leaves it ready for the next call.  One workspace serves one call at a time:
+ * calls that share a workspace must be ordered (same stream, or events).  After a call whose
+ * device status is not DSPARK_OK, call dspark_get_status() before reusing the workspace.
+ * Returns 0 for arguments the draft calls would reject.
+ */
+size_t dspark_workspace_bytes(int head, int B, int gamma, int V, int r, int d);
+
+/*
+ * One semi-autoregressive draft block with the Markov head [P1 s1 Eq 4, Eq 5, Eq 7, Eq 8;
+ * P3 "A parallel backbone with autoregressive sampling"].  For every request b and
+ * k = 1..gamma, in one persistent launch:
+ *   e = W1[x_{k-1}] (x_0 = x0[b]);  B_k = e . W2^T;  z = U[b][k] + B_k;  y = z / T;
+ *   lse_k = log sum_v exp y_v;  x_k = Gumbel-max sample (see above);
+ *   c_k = sigmoid(w[0:d] . h[b][k] + w[d:] . e);  S_k = prod_{i<=k} c_i;
+ *   c*_k = clamp(1 - 1/2 || softmax(y) - softmax(target[b][k] / T) ||_1, 0, 1)  (Eq 8),
+ *   l1_k = || softmax(y) - softmax(target[b][k] / T) ||_1.
+ * W2 and U are streamed from HBM once per step.
+ *
+ *   forced   NULL: step k+1 conditions on the sampled x_k.  Otherwise [B][gamma] int32
+ *            teacher-forcing tokens: step k+1 conditions on forced[b][k-1] ([P3] "Training
+ *            DSpark"); tokens[] still receives each step's own sample.
+ *   h, w     both NULL: c and S are not computed (c, S must then be NULL).
+ *   target   NULL: cstar and l1 are not computed (cstar, l1 must then be NULL).
+ *   outputs  tokens, lse: [B][gamma] (required).  c, S, cstar, l1: [B][gamma] fp32 or NULL.
+ *            logits: [B][gamma][V] fp32 copy of z (debugging; NULL in production).
+ * Device-side errors: an anchor or forced token outside [0, V) sets DSPARK_ERR_INVALID; that
+ * request's tokens become -1 and its floats NaN, other requests are unaffected.  A wait
+ * between thread blocks that exceeds about one second sets DSPARK_ERR_TIMEOUT and the launch
+ * returns early.  Read either with dspark_get_status().
+ */
+dspark_status dspark_markov_draft(int B, int gamma, int V, int r, int d, float T, uint64_t seed,
+                                  dspark_dtype wdt, const void* W1, const void* W2,
+                                  const void* w, dspark_dtype udt, const void* U, const void* h,
+                                  const int32_t* x0, const int32_t* forced, const float* target,
+                                  int32_t* tokens, float* lse, float* c, float* S, float* cstar,
+                                  float* l1, float* logits, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
+ * The same block with the RNN head [P1 s1 Eq 6; delta table D8]:
+ *   z_k = [s_{k-1}; W1[x_{k-1}]; h_k],  (g; c; o) = Wj z_k split in three,
+ *   s_k = sigmoid(g) * s_{k-1} + (1 - sigmoid(g)) * tanh(c),  B_k = tanh(o) . W2^T.
+ * B_k is built from z_k, i.e. from s_{k-1}.  s0: [B][r] fp32 initial state or NULL for zeros.
+ * s_out: [B][r] fp32 final state s_gamma, or NULL.  Eq 7 is unchanged (uses W1[x_{k-1}]).
+ * h is required (it feeds Eq 6); w may be NULL (then c, S are NULL).  All other arguments,
+ * outputs and errors as dspark_markov_draft.
+ */
+dspark_status dspark_rnn_draft(int B, int gamma, int V, int r, int d, float T, uint64_t seed,
+                               dspark_dtype wdt, const void* W1, const void* W2, const void* w,
+                               const void* Wj, dspark_dtype udt, const void* U, const void* h,
+                               const int32_t* x0, const int32_t* forced, const float* target,
+                               const float* s0, int32_t* tokens, float* lse, float* c, float* S,
+                               float* cstar, float* l1, float* logits, float* s_out,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Teacher-forced confidence head [P1 s1 Eq 7; P4 s3]: for given tokens,
+ *   c_k = sigmoid(w[0:d] . h[b][k] + w[d:] . W1[x_{k-1}]),  S_k = prod_{i<=k} c_i,
+ * with x_0 = x0[b] and x_k = tokens[b][k-1].  Outputs c, S: [B][gamma] fp32.  A token outside
+ * [0, V) makes c and S NaN from that position on (no status word; no workspace needed).
+ */
+dspark_status dspark_confidence(int B, int gamma, int V, int r, int d, dspark_dtype wdt,
+                                const void* W1, const void* w, dspark_dtype udt, const void* h,
+                                const int32_t* x0, const int32_t* tokens, float* c, float* S,
+                                void* stream);
+
+/*
+ * Soft acceptance label on N independent rows [P1 s1 Eq 8, D7; P4 s3]:
+ *   l1 = || softmax(draft/T) - softmax(target/T) ||_1,  cstar = clamp(1 - l1/2, 0, 1),
+ * the acceptance probability of the standard speculative accept/reject rule.
+ * draft_logits, target_logits: [N][V] fp32.  cstar, l1: [N] fp32 (l1 may be NULL).
+ */
+dspark_status dspark_tv_label(int N, int V, float T, const float* draft_logits,
+                              const float* target_logits, float* cstar, float* l1, void* stream);
+
+/*
+ * Hardware-aware prefix scheduler [P2 "设计"; P4 s3 Theta = tau * SPS(B)].  Picks each
+ * request's verify length len[b] in 0..gamma to maximise
+ *   Theta = sps[n] * sum_b (1 + sum_{k <= len[b]} S[b][k]),  n = sum_b (len[b] + 1),
+ * over legal (contiguous-prefix) choices: steps/s at n verify tokens times expected tokens per
+ * step.  Ties go to fewer tokens.  S: [B][gamma] fp32 prefix survival (each row in [0, 1] and
+ * non-increasing); sps: [B*(gamma+1)+1] fp64 steps/s table indexed by n.  Outputs len [B] int32,
+ * theta [1] fp64.  Sums of S are exact (2^-32 fixed point); the result is bit-identical to the
+ * CPU reference.  B * gamma <= 16384.  Invalid S on the device: every len[b] = -1, theta NaN.
+ */
+dspark_status dspark_prefix_schedule(int B, int gamma, const float* S, const double* sps,
+                                     int32_t* len, double* theta, void* stream);
+
+/*
+ * Synchronises `stream`, returns the device status word of `workspace` (the most severe error
+ * any draft call recorded since the last read, DSPARK_OK if none) and resets the workspace so
+ * the next call starts clean.  DSPARK_ERR_CUDA if the synchronisation itself fails.
+ */
+dspark_status dspark_get_status(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Text of the last host-side error on the calling thread ("" if none). */
+const char* dspark_last_error(void);
+
+/*
+ * Which kernel path a draft call with these arguments takes: 0 = CUDA-core path (small B or
+ * fp32 weights), 1 = tensor-core (tcgen05) path.  Negative for arguments it would reject.
+ */
+int dspark_draft_path(int head, int B, int V, int r, dspark_dtype wdt);
+
+/* Number of kernel launches one draft call with these arguments makes on its stream. */
+int dspark_draft_launches(int head, int B, int V, int r, dspark_dtype wdt);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

@@ -1,0 +1,186 @@
+"""libdspark Python binding: DSpark's semi-autoregressive draft-sampling hot path on GB300.
+
+Every function here only marshals arguments: it checks dtypes and devices, allocates the
+output tensors with PyTorch (device memory is PyTorch's job) and calls the C ABI declared in
+``include/dspark.h``.  All arithmetic runs in the CUDA kernels of ``libdspark.so``; there is no
+fallback path, and a missing library raises.
+
+Names follow the pages: B requests, block size gamma, vocab V, Markov rank r, hidden size d,
+temperature T; W1 (embedding, [V][r]), W2 (logit projection stored [V][r]), w (confidence
+weight [d + r]), Wj (RNN joint projection [3r][2r + d]), U (base logits [B][gamma][V]),
+h (hidden states [B][gamma][d]), x0 (anchors [B]).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+
+__all__ = ["Workspace", "markov_draft", "rnn_draft", "confidence", "tv_label",
+           "prefix_schedule", "draft_path", "draft_launches", "DraftOutput"]
+
+_F32, _BF16 = 0, 1
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return _F32
+    if t.dtype == torch.bfloat16:
+        return _BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libdspark takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("libdspark takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class Workspace:
+    """Zero-initialised device scratch for the draft calls; reusable across calls of the same
+    or smaller shape, one call at a time (stream order)."""
+
+    def __init__(self, head: int, B: int, gamma: int, V: int, r: int, d: int, device=None):
+        lib = _lib.load()
+        n = lib.dspark_workspace_bytes(head, B, gamma, V, r, d)
+        if n == 0:
+            raise ValueError("invalid draft shape for a workspace")
+        self.nbytes = int(n)
+        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+
+    def status(self, stream=None) -> int:
+        """Synchronise and read (then clear) the device status word."""
+        return _lib.load().dspark_get_status(self.buf.data_ptr(), self.nbytes, _stream(stream))
+
+
+@dataclass
+class DraftOutput:
+    tokens: torch.Tensor          # [B, gamma] int32
+    lse: torch.Tensor             # [B, gamma] fp32, log-sum-exp of (U + B_k) / T
+    c: torch.Tensor | None        # [B, gamma] Eq 7 confidence
+    S: torch.Tensor | None        # [B, gamma] prefix survival
+    cstar: torch.Tensor | None    # [B, gamma] Eq 8 soft acceptance label
+    l1: torch.Tensor | None       # [B, gamma] ||p^d - p^t||_1
+    logits: torch.Tensor | None   # [B, gamma, V] z = U + B_k (debug)
+    s_out: torch.Tensor | None    # [B, r] final RNN state
+
+
+def _draft(head, W1, W2, U, x0, *, T, seed, h, w, Wj, target, forced, s0, want_logits,
+           workspace, stream, out=None):
+    lib = _lib.load()
+    B, gamma, V = U.shape
+    r = W1.shape[1]
+    d = h.shape[2] if h is not None else 0
+    dev = U.device
+    if workspace is None:
+        workspace = Workspace(head, B, gamma, V, r, d, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    o = out or {}
+    tokens = o.get("tokens") if o.get("tokens") is not None else torch.empty(B, gamma, dtype=torch.int32, device=dev)
+    lse = o.get("lse") if o.get("lse") is not None else torch.empty(B, gamma, **f32)
+    conf = h is not None and w is not None
+    c = (o.get("c") if o.get("c") is not None else torch.empty(B, gamma, **f32)) if conf else None
+    S = (o.get("S") if o.get("S") is not None else torch.empty(B, gamma, **f32)) if conf else None
+    cstar = torch.empty(B, gamma, **f32) if target is not None else None
+    l1 = torch.empty(B, gamma, **f32) if target is not None else None
+    logits = torch.empty(B, gamma, V, **f32) if want_logits else None
+    s_out = torch.empty(B, r, **f32) if head == 1 else None
+    if x0.dtype != torch.int32 or (forced is not None and forced.dtype != torch.int32):
+        raise TypeError("x0 and forced are int32")
+    if target is not None and target.dtype != torch.float32:
+        raise TypeError("target is float32")
+    wdt, udt = _dtype_code(W1), _dtype_code(U)
+    for t in (W2, w, Wj):
+        if t is not None and _dtype_code(t) != wdt:
+            raise TypeError("W1, W2, w and Wj share one dtype")
+    if h is not None and _dtype_code(h) != udt:
+        raise TypeError("U and h share one dtype")
+    common_in = [_ptr(x0), _ptr(forced), _ptr(target)]
+    outs = [_ptr(tokens), _ptr(lse), _ptr(c), _ptr(S), _ptr(cstar), _ptr(l1), _ptr(logits)]
+    ws = [workspace.buf.data_ptr(), workspace.nbytes, _stream(stream)]
+    if head == 0:
+        code = lib.dspark_markov_draft(B, gamma, V, r, d, float(T), int(seed), wdt, _ptr(W1),
+                                       _ptr(W2), _ptr(w), udt, _ptr(U), _ptr(h), *common_in,
+                                       *outs, *ws)
+        where = "dspark_markov_draft"
+    else:
+        code = lib.dspark_rnn_draft(B, gamma, V, r, d, float(T), int(seed), wdt, _ptr(W1),
+                                    _ptr(W2), _ptr(w), _ptr(Wj), udt, _ptr(U), _ptr(h),
+                                    *common_in, _ptr(s0), *outs, _ptr(s_out), *ws)
+        where = "dspark_rnn_draft"
+    _lib.check(code, where)
+    return DraftOutput(tokens, lse, c, S, cstar, l1, logits, s_out)
+
+
+def markov_draft(W1, W2, U, x0, *, T=1.0, seed=0, h=None, w=None, target=None, forced=None,
+                 want_logits=False, workspace=None, stream=None, out=None) -> DraftOutput:
+    """One draft block with the Markov head (Eq 5), sampling, Eq 7 confidence and S_k, and
+    the Eq 8 label when ``target`` is given.  See ``dspark_markov_draft``."""
+    return _draft(0, W1, W2, U, x0, T=T, seed=seed, h=h, w=w, Wj=None, target=target,
+                  forced=forced, s0=None, want_logits=want_logits, workspace=workspace,
+                  stream=stream, out=out)
+
+
+def rnn_draft(W1, W2, Wj, U, h, x0, *, T=1.0, seed=0, w=None, target=None, forced=None, s0=None,
+              want_logits=False, workspace=None, stream=None, out=None) -> DraftOutput:
+    """One draft block with the RNN head (Eq 6).  See ``dspark_rnn_draft``."""
+    return _draft(1, W1, W2, U, x0, T=T, seed=seed, h=h, w=w, Wj=Wj, target=target,
+                  forced=forced, s0=s0, want_logits=want_logits, workspace=workspace,
+                  stream=stream, out=out)
+
+
+def confidence(W1, w, h, x0, tokens, *, stream=None):
+    """Teacher-forced Eq 7 confidence and prefix survival for given tokens."""
+    lib = _lib.load()
+    B, gamma, d = h.shape
+    V, r = W1.shape
+    c = torch.empty(B, gamma, dtype=torch.float32, device=h.device)
+    S = torch.empty_like(c)
+    code = lib.dspark_confidence(B, gamma, V, r, d, _dtype_code(W1), _ptr(W1), _ptr(w),
+                                 _dtype_code(h), _ptr(h), _ptr(x0), _ptr(tokens), _ptr(c),
+                                 _ptr(S), _stream(stream))
+    _lib.check(code, "dspark_confidence")
+    return c, S
+
+
+def tv_label(draft_logits, target_logits, *, T=1.0, stream=None):
+    """Eq 8 soft acceptance label c* and the L1 distance on [N, V] fp32 logit rows."""
+    lib = _lib.load()
+    N, V = draft_logits.shape
+    cstar = torch.empty(N, dtype=torch.float32, device=draft_logits.device)
+    l1 = torch.empty_like(cstar)
+    code = lib.dspark_tv_label(N, V, float(T), _ptr(draft_logits), _ptr(target_logits),
+                               _ptr(cstar), _ptr(l1), _stream(stream))
+    _lib.check(code, "dspark_tv_label")
+    return cstar, l1
+
+
+def prefix_schedule(S, sps, *, stream=None):
+    """Per-request verify lengths maximising SPS(n) * expected accepted tokens."""
+    lib = _lib.load()
+    B, gamma = S.shape
+    ln = torch.empty(B, dtype=torch.int32, device=S.device)
+    theta = torch.empty(1, dtype=torch.float64, device=S.device)
+    code = lib.dspark_prefix_schedule(B, gamma, _ptr(S), _ptr(sps), _ptr(ln), _ptr(theta),
+                                      _stream(stream))
+    _lib.check(code, "dspark_prefix_schedule")
+    return ln, theta
+
+
+def draft_path(head: int, B: int, V: int, r: int, bf16: bool = True) -> int:
+    return _lib.load().dspark_draft_path(head, B, V, r, _BF16 if bf16 else _F32)
+
+
+def draft_launches(head: int, B: int, V: int, r: int, bf16: bool = True) -> int:
+    return _lib.load().dspark_draft_launches(head, B, V, r, _BF16 if bf16 else _F32)

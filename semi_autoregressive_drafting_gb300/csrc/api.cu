@@ -1,0 +1,317 @@
+// api.cu -- the C ABI of libdspark (declared in include/dspark.h): argument validation,
+// workspace layout, kernel-path selection and stream-ordered launches.  No torch types, no
+// allocation; the only process-wide state is a per-device cache of SM count and shared-memory
+// limit (filled once, under a mutex).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "dspark.h"
+#include "draft.cuh"
+#include "kernels.h"
+
+using namespace dspark;
+
+namespace {
+
+thread_local std::string g_err;
+
+dspark_status fail(dspark_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+dspark_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(DSPARK_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DevInfo {
+  bool init = false;
+  int sms = 0;
+  int smem_optin = 0;
+};
+std::mutex g_mu;
+DevInfo g_dev[64];
+
+bool dev_info(DevInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return false;
+    if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaSuccess)
+      return false;
+    d.init = true;
+  }
+  *out = d;
+  return true;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+struct WsLayout {
+  size_t keys, ml, mlt, l1p, rnn_s, rnn_a, rnn_gh, total;
+};
+
+WsLayout ws_layout(int head, int B, int G, int r, int nCTA) {
+  WsLayout L;
+  size_t off = sizeof(WsHeader);
+  L.keys = off;
+  off = align256(off + (size_t)G * B * 8);
+  L.ml = off;
+  off = align256(off + (size_t)G * B * nCTA * 8);
+  L.mlt = off;
+  off = align256(off + (size_t)G * B * nCTA * 8);
+  L.l1p = off;
+  off = align256(off + (size_t)G * B * nCTA * 4);
+  L.rnn_s = off;
+  off = align256(off + (head == 1 ? (size_t)2 * B * r * 4 : 0));
+  L.rnn_a = off;
+  off = align256(off + (head == 1 ? (size_t)B * r * 4 : 0));
+  L.rnn_gh = off;
+  off = align256(off + (head == 1 ? (size_t)B * G * 3 * r * 4 : 0));
+  L.total = off;
+  return L;
+}
+
+bool shape_ok(int head, int B, int G, int V, int r, int d) {
+  return (head == 0 || head == 1) && B >= 1 && G >= 1 && G <= 16 && V >= 2 && V <= (1 << 24) &&
+         r >= 8 && r <= 512 && r % 8 == 0 && d >= 0 && d % 8 == 0 && B <= (1 << 20);
+}
+
+int path_of(int head, int B, int r, int w_bf16) {
+  (void)head;
+  if (draft_cc_supported(B, r, w_bf16)) return 0;
+  return -1;  // tensor-core path: not in this build yet
+}
+
+struct DraftArgs {
+  int head, B, G, V, r, d;
+  float T;
+  uint64_t seed;
+  dspark_dtype wdt, udt;
+  const void *W1, *W2, *w, *Wj, *U, *h;
+  const int32_t *x0, *forced;
+  const float *target, *s0;
+  int32_t* tokens;
+  float *lse, *c, *S, *cstar, *l1, *logits, *s_out;
+  void* ws;
+  size_t ws_bytes;
+  void* stream;
+};
+
+dspark_status run_draft(const DraftArgs& a) {
+  g_err.clear();
+  if (!shape_ok(a.head, a.B, a.G, a.V, a.r, a.d))
+    return fail(DSPARK_ERR_INVALID, "bad shape B=%d gamma=%d V=%d r=%d d=%d", a.B, a.G, a.V, a.r,
+                a.d);
+  if (!(a.T > 0.f) || !std::isfinite(a.T)) return fail(DSPARK_ERR_INVALID, "T must be finite and > 0");
+  if ((a.wdt != DSPARK_F32 && a.wdt != DSPARK_BF16) || (a.udt != DSPARK_F32 && a.udt != DSPARK_BF16))
+    return fail(DSPARK_ERR_INVALID, "unknown dtype");
+  if (!a.W1 || !a.W2 || !a.U || !a.x0 || !a.tokens || !a.lse)
+    return fail(DSPARK_ERR_INVALID, "W1, W2, U, x0, tokens and lse are required");
+  if (!aligned(a.W1, 16) || !aligned(a.W2, 16) || !aligned(a.U, 16) ||
+      (a.target && !aligned(a.target, 16)) || (a.h && !aligned(a.h, 16)) ||
+      (a.Wj && !aligned(a.Wj, 16)))
+    return fail(DSPARK_ERR_INVALID, "W1, W2, U, h, Wj and target must be 16-byte aligned");
+  const bool conf = a.h && a.w;
+  if (a.head == 0 && ((a.h != nullptr) != (a.w != nullptr)))
+    return fail(DSPARK_ERR_INVALID, "h and w go together for the Markov head");
+  if (a.head == 1 && (!a.Wj || !a.h)) return fail(DSPARK_ERR_INVALID, "the RNN head needs Wj and h");
+  if (conf && a.d == 0) return fail(DSPARK_ERR_INVALID, "confidence needs d > 0");
+  if ((a.c != nullptr) != conf || (a.S != nullptr) != conf)
+    return fail(DSPARK_ERR_INVALID, "c and S are given exactly when h and w are");
+  if ((a.cstar != nullptr) != (a.target != nullptr) || (a.l1 != nullptr) != (a.target != nullptr))
+    return fail(DSPARK_ERR_INVALID, "cstar and l1 are given exactly when target is");
+  DevInfo di;
+  if (!dev_info(&di)) return fail(DSPARK_ERR_CUDA, "cannot query the current device");
+  const int nCTA = di.sms;
+  const WsLayout L = ws_layout(a.head, a.B, a.G, a.r, nCTA);
+  if (!a.ws || !aligned(a.ws, 256) || a.ws_bytes < L.total)
+    return fail(DSPARK_ERR_WORKSPACE, "workspace must be 256-byte aligned and >= %zu bytes", L.total);
+  const int w_bf16 = a.wdt == DSPARK_BF16, u_bf16 = a.udt == DSPARK_BF16;
+  const int path = path_of(a.head, a.B, a.r, w_bf16);
+  if (path < 0 || a.head == 1)
+    return fail(DSPARK_ERR_UNSUPPORTED, "no kernel for head=%d B=%d r=%d in this build", a.head,
+                a.B, a.r);
+
+  DraftParams p;
+  std::memset(&p, 0, sizeof p);
+  p.head = a.head;
+  p.B = a.B;
+  p.gamma = a.G;
+  p.V = a.V;
+  p.r = a.r;
+  p.d = a.d;
+  p.invT = 1.f / a.T;
+  p.seed_lo = (uint32_t)(a.seed & 0xFFFFFFFFu);
+  p.seed_hi = (uint32_t)(a.seed >> 32);
+  p.w_bf16 = w_bf16;
+  p.u_bf16 = u_bf16;
+  p.W1 = a.W1;
+  p.W2 = a.W2;
+  p.w = a.w;
+  p.Wj = a.Wj;
+  p.U = a.U;
+  p.h = a.h;
+  p.x0 = a.x0;
+  p.forced = a.forced;
+  p.target = a.target;
+  p.s0 = a.s0;
+  p.tokens = a.tokens;
+  p.lse = a.lse;
+  p.c = a.c;
+  p.S = a.S;
+  p.cstar = a.cstar;
+  p.l1 = a.l1;
+  p.logits = a.logits;
+  p.s_out = a.s_out;
+  uint8_t* ws = (uint8_t*)a.ws;
+  p.hdr = (WsHeader*)ws;
+  p.keys = (unsigned long long*)(ws + L.keys);
+  p.ml = (float2*)(ws + L.ml);
+  p.mlt = (float2*)(ws + L.mlt);
+  p.l1p = (float*)(ws + L.l1p);
+  p.rnn_s = (float*)(ws + L.rnn_s);
+  p.rnn_a = (float*)(ws + L.rnn_a);
+  p.rnn_gh = (float*)(ws + L.rnn_gh);
+
+  const int units = (a.V + 7) / 8;
+  p.slice_max = ((units + nCTA - 1) / nCTA) * 8;
+  const int ues = u_bf16 ? 2 : 4;
+  p.u_bulk = ((size_t)a.V * ues) % 16 == 0 && (!a.target || ((size_t)a.V * 4) % 16 == 0);
+  cudaStream_t stream = (cudaStream_t)a.stream;
+
+  if (path == 0) {
+    const int row_bytes = a.r * (w_bf16 ? 2 : 4);
+    p.rows_per_stage = (16384 / row_bytes) / 4 * 4;
+    p.nstages = 2;
+    const size_t base = draft_cc_smem_bytes(p) - 2 * 16384;
+    const size_t avail = (size_t)di.smem_optin > base ? di.smem_optin - base : 0;
+    p.nstages = (int)std::min<size_t>(16, avail / 16384);
+    if (p.nstages < 2) return fail(DSPARK_ERR_UNSUPPORTED, "vocab slice too large for shared memory");
+    p.smem_bytes = draft_cc_smem_bytes(p);
+    cudaError_t e = launch_draft_cc(p, nCTA, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "draft_cc launch");
+  }
+  return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dspark_workspace_bytes(int head, int B, int gamma, int V, int r, int d) {
+  if (!shape_ok(head, B, gamma, V, r, d)) return 0;
+  DevInfo di;
+  if (!dev_info(&di)) return 0;
+  return ws_layout(head, B, gamma, r, di.sms).total;
+}
+
+dspark_status dspark_markov_draft(int B, int gamma, int V, int r, int d, float T, uint64_t seed,
+                                  dspark_dtype wdt, const void* W1, const void* W2,
+                                  const void* w, dspark_dtype udt, const void* U, const void* h,
+                                  const int32_t* x0, const int32_t* forced, const float* target,
+                                  int32_t* tokens, float* lse, float* c, float* S, float* cstar,
+                                  float* l1, float* logits, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  DraftArgs a{0,       B,      gamma,  V,      r,      d,     T,     seed,    wdt,
+              udt,     W1,     W2,     w,      nullptr, U,    h,     x0,      forced,
+              target,  nullptr, tokens, lse,   c,      S,     cstar, l1,      logits,
+              nullptr, workspace, workspace_bytes, stream};
+  return run_draft(a);
+}
+
+dspark_status dspark_rnn_draft(int B, int gamma, int V, int r, int d, float T, uint64_t seed,
+                               dspark_dtype wdt, const void* W1, const void* W2, const void* w,
+                               const void* Wj, dspark_dtype udt, const void* U, const void* h,
+                               const int32_t* x0, const int32_t* forced, const float* target,
+                               const float* s0, int32_t* tokens, float* lse, float* c, float* S,
+                               float* cstar, float* l1, float* logits, float* s_out,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  DraftArgs a{1,      B,     gamma,  V,     r,     d,     T,      seed,      wdt,
+              udt,    W1,    W2,     w,     Wj,    U,     h,      x0,        forced,
+              target, s0,    tokens, lse,   c,     S,     cstar,  l1,        logits,
+              s_out,  workspace, workspace_bytes, stream};
+  return run_draft(a);
+}
+
+dspark_status dspark_confidence(int B, int gamma, int V, int r, int d, dspark_dtype wdt,
+                                const void* W1, const void* w, dspark_dtype udt, const void* h,
+                                const int32_t* x0, const int32_t* tokens, float* c, float* S,
+                                void* stream) {
+  g_err.clear();
+  if (!shape_ok(0, B, gamma, V, r, d) || d == 0)
+    return fail(DSPARK_ERR_INVALID, "bad shape B=%d gamma=%d V=%d r=%d d=%d", B, gamma, V, r, d);
+  if (!W1 || !w || !h || !x0 || !tokens || !c || !S)
+    return fail(DSPARK_ERR_INVALID, "all arrays are required");
+  cudaError_t e = launch_confidence(B, gamma, V, r, d, wdt == DSPARK_BF16, W1, w,
+                                    udt == DSPARK_BF16, h, x0, tokens, c, S, (cudaStream_t)stream);
+  return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "confidence launch");
+}
+
+dspark_status dspark_tv_label(int N, int V, float T, const float* draft_logits,
+                              const float* target_logits, float* cstar, float* l1, void* stream) {
+  g_err.clear();
+  if (N < 1 || V < 2 || !(T > 0.f) || !std::isfinite(T))
+    return fail(DSPARK_ERR_INVALID, "bad arguments N=%d V=%d", N, V);
+  if (!draft_logits || !target_logits || !cstar)
+    return fail(DSPARK_ERR_INVALID, "draft_logits, target_logits and cstar are required");
+  cudaError_t e = launch_tv_label(N, V, T, draft_logits, target_logits, cstar, l1,
+                                  (cudaStream_t)stream);
+  return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "tv_label launch");
+}
+
+dspark_status dspark_prefix_schedule(int B, int gamma, const float* S, const double* sps,
+                                     int32_t* len, double* theta, void* stream) {
+  g_err.clear();
+  if (B < 1 || gamma < 1 || gamma > 16 || (long long)B * gamma > 16384)
+    return fail(DSPARK_ERR_INVALID, "need 1 <= gamma <= 16 and B * gamma <= 16384");
+  if (!S || !sps || !len || !theta) return fail(DSPARK_ERR_INVALID, "all arrays are required");
+  cudaError_t e = launch_prefix_schedule(B, gamma, S, sps, len, theta, (cudaStream_t)stream);
+  return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "prefix_schedule launch");
+}
+
+dspark_status dspark_get_status(void* workspace, size_t workspace_bytes, void* stream) {
+  g_err.clear();
+  if (!workspace || workspace_bytes < sizeof(WsHeader))
+    return fail(DSPARK_ERR_WORKSPACE, "workspace missing or too small");
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  unsigned st = 0;
+  e = cudaMemcpy(&st, workspace, sizeof st, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (st != 0) {
+    e = cudaMemset(workspace, 0, workspace_bytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "workspace reset");
+  }
+  return (dspark_status)st;
+}
+
+const char* dspark_last_error(void) { return g_err.c_str(); }
+
+int dspark_draft_path(int head, int B, int V, int r, dspark_dtype wdt) {
+  if (!shape_ok(head, B, 1, V, r, 0)) return -1;
+  return path_of(head, B, r, wdt == DSPARK_BF16);
+}
+
+int dspark_draft_launches(int head, int B, int V, int r, dspark_dtype wdt) {
+  const int p = dspark_draft_path(head, B, V, r, wdt);
+  if (p < 0) return -1;
+  return 1;
+}
+
+}  // extern "C"

@@ -1,0 +1,256 @@
+// aux_kernels.cu -- the three per-round kernels that sit beside the draft loop:
+//   confidence_kernel  teacher-forced Eq 7 and prefix survival S_k = prod c_i
+//                      ("DSpark -- paper verification", section 1, Eq 7, section 3.2.1)
+//   tv_label_kernel    Eq 8: c* = 1 - 1/2 ||softmax(d/T) - softmax(t/T)||_1, clamped
+//                      ("Phase-Conditioned Speculative Decoding", section 3: c* = 1 - TV)
+//   schedule_kernel    the hardware-aware prefix scheduler: per-request verify lengths that
+//                      maximise SPS(n) * expected accepted tokens over legal prefixes
+//                      ("DSpark: 既要猜得连贯..." design section; same page-4 section, Theta)
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dspark {
+namespace {
+
+__device__ __forceinline__ float ldv(const void* p, size_t i, int bf16) {
+  return bf16 ? __bfloat162float(((const __nv_bfloat16*)p)[i]) : ((const float*)p)[i];
+}
+
+// One warp per (request, position): logit = w[0:d].h + w[d:].W1[x_{k-1}]; a second pass turns
+// the logits of a request into c and the running product S.
+__global__ void confidence_logits_kernel(int B, int G, int V, int r, int d, int w_bf16,
+                                         const void* W1, const void* w, int u_bf16, const void* h,
+                                         const int32_t* x0, const int32_t* tokens, float* c) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= B * G) return;
+  const int b = warp / G, k = warp % G;
+  const int prev = k == 0 ? x0[b] : tokens[(size_t)b * G + k - 1];
+  if (prev < 0 || prev >= V) {
+    if (lane == 0) c[warp] = NAN;
+    return;
+  }
+  float acc = 0.f;
+  for (int j = lane; j < d; j += 32) acc += ldv(w, j, w_bf16) * ldv(h, (size_t)warp * d + j, u_bf16);
+  for (int j = lane; j < r; j += 32)
+    acc += ldv(w, (size_t)d + j, w_bf16) * ldv(W1, (size_t)prev * r + j, w_bf16);
+  acc = warp_sum(acc);
+  if (lane == 0) c[warp] = acc;  // logit for now
+}
+
+__global__ void confidence_finish_kernel(int B, int G, float* c, float* S) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  float s = 1.f;
+  bool bad = false;
+  for (int k = 0; k < G; ++k) {
+    const size_t o = (size_t)b * G + k;
+    const float logit = c[o];
+    bad = bad || isnan(logit);
+    const float cv = bad ? NAN : sigmoidf_acc(logit);
+    s = bad ? NAN : s * cv;
+    c[o] = cv;
+    S[o] = s;
+  }
+}
+
+// Eq 8 for one row per block: pass 1 online (max, sum-exp) of both rows, pass 2 the L1 sum.
+__global__ void __launch_bounds__(512) tv_label_kernel(int V, float invT, const float* dl,
+                                                       const float* tl, float* cstar, float* l1) {
+  __shared__ float sm[4][16];
+  const size_t base = (size_t)blockIdx.x * V;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  float md = -INFINITY, ld = 0.f, mt = -INFINITY, lt = 0.f;
+  for (int v = tid; v < V; v += blockDim.x) {
+    lse_push(md, ld, dl[base + v] * invT);
+    lse_push(mt, lt, tl[base + v] * invT);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lse_merge(md, ld, __shfl_xor_sync(~0u, md, o), __shfl_xor_sync(~0u, ld, o));
+    lse_merge(mt, lt, __shfl_xor_sync(~0u, mt, o), __shfl_xor_sync(~0u, lt, o));
+  }
+  if (lane == 0) {
+    sm[0][warp] = md;
+    sm[1][warp] = ld;
+    sm[2][warp] = mt;
+    sm[3][warp] = lt;
+  }
+  __syncthreads();
+  md = -INFINITY, ld = 0.f, mt = -INFINITY, lt = 0.f;
+  for (int w = 0; w < nw; ++w) {
+    lse_merge(md, ld, sm[0][w], sm[1][w]);
+    lse_merge(mt, lt, sm[2][w], sm[3][w]);
+  }
+  const float Ld = md + logf(ld), Lt = mt + logf(lt);
+  __syncthreads();
+  float acc = 0.f;
+  for (int v = tid; v < V; v += blockDim.x)
+    acc += fabsf(__expf(dl[base + v] * invT - Ld) - __expf(tl[base + v] * invT - Lt));
+  acc = warp_sum(acc);
+  if (lane == 0) sm[0][warp] = acc;
+  __syncthreads();
+  if (tid == 0) {
+    float s = 0.f;
+    for (int w = 0; w < nw; ++w) s += sm[0][w];
+    if (l1) l1[blockIdx.x] = s;
+    cstar[blockIdx.x] = fminf(1.f, fmaxf(0.f, 1.f - 0.5f * s));
+  }
+}
+
+// Prefix scheduler, one block.  Keys rank every (b, k) by S descending, then k, then b:
+//   key = ((~bits(S)) << 32) | (k << 24) | b   sorted ascending (S >= 0, so bits order S).
+// Because each S row is non-increasing, every top-m set is a union of per-request prefixes
+// and the top-m sum is the best legal sum with B + m verify tokens.  The sums are exact
+// (floor(S 2^32) added as integers), so Theta(m) = sps[B + m] * (B + sum 2^-32) is a single
+// IEEE double multiply and the argmax (smallest m on ties) is reproducible bit for bit.
+constexpr int kSchedThreads = 1024;
+
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(int B, int G, int M, int Mp2,
+                                                                 const float* S, const double* sps,
+                                                                 int32_t* len, double* theta) {
+  extern __shared__ __align__(16) unsigned long long keys[];  // [Mp2] then scan scratch
+  unsigned long long* csum = keys + Mp2;                       // [kSchedThreads] block sums
+  __shared__ int bad;
+  __shared__ double best_val[32];
+  __shared__ int best_m[32];
+  const int tid = threadIdx.x;
+  if (tid == 0) bad = 0;
+  __syncthreads();
+  for (int i = tid; i < Mp2; i += kSchedThreads) {
+    if (i < M) {
+      const float s = S[i];
+      const int b = i / G, k = i - b * G;
+      const bool ok = s >= 0.f && s <= 1.f && (k == 0 || s <= S[i - 1]);
+      if (!ok) bad = 1;
+      keys[i] = ((unsigned long long)(~__float_as_uint(s)) << 32) |
+                ((unsigned long long)k << 24) | (unsigned long long)b;
+    } else {
+      keys[i] = ~0ull;  // padding sorts last
+    }
+  }
+  __syncthreads();
+  if (bad) {
+    for (int b = tid; b < B; b += kSchedThreads) len[b] = -1;
+    if (tid == 0) *theta = __longlong_as_double(0x7ff8000000000000ll);
+    return;
+  }
+  // bitonic sort, ascending
+  for (int size = 2; size <= Mp2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < Mp2 / 2; i += kSchedThreads) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const unsigned long long a = keys[lo], c = keys[hi];
+        if ((a > c) == up) {
+          keys[lo] = c;
+          keys[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // fixed-point values of the sorted S, inclusive prefix sums (chunk per thread)
+  const int chunk = (M + kSchedThreads - 1) / kSchedThreads;
+  const int c0 = min(M, tid * chunk), c1 = min(M, c0 + chunk);
+  unsigned long long run = 0;
+  for (int i = c0; i < c1; ++i) {
+    const float s = __uint_as_float(~(uint32_t)(keys[i] >> 32));
+    run += (unsigned long long)floor((double)s * 4294967296.0);
+  }
+  csum[tid] = run;
+  __syncthreads();
+  if (tid == 0) {
+    unsigned long long acc = 0;
+    for (int t = 0; t < kSchedThreads; ++t) {
+      const unsigned long long v = csum[t];
+      csum[t] = acc;  // exclusive prefix of chunk sums
+      acc += v;
+    }
+  }
+  __syncthreads();
+  // Theta(m) for this thread's m values; m = i + 1 covers the first i + 1 sorted entries
+  double bv = -1.0;
+  int bm = 0x7fffffff;
+  if (tid == 0) {
+    bv = sps[B] * (double)B;  // m = 0
+    bm = 0;
+  }
+  run = csum[tid];
+  for (int i = c0; i < c1; ++i) {
+    const float s = __uint_as_float(~(uint32_t)(keys[i] >> 32));
+    run += (unsigned long long)floor((double)s * 4294967296.0);
+    const double tau = (double)B + (double)run / 4294967296.0;
+    const double th = __dmul_rn(sps[B + i + 1], tau);
+    if (th > bv) {
+      bv = th;
+      bm = i + 1;
+    }
+  }
+  // block argmax, smallest m on ties
+  for (int o = 16; o > 0; o >>= 1) {
+    const double v2 = __shfl_xor_sync(~0u, bv, o);
+    const int m2 = __shfl_xor_sync(~0u, bm, o);
+    if (v2 > bv || (v2 == bv && m2 < bm)) {
+      bv = v2;
+      bm = m2;
+    }
+  }
+  if ((tid & 31) == 0) {
+    best_val[tid >> 5] = bv;
+    best_m[tid >> 5] = bm;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    double v = best_val[0];
+    int m = best_m[0];
+    for (int w = 1; w < kSchedThreads / 32; ++w)
+      if (best_val[w] > v || (best_val[w] == v && best_m[w] < m)) {
+        v = best_val[w];
+        m = best_m[w];
+      }
+    best_val[0] = v;
+    best_m[0] = m;
+    *theta = v;
+  }
+  __syncthreads();
+  const int mstar = best_m[0];
+  for (int b = tid; b < B; b += kSchedThreads) len[b] = 0;
+  __syncthreads();
+  for (int i = tid; i < mstar; i += kSchedThreads) atomicAdd(&len[(int)(keys[i] & 0xFFFFFFu)], 1);
+}
+
+}  // namespace
+
+cudaError_t launch_confidence(int B, int G, int V, int r, int d, int w_bf16, const void* W1,
+                              const void* w, int u_bf16, const void* h, const int32_t* x0,
+                              const int32_t* tokens, float* c, float* S, cudaStream_t stream) {
+  const int warps = B * G;
+  confidence_logits_kernel<<<(warps + 7) / 8, 256, 0, stream>>>(B, G, V, r, d, w_bf16, W1, w,
+                                                                 u_bf16, h, x0, tokens, c);
+  confidence_finish_kernel<<<(B + 127) / 128, 128, 0, stream>>>(B, G, c, S);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tv_label(int N, int V, float T, const float* d, const float* t, float* cstar,
+                            float* l1, cudaStream_t stream) {
+  tv_label_kernel<<<N, 512, 0, stream>>>(V, 1.f / T, d, t, cstar, l1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefix_schedule(int B, int G, const float* S, const double* sps, int32_t* len,
+                                   double* theta, cudaStream_t stream) {
+  const int M = B * G;
+  int Mp2 = 2;
+  while (Mp2 < M) Mp2 <<= 1;
+  const size_t smem = (size_t)(Mp2 + kSchedThreads) * 8;
+  cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  schedule_kernel<<<1, kSchedThreads, smem, stream>>>(B, G, M, Mp2, S, sps, len, theta);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

@@ -1,0 +1,61 @@
+// draft.cuh -- parameters and host-side launch interface of the persistent draft kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace dspark {
+
+struct DraftParams {
+  // problem
+  int head;  // 0 Markov, 1 RNN
+  int B, gamma, V, r, d;
+  float invT;
+  uint32_t seed_lo, seed_hi;
+  int w_bf16, u_bf16;  // dtype flags (weights / activations)
+  // inputs
+  const void* W1;
+  const void* W2;
+  const void* w;   // may be null
+  const void* Wj;  // RNN only
+  const void* U;
+  const void* h;   // may be null (Markov without confidence)
+  const int32_t* x0;
+  const int32_t* forced;  // may be null
+  const float* target;    // may be null
+  const float* s0;        // RNN, may be null
+  // outputs
+  int32_t* tokens;
+  float* lse;
+  float* c;
+  float* S;
+  float* cstar;
+  float* l1;
+  float* logits;
+  float* s_out;
+  // workspace
+  WsHeader* hdr;
+  unsigned long long* keys;  // [gamma][B]
+  float2* ml;                // [gamma][B][nCTA] (max, sum exp) of y per block
+  float2* mlt;               // [gamma][B][nCTA] same for the target
+  float* l1p;                // [gamma][B][nCTA] partial L1 distances
+  float* rnn_s;              // [2][B][r] RNN state ping-pong
+  float* rnn_a;              // [B][r] RNN conditioning vector tanh(o) for the current step
+  float* rnn_gh;             // [B][gamma][3r] RNN h-part of the joint projection
+  // launch geometry (set by the host)
+  int rows_per_stage;  // W2 rows per ring stage
+  int nstages;         // ring depth
+  int slice_max;       // largest vocab slice of any block (multiple of 8)
+  int u_bulk;          // 1: U/target rows are 16-byte aligned and copied with TMA bulk copies
+  size_t smem_bytes;
+};
+
+// Host launchers (defined in the .cu files).  Return a cudaError_t.
+cudaError_t launch_draft_cc(DraftParams& p, int nblocks, cudaStream_t stream);
+size_t draft_cc_smem_bytes(const DraftParams& p);
+int draft_cc_supported(int B, int r, int w_bf16);
+
+}  // namespace dspark

@@ -1,0 +1,17 @@
+// kernels.h -- host launchers of the libdspark kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dspark {
+
+cudaError_t launch_confidence(int B, int G, int V, int r, int d, int w_bf16, const void* W1,
+                              const void* w, int u_bf16, const void* h, const int32_t* x0,
+                              const int32_t* tokens, float* c, float* S, cudaStream_t stream);
+cudaError_t launch_tv_label(int N, int V, float T, const float* d, const float* t, float* cstar,
+                            float* l1, cudaStream_t stream);
+cudaError_t launch_prefix_schedule(int B, int G, const float* S, const double* sps, int32_t* len,
+                                   double* theta, cudaStream_t stream);
+
+}  // namespace dspark

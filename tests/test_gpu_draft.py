@@ -1,0 +1,120 @@
+"""GPU parity of the draft calls against the fp64 oracle, through the C ABI.
+
+Each case runs the library free-running and teacher-forced on the oracle's tokens, checks
+tokens bit-exact up to counted near-ties, and every float output within 2e-3 absolute.
+Cases span several vocab slices per block and a ragged tail, both dtypes, the degenerate
+shapes (B = 1, gamma = 1, vocab smaller than the grid's slices), the 16-byte-misaligned U
+row path, forced tokens, a target for Eq 8, and the full latency-regime workload.
+"""
+import numpy as np
+import pytest
+import torch
+
+import semi_autoregressive_drafting_gb300 as ds
+from semi_autoregressive_drafting_gb300 import inputs
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+TINY = inputs.WORKLOADS["tiny_markov"]
+
+
+def _run_case(wl, *, target_noise=None, want_logits=True, rows=None, check_free=True):
+    if target_noise is not None:
+        wl = wl.with_(target_noise=target_noise)
+    t = inputs.generate(wl)
+    d = parity.to_dev(t)
+    o = parity.oracle_draft(wl, t, rows=rows, want_z=want_logits)
+    assert o.status == 0
+    ws = ds.Workspace(0, wl.B, wl.gamma, wl.V, wl.r, wl.d)
+    kw = dict(T=wl.T, seed=wl.seed, h=d["h"], w=d["w"], target=d.get("target"), workspace=ws)
+    sel = (lambda a: a) if rows is None else (lambda a: a[rows])
+    ties = 0
+    if check_free:
+        free = ds.markov_draft(d["W1"], d["W2"], d["U"], d["x0"], **kw)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
+        ties += parity.check_tokens_free(sel(free.tokens.cpu().numpy()), o)
+    forced = np.zeros((wl.B, wl.gamma), np.int32)
+    forced[rows if rows is not None else slice(None)] = o.tokens
+    tf = ds.markov_draft(d["W1"], d["W2"], d["U"], d["x0"], forced=torch.from_numpy(forced).cuda(),
+                         want_logits=want_logits, **kw)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    ties += parity.check_tokens_forced(sel(tf.tokens.cpu().numpy()), o)
+    errs = parity.compare_floats(tf, o, rows=rows, logits=want_logits)
+    print(f"{wl.name} B={wl.B} V={wl.V}: near-ties {ties}, max errors {errs}")
+    return ties, errs
+
+
+def test_tiny_markov_workload():
+    _run_case(TINY)
+
+
+@pytest.mark.parametrize("B", [1, 2, 3])
+def test_tiny_batches(B):
+    _run_case(TINY.with_(B=B, seed=10 + B))
+
+
+@pytest.mark.parametrize("gamma", [1, 16])
+def test_block_sizes(gamma):
+    _run_case(TINY.with_(gamma=gamma, seed=20 + gamma))
+
+
+def test_temperature_and_target_fp32():
+    _run_case(TINY.with_(T=0.7, seed=31), target_noise=1.0)
+
+
+def test_ragged_vocab_unaligned_rows():
+    # V * 4 bytes is not a multiple of 16: U rows are fetched with plain loads
+    _run_case(TINY.with_(V=1001, seed=32), target_noise=0.5)
+
+
+def test_vocab_smaller_than_grid():
+    # most blocks own an empty slice
+    _run_case(TINY.with_(V=40, B=2, seed=33), target_noise=1.0)
+
+
+def test_bf16_small_with_target():
+    wl = inputs.WORKLOADS["qwen3_4b_markov"].with_(V=20008, d=512, B=3, seed=34)
+    _run_case(wl, target_noise=1.0)
+
+
+def test_bf16_rank_512():
+    wl = inputs.WORKLOADS["qwen3_4b_markov"].with_(V=12000, r=512, d=64, B=2, seed=35)
+    _run_case(wl)
+
+
+@pytest.mark.slow
+def test_qwen3_4b_markov_full():
+    ties, _ = _run_case(inputs.WORKLOADS["qwen3_4b_markov"], want_logits=False)
+    assert ties <= 1
+
+
+def test_invalid_anchor_sets_status():
+    wl = TINY.with_(seed=40)
+    t = parity.to_dev(inputs.generate(wl))
+    x0 = t["x0"].clone()
+    x0[1] = wl.V
+    ws = ds.Workspace(0, wl.B, wl.gamma, wl.V, wl.r, wl.d)
+    out = ds.markov_draft(t["W1"], t["W2"], t["U"], x0, h=t["h"], w=t["w"], seed=wl.seed,
+                          workspace=ws)
+    assert ws.status() == 1                      # DSPARK_ERR_INVALID, then reset
+    tok = out.tokens.cpu().numpy()
+    assert np.all(tok[1] == -1) and np.all(tok[[0, 2, 3]] >= 0)
+    assert np.all(np.isnan(out.c.cpu().numpy()[1]))
+    # the workspace is clean again: the next call succeeds
+    out2 = ds.markov_draft(t["W1"], t["W2"], t["U"], t["x0"], seed=wl.seed, workspace=ws)
+    assert ws.status() == 0 and np.all(out2.tokens.cpu().numpy() >= 0)
+
+
+def test_repeat_runs_are_bit_identical():
+    wl = inputs.WORKLOADS["qwen3_4b_markov"].with_(V=50000, d=256, B=4, seed=41)
+    t = parity.to_dev(inputs.generate(wl.with_(target_noise=1.0)))
+    ws = ds.Workspace(0, wl.B, wl.gamma, wl.V, wl.r, wl.d)
+    runs = [ds.markov_draft(t["W1"], t["W2"], t["U"], t["x0"], h=t["h"], w=t["w"],
+                            target=t["target"], seed=7, workspace=ws) for _ in range(3)]
+    torch.cuda.synchronize()
+    for o in runs[1:]:
+        for f in ("tokens", "lse", "c", "S", "cstar", "l1"):
+            assert torch.equal(getattr(o, f), getattr(runs[0], f)), f
