@@ -19,7 +19,7 @@ import torch
 from . import _lib
 
 __all__ = ["Workspace", "markov_draft", "rnn_draft", "confidence", "tv_label",
-           "prefix_schedule", "draft_path", "draft_launches", "DraftOutput"]
+           "prefix_schedule", "draft_path", "draft_launches", "DraftOutput", "DraftPlan"]
 
 _F32, _BF16 = 0, 1
 
@@ -76,51 +76,75 @@ class DraftOutput:
     s_out: torch.Tensor | None    # [B, r] final RNN state
 
 
-def _draft(head, W1, W2, U, x0, *, T, seed, h, w, Wj, target, forced, s0, want_logits,
-           workspace, stream, out=None):
-    lib = _lib.load()
-    B, gamma, V = U.shape
-    r = W1.shape[1]
-    d = h.shape[2] if h is not None else 0
-    dev = U.device
-    if workspace is None:
-        workspace = Workspace(head, B, gamma, V, r, d, device=dev)
-    f32 = dict(dtype=torch.float32, device=dev)
-    o = out or {}
-    tokens = o.get("tokens") if o.get("tokens") is not None else torch.empty(B, gamma, dtype=torch.int32, device=dev)
-    lse = o.get("lse") if o.get("lse") is not None else torch.empty(B, gamma, **f32)
-    conf = h is not None and w is not None
-    c = (o.get("c") if o.get("c") is not None else torch.empty(B, gamma, **f32)) if conf else None
-    S = (o.get("S") if o.get("S") is not None else torch.empty(B, gamma, **f32)) if conf else None
-    cstar = torch.empty(B, gamma, **f32) if target is not None else None
-    l1 = torch.empty(B, gamma, **f32) if target is not None else None
-    logits = torch.empty(B, gamma, V, **f32) if want_logits else None
-    s_out = torch.empty(B, r, **f32) if head == 1 else None
-    if x0.dtype != torch.int32 or (forced is not None and forced.dtype != torch.int32):
-        raise TypeError("x0 and forced are int32")
-    if target is not None and target.dtype != torch.float32:
-        raise TypeError("target is float32")
-    wdt, udt = _dtype_code(W1), _dtype_code(U)
-    for t in (W2, w, Wj):
-        if t is not None and _dtype_code(t) != wdt:
-            raise TypeError("W1, W2, w and Wj share one dtype")
-    if h is not None and _dtype_code(h) != udt:
-        raise TypeError("U and h share one dtype")
-    common_in = [_ptr(x0), _ptr(forced), _ptr(target)]
-    outs = [_ptr(tokens), _ptr(lse), _ptr(c), _ptr(S), _ptr(cstar), _ptr(l1), _ptr(logits)]
-    ws = [workspace.buf.data_ptr(), workspace.nbytes, _stream(stream)]
-    if head == 0:
-        code = lib.dspark_markov_draft(B, gamma, V, r, d, float(T), int(seed), wdt, _ptr(W1),
-                                       _ptr(W2), _ptr(w), udt, _ptr(U), _ptr(h), *common_in,
-                                       *outs, *ws)
-        where = "dspark_markov_draft"
-    else:
-        code = lib.dspark_rnn_draft(B, gamma, V, r, d, float(T), int(seed), wdt, _ptr(W1),
-                                    _ptr(W2), _ptr(w), _ptr(Wj), udt, _ptr(U), _ptr(h),
-                                    *common_in, _ptr(s0), *outs, _ptr(s_out), *ws)
-        where = "dspark_rnn_draft"
-    _lib.check(code, where)
-    return DraftOutput(tokens, lse, c, S, cstar, l1, logits, s_out)
+class DraftPlan:
+    """A draft call with its arguments marshalled once: ``run()`` enqueues it again with the
+    same input and output buffers (one C call, no per-call allocation or checks)."""
+
+    def __init__(self, head, W1, W2, U, x0, *, T, seed, h, w, Wj, target, forced, s0,
+                 want_logits, workspace, stream, out=None):
+        lib = _lib.load()
+        B, gamma, V = U.shape
+        r = W1.shape[1]
+        d = h.shape[2] if h is not None else 0
+        dev = U.device
+        if workspace is None:
+            workspace = Workspace(head, B, gamma, V, r, d, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        o = dict(out or {})
+        conf = h is not None and w is not None
+
+        def buf(name, shape, want, dtype=torch.float32):
+            if not want:
+                return None
+            t = o.get(name)
+            return t if t is not None else torch.empty(*shape, dtype=dtype, device=dev)
+
+        tokens = buf("tokens", (B, gamma), True, torch.int32)
+        lse = buf("lse", (B, gamma), True)
+        c = buf("c", (B, gamma), conf)
+        S = buf("S", (B, gamma), conf)
+        cstar = buf("cstar", (B, gamma), target is not None)
+        l1 = buf("l1", (B, gamma), target is not None)
+        logits = buf("logits", (B, gamma, V), want_logits)
+        s_out = buf("s_out", (B, r), head == 1)
+        if x0.dtype != torch.int32 or (forced is not None and forced.dtype != torch.int32):
+            raise TypeError("x0 and forced are int32")
+        if target is not None and target.dtype != torch.float32:
+            raise TypeError("target is float32")
+        wdt, udt = _dtype_code(W1), _dtype_code(U)
+        for t in (W2, w, Wj):
+            if t is not None and _dtype_code(t) != wdt:
+                raise TypeError("W1, W2, w and Wj share one dtype")
+        if h is not None and _dtype_code(h) != udt:
+            raise TypeError("U and h share one dtype")
+        common_in = [_ptr(x0), _ptr(forced), _ptr(target)]
+        outs = [_ptr(tokens), _ptr(lse), _ptr(c), _ptr(S), _ptr(cstar), _ptr(l1), _ptr(logits)]
+        ws = [workspace.buf.data_ptr(), workspace.nbytes, _stream(stream)]
+        if head == 0:
+            self._fn = lib.dspark_markov_draft
+            self._args = (B, gamma, V, r, d, float(T), int(seed), wdt, _ptr(W1), _ptr(W2),
+                          _ptr(w), udt, _ptr(U), _ptr(h), *common_in, *outs, *ws)
+            self._where = "dspark_markov_draft"
+        else:
+            self._fn = lib.dspark_rnn_draft
+            self._args = (B, gamma, V, r, d, float(T), int(seed), wdt, _ptr(W1), _ptr(W2),
+                          _ptr(w), _ptr(Wj), udt, _ptr(U), _ptr(h), *common_in, _ptr(s0), *outs,
+                          _ptr(s_out), *ws)
+            self._where = "dspark_rnn_draft"
+        # keep every tensor whose address is baked into the arguments alive
+        self._keep = (W1, W2, U, x0, h, w, Wj, target, forced, s0)
+        self.workspace = workspace
+        self.out = DraftOutput(tokens, lse, c, S, cstar, l1, logits, s_out)
+
+    def run(self) -> DraftOutput:
+        code = self._fn(*self._args)
+        if code != 0:
+            _lib.check(code, self._where)
+        return self.out
+
+
+def _draft(head, W1, W2, U, x0, **kw):
+    return DraftPlan(head, W1, W2, U, x0, **kw).run()
 
 
 def markov_draft(W1, W2, U, x0, *, T=1.0, seed=0, h=None, w=None, target=None, forced=None,

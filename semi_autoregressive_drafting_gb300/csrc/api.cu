@@ -195,14 +195,8 @@ dspark_status run_draft(const DraftArgs& a) {
   cudaStream_t stream = (cudaStream_t)a.stream;
 
   if (path == 0) {
-    const int row_bytes = a.r * (w_bf16 ? 2 : 4);
-    p.rows_per_stage = (16384 / row_bytes) / 4 * 4;
-    p.nstages = 2;
-    const size_t base = draft_cc_smem_bytes(p) - 2 * 16384;
-    const size_t avail = (size_t)di.smem_optin > base ? di.smem_optin - base : 0;
-    p.nstages = (int)std::min<size_t>(16, avail / 16384);
-    if (p.nstages < 2) return fail(DSPARK_ERR_UNSUPPORTED, "vocab slice too large for shared memory");
-    p.smem_bytes = draft_cc_smem_bytes(p);
+    if (!draft_cc_configure(p, (size_t)di.smem_optin))
+      return fail(DSPARK_ERR_UNSUPPORTED, "vocab slice too large for shared memory");
     cudaError_t e = launch_draft_cc(p, nCTA, stream);
     if (e != cudaSuccess) return cuda_fail(e, "draft_cc launch");
   }

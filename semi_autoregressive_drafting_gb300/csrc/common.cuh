@@ -176,16 +176,22 @@ __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Grid-wide barrier of a co-resident (cooperative) grid: barrier number `n` (1-based within the
-// launch) completes when every block has arrived n times.  Thread 0 of each block spins with
-// a time bound; returns false (and records a timeout) if the bound ran out.  Must be called by
-// every thread of the block (it contains __syncthreads).
-__device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned n, int* s_flag) {
+// Grid-wide barrier of a co-resident (cooperative) grid, split in two so a block can do
+// independent work between arriving and waiting.  Barrier number `n` (1-based within the
+// launch) completes when every block has arrived n times.  grid_arrive: every thread calls it
+// (it starts with __syncthreads); thread 0 publishes the block's writes and arrives.
+// grid_wait: every thread calls it; thread 0 spins with a time bound; returns false (and records
+// DSPARK_ERR_TIMEOUT) if the bound ran out.
+__device__ __forceinline__ void grid_arrive(WsHeader* hdr) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    int ok = 1;
     __threadfence();
     red_release_add(&hdr->arrive, 1u);
+  }
+}
+__device__ __forceinline__ bool grid_wait(WsHeader* hdr, unsigned n, int* s_flag) {
+  if (threadIdx.x == 0) {
+    int ok = 1;
     const unsigned target = n * gridDim.x;
     if (ld_acquire(&hdr->arrive) < target) {
       const unsigned long long t0 = globaltimer();
@@ -203,6 +209,15 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned n, int* s_f
   }
   __syncthreads();
   return *s_flag != 0;
+}
+__device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned n, int* s_flag) {
+  grid_arrive(hdr);
+  return grid_wait(hdr, n, s_flag);
+}
+
+// L2 prefetch of `bytes` (multiple of 16) starting at a 16-byte aligned global address.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // ------------------------------------------------------------------ mbarrier + bulk copies

@@ -46,7 +46,7 @@ struct DraftParams {
   float* rnn_a;              // [B][r] RNN conditioning vector tanh(o) for the current step
   float* rnn_gh;             // [B][gamma][3r] RNN h-part of the joint projection
   // launch geometry (set by the host)
-  int rows_per_stage;  // W2 rows per ring stage
+  int stage_bytes;     // bytes per ring stage (a multiple of 32 W2 rows)
   int nstages;         // ring depth
   int slice_max;       // largest vocab slice of any block (multiple of 8)
   int u_bulk;          // 1: U/target rows are 16-byte aligned and copied with TMA bulk copies
@@ -56,6 +56,7 @@ struct DraftParams {
 // Host launchers (defined in the .cu files).  Return a cudaError_t.
 cudaError_t launch_draft_cc(DraftParams& p, int nblocks, cudaStream_t stream);
 size_t draft_cc_smem_bytes(const DraftParams& p);
+bool draft_cc_configure(DraftParams& p, size_t smem_optin);
 int draft_cc_supported(int B, int r, int w_bf16);
 
 }  // namespace dspark

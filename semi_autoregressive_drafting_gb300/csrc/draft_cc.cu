@@ -3,48 +3,57 @@
 // One semi-autoregressive block of the DSpark sequential head ("DSpark -- paper verification",
 // section 1, Eqs 4, 5, 7, 8; "DSpark: Wait It's All Autoregressive?", "A parallel backbone with
 // autoregressive sampling": the serial loop is a lookup, a small projection, an addition and
-// sampling).  At small B the bias product W1[x] W2^T is a GEMV bound by HBM, so it stays on
-// the CUDA cores:
-//   * one thread block per SM owns a contiguous vocab slice [v0, v1) for all gamma steps;
-//     its W2 rows form one contiguous block of memory, streamed through a ring of 16 KB TMA
-//     bulk-copy stages.  The ring is refilled as soon as a stage is consumed, including across
-//     the step boundary, so the next step's W2 bytes are in flight while the grid agrees on x_k;
-//   * U_k and the target rows of the slice arrive by bulk copy one step ahead;
-//   * each warp reduces 4 vocab rows x NB requests at once with a transposing shuffle
-//     reduction, and the owning lane fuses +U_k, /T, the online (max, sum-exp), the Philox
+// sampling).  At small B the bias product W1[x] W2^T is a GEMV bound by memory, so it stays on
+// the CUDA cores.  Design (one cooperative launch for the whole block of gamma steps):
+//   * one thread block per SM owns a contiguous vocab slice [v0, v1) for all steps; its W2 rows
+//     are one contiguous block of memory, streamed through a ring of TMA bulk-copy stages by a
+//     dedicated producer warp (full/empty mbarriers).  The producer does not depend on the
+//     sampled tokens, so it runs ahead across step boundaries: the next step's W2 bytes are in
+//     flight while the grid agrees on x_k.  W2 is fetched with an L2 evict-last policy, so the
+//     steps after the first find it in L2 when it fits;
+//   * U_k and target rows of the slice arrive by bulk copy ahead of their step;
+//   * stages go round-robin to 8 consumer warps.  A warp takes 32/NB rows at a time, every
+//     lane accumulating a 16-byte K-chunk of each row for each request (32 independent sums),
+//     then one transposing shuffle reduction leaves lane l with the full dot product of
+//     (row l/NB, request l%NB), and every lane fuses +U_k, /T, the online (max, sum-exp), the
 //     Gumbel-max update and, with a target, the target's (max, sum-exp);
+//   * the Gumbel noise of step k+1 is computed while the block waits at the grid barrier of
+//     step k (it does not depend on the tokens);
 //   * the grid-wide argmax is one 64-bit atomicMax per (request, block) on an order-independent
-//     key; a bounded grid barrier publishes x_k; the Eq 8 label needs both normalisers, so its
-//     L1 sum runs right after the barrier from y and target values kept in shared memory.
+//     key; each block also prefetches its candidate's W1 row into L2 so the winner's row is
+//     warm when every block gathers it after the barrier;
+//   * the Eq 8 label needs both normalisers, so its L1 sum runs right after the barrier from y
+//     and target values kept in shared memory.
 #include "draft.cuh"
 
 namespace dspark {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kStageBytes = 16384;
+constexpr int kCWarps = 8;                   // consumer warps
+constexpr int kCThreads = kCWarps * 32;      // consumer threads (named barrier 1)
+constexpr int kThreads = kCThreads + 32;     // + one producer warp
 constexpr int kMaxG = 16;
 
-struct Slot {  // per owning lane, merged at the end of a step
+struct Slot {  // running state of one (request, vocab subset)
   float best;
   uint32_t tok;
   float m, l, mt, lt;
 };
 
 struct Misc {
-  int cond[4];       // conditioning token of the next step per request
-  int valid[4];      // request still valid
-  int xk[4];         // token sampled at the current step
-  float hdot[kMaxG]; // w[0:d] . h[b][k] for the owned request
-  float S_run;       // running prefix survival of the owned request
+  int cond[4];        // conditioning token of the next step per request
+  int valid[4];       // request still valid
+  float hdot[kMaxG];  // w[0:d] . h[b][k] for the owned request
+  float S_run;        // running prefix survival of the owned request
   float Ld[4], Lt[4];
+  float red[kCWarps];
   int flag;
   int last;
+  volatile int abort;
 };
 
 struct CCLayout {
-  size_t ring, ubuf, tbuf, ybuf, ebuf, slots, misc, bars, total;
+  size_t ring, ubuf, tbuf, ybuf, gbuf, ebuf, wsm, slots, misc, bars, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -55,43 +64,91 @@ __host__ __device__ inline CCLayout cc_layout(const DraftParams& p, int NB) {
   const bool tgt = p.target != nullptr;
   size_t off = 0;
   L.ring = off;
-  off += (size_t)p.nstages * kStageBytes;
+  off += (size_t)p.nstages * p.stage_bytes;
   L.ubuf = off;
   off = align_up(off + 2 * NB * (size_t)p.slice_max * ues, 128);
   L.tbuf = off;
   off = align_up(off + (tgt ? 2 * NB * (size_t)p.slice_max * 4 : 0), 128);
   L.ybuf = off;
   off = align_up(off + (tgt ? NB * (size_t)p.slice_max * 4 : 0), 128);
+  L.gbuf = off;
+  off = align_up(off + (size_t)NB * p.slice_max * 4, 128);
   L.ebuf = off;
   off = align_up(off + (size_t)NB * p.r * 4, 128);
+  L.wsm = off;
+  off = align_up(off + (size_t)p.r * 4, 128);
   L.slots = off;
-  off = align_up(off + kWarps * 16 * sizeof(Slot), 128);
+  off = align_up(off + kCWarps * 4 * sizeof(Slot), 128);
   L.misc = off;
   off = align_up(off + sizeof(Misc), 128);
   L.bars = off;
-  off += (size_t)(p.nstages + 2) * 8;
+  off += (size_t)(2 * p.nstages + 4) * 8;
   L.total = align_up(off, 128);
   return L;
 }
 
-template <int N>
-struct Log2 {
-  static constexpr int v = 1 + Log2<N / 2>::v;
-};
-template <>
-struct Log2<1> {
-  static constexpr int v = 0;
-};
+// ------------------------------------------------------------------ consumer-only barriers
+__device__ __forceinline__ void csync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kCThreads) : "memory");
+}
+__device__ __forceinline__ int csync_or(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "n"(kCThreads)
+      : "memory");
+  return r;
+}
+// grid barrier among the consumer threads of every block (the producer warp never takes part)
+__device__ __forceinline__ void c_grid_arrive(WsHeader* hdr) {
+  csync();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    red_release_add(&hdr->arrive, 1u);
+  }
+}
+__device__ __forceinline__ bool c_grid_wait(WsHeader* hdr, unsigned n, int* s_flag) {
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const unsigned target = n * gridDim.x;
+    if (ld_acquire(&hdr->arrive) < target) {
+      const unsigned long long t0 = globaltimer();
+      while (ld_acquire(&hdr->arrive) < target) {
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(20);
+      }
+    }
+    __threadfence();
+    *s_flag = ok;
+  }
+  csync();
+  return *s_flag != 0;
+}
 
-// Sum N values per lane across the warp so that lane l ends with the total of value
-// index (l >> (5 - log2 N)); every other index lives in another lane.
-template <int N>
-__device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
-  constexpr int L = Log2<N>::v;
+// bounded mbarrier wait that also gives up when the consumers abort
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
+                                                   volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort || globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// Sum 32 values per lane across the warp: lane l ends with the total of value index l.
+__device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
 #pragma unroll
-  for (int step = 0; step < L; ++step) {
+  for (int step = 0; step < 5; ++step) {
     const int o = 16 >> step;
-    const int c = N >> step;
+    const int c = 32 >> step;
     const bool upper = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < c / 2; ++i) {
@@ -100,8 +157,6 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
       v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
   }
-#pragma unroll
-  for (int o = 16 >> L; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
   return v[0];
 }
 
@@ -132,6 +187,47 @@ __device__ __forceinline__ float warp_sum_strided(const float* part, int n, int 
   return warp_sum(s);
 }
 
+// Gumbel noise of one step for this block's slice: one Philox call per 4 vocab entries.
+template <int NB>
+__device__ __forceinline__ void fill_noise(float* gbuf, int SLM, int SL, int v0, int B, int ks,
+                                           uint32_t s_lo, uint32_t s_hi, int tid, int nthr) {
+  const int nq = (SL + 3) >> 2;
+  for (int i = tid; i < NB * nq; i += nthr) {
+    const int b = i / nq, q = i - b * nq;
+    if (b >= B) continue;
+    const int v = v0 + 4 * q;  // v0 is a multiple of 8: one counter covers v .. v+3
+    const U4 r4 = philox4x32_10((uint32_t)(v >> 2), (uint32_t)ks, (uint32_t)b, kNoiseTag, s_lo, s_hi);
+    const uint32_t w[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (4 * q + j < SL) gbuf[(size_t)b * SLM + 4 * q + j] = gumbel_from_uniform(bits_to_uniform(w[j]));
+  }
+}
+
+__device__ __forceinline__ void slot_init(Slot& s) {
+  s.best = -INFINITY;
+  s.tok = 0xFFFFFFFFu;
+  s.m = -INFINITY;
+  s.l = 0.f;
+  s.mt = -INFINITY;
+  s.lt = 0.f;
+}
+__device__ __forceinline__ void slot_merge(Slot& a, const Slot& q) {
+  best_merge(a.best, a.tok, q.best, q.tok);
+  lse_merge(a.m, a.l, q.m, q.l);
+  lse_merge(a.mt, a.lt, q.mt, q.lt);
+}
+__device__ __forceinline__ Slot slot_shfl(const Slot& s, int o) {
+  Slot q;
+  q.best = __shfl_xor_sync(0xffffffffu, s.best, o);
+  q.tok = __shfl_xor_sync(0xffffffffu, s.tok, o);
+  q.m = __shfl_xor_sync(0xffffffffu, s.m, o);
+  q.l = __shfl_xor_sync(0xffffffffu, s.l, o);
+  q.mt = __shfl_xor_sync(0xffffffffu, s.mt, o);
+  q.lt = __shfl_xor_sync(0xffffffffu, s.lt, o);
+  return q;
+}
+
 template <typename WT, int NB, int NCV>
 __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -140,16 +236,18 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
   uint8_t* ubuf = smem + Lay.ubuf;
   float* tbuf = (float*)(smem + Lay.tbuf);
   float* ybuf = (float*)(smem + Lay.ybuf);
+  float* gbuf = (float*)(smem + Lay.gbuf);
   float* ebuf = (float*)(smem + Lay.ebuf);
+  float* wsm = (float*)(smem + Lay.wsm);
   Slot* slots = (Slot*)(smem + Lay.slots);
   Misc* ms = (Misc*)(smem + Lay.misc);
   uint64_t* full = (uint64_t*)(smem + Lay.bars);
-  uint64_t* ufull = full + p.nstages;
+  uint64_t* empty = full + p.nstages;
+  uint64_t* ufull = empty + p.nstages;
+  uint64_t* uempty = ufull + 2;
 
   constexpr int VEC = Vec<WT>::N;
-  constexpr int NV = 4 * NB;            // values per lane in the transposing reduction
-  constexpr int LNV = Log2<NV>::v;
-  constexpr int OWN_MASK = (32 >> LNV) - 1;
+  constexpr int SR = 32 / NB;  // rows per super-group: SR rows x NB requests = 32 sums
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nCTA = gridDim.x, cta = blockIdx.x;
   const int B = p.B, G = p.gamma, V = p.V, r = p.r;
@@ -166,19 +264,24 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
   const int SLM = p.slice_max;
   const int row_bytes = r * (int)sizeof(WT);
   const int VR = row_bytes / 16;  // 16-byte vectors per W2 row
-  const int R = p.rows_per_stage;
+  const int R = p.stage_bytes / row_bytes;  // rows per stage, a multiple of 32
   const int NS = p.nstages;
   const int nst = (SL + R - 1) / R;
   const int total = G * nst;
-  const uint64_t pol_stream = policy_evict_first();
-  const uint64_t pol_w = policy_evict_last();  // W2 is re-read every step: keep it in L2
+  const bool ubulk = p.u_bulk && SL > 0;
 
   if (tid == 0) {
-    for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
-    mbar_init(&ufull[0], 1);
-    mbar_init(&ufull[1], 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ufull[i], 1);
+      mbar_init(&uempty[i], 1);
+    }
     fence_mbar_init();
     ms->S_run = 1.f;
+    ms->abort = 0;
   }
   if (tid < 4) {
     const int b = tid;
@@ -188,71 +291,93 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
     ms->valid[b] = ok;
     if (b < B && !ok) atomicMax(&hdr->status, kErrInvalid);
   }
-  __syncthreads();
+  __syncthreads();  // the last block-wide barrier: from here the producer warp runs on its own
 
-  auto issue_stage = [&](int g) {
-    const int s = g % nst, slot = g % NS;
-    const int rows = min(R, SL - s * R);
-    const uint32_t bytes = (uint32_t)(rows * row_bytes);
-    mbar_expect_tx(&full[slot], bytes);
-    bulk_g2s(ring + (size_t)slot * kStageBytes,
-             (const uint8_t*)p.W2 + (size_t)(v0 + s * R) * row_bytes, bytes, &full[slot], pol_w);
-  };
-  auto issue_u = [&](int ks) {
-    const int buf = ks & 1;
-    const uint32_t bytes = (uint32_t)(B * SL * ues + (tgt ? B * SL * 4 : 0));
-    mbar_expect_tx(&ufull[buf], bytes);
-    if (SL == 0) return;
-    for (int b = 0; b < B; ++b) {
-      bulk_g2s(ubuf + ((size_t)(buf * NB + b) * SLM) * ues,
-               (const uint8_t*)p.U + (((size_t)b * G + ks) * V + v0) * ues, (uint32_t)(SL * ues),
-               &ufull[buf], pol_stream);
-      if (tgt)
-        bulk_g2s(tbuf + (size_t)(buf * NB + b) * SLM, p.target + ((size_t)b * G + ks) * V + v0,
-                 (uint32_t)(SL * 4), &ufull[buf], pol_stream);
+  // =========================================================== producer warp
+  if (warp == kCWarps) {
+    if (lane == 0) {
+      const uint64_t pol_stream = policy_evict_first();
+      const uint64_t pol_w = policy_evict_last();  // W2 is re-read every step: keep it in L2
+      int issued = 0, u_issued = 0;
+      bool stop = false;
+      for (int g = 0; g < total && !stop; ++g) {
+        const int ks = g / nst, s = g - ks * nst;
+        if (s == 0 && ubulk) {  // U_k (and target) rows of step ks
+          const int buf = ks & 1;
+          if (ks >= 2 &&
+              !mbar_wait_or_abort(&uempty[buf], (uint32_t)(((ks - 2) >> 1) & 1), &ms->abort)) {
+            stop = true;
+            break;
+          }
+          mbar_expect_tx(&ufull[buf], (uint32_t)(B * SL * ues + (tgt ? B * SL * 4 : 0)));
+          for (int b = 0; b < B; ++b) {
+            bulk_g2s(ubuf + ((size_t)(buf * NB + b) * SLM) * ues,
+                     (const uint8_t*)p.U + (((size_t)b * G + ks) * V + v0) * ues,
+                     (uint32_t)(SL * ues), &ufull[buf], pol_stream);
+            if (tgt)
+              bulk_g2s(tbuf + (size_t)(buf * NB + b) * SLM,
+                       p.target + ((size_t)b * G + ks) * V + v0, (uint32_t)(SL * 4), &ufull[buf],
+                       pol_stream);
+          }
+          u_issued = ks + 1;
+        }
+        const int slot = g % NS;
+        if (g >= NS &&
+            !mbar_wait_or_abort(&empty[slot], (uint32_t)(((g - NS) / NS) & 1), &ms->abort)) {
+          stop = true;
+          break;
+        }
+        const int rows = min(R, SL - s * R);
+        const uint32_t bytes = (uint32_t)(rows * row_bytes);
+        mbar_expect_tx(&full[slot], bytes);
+        bulk_g2s(ring + (size_t)slot * p.stage_bytes,
+                 (const uint8_t*)p.W2 + (size_t)(v0 + s * R) * row_bytes, bytes, &full[slot], pol_w);
+        issued = g + 1;
+      }
+      if (stop) atomicMax(&hdr->status, kErrTimeout);
+      // every copy this warp started must land before the block may exit
+      for (int g = max(0, issued - NS); g < issued; ++g)
+        mbar_wait(&full[g % NS], (uint32_t)((g / NS) & 1));
+      for (int k = max(0, u_issued - 2); k < u_issued; ++k)
+        mbar_wait(&ufull[k & 1], (uint32_t)((k >> 1) & 1));
     }
-  };
-
-  int u_issued = 0, u_waited = 0;  // block-uniform bookkeeping of U/target fills
-  if (tid == 0) {
-    for (int g = 0; g < min(NS, total); ++g) issue_stage(g);
-    if (p.u_bulk) {
-      issue_u(0);
-      if (G > 1) issue_u(1);
-    }
+    return;
   }
-  if (p.u_bulk) u_issued = min(G, 2);
 
-  // Eq 7, hidden half, for the owned request (request b is owned by block b)
+  // =========================================================== consumer warps
+  // Eq 7 inputs of the owned request (request b is owned by block b): the hidden half
+  // w[0:d].h[b][k] for every k, and w[d:d+r] kept in shared memory for the per-step half.
   if (conf && cta < B) {
-    for (int k = warp; k < G; k += kWarps) {
+    for (int j = tid; j < r; j += kCThreads) wsm[j] = to_f<WT>(((const WT*)p.w)[p.d + j]);
+    for (int k = warp; k < G; k += kCWarps) {
       const size_t base = ((size_t)cta * G + k) * p.d;
       float acc = 0.f;
+#pragma unroll 4
       for (int j = lane; j < p.d; j += 32)
         acc += to_f<WT>(((const WT*)p.w)[j]) * ld_act(p.h, base + j, p.u_bf16);
       acc = warp_sum(acc);
       if (lane == 0) ms->hdot[k] = acc;
     }
   }
+  fill_noise<NB>(gbuf, SLM, SL, v0, B, 0, p.seed_lo, p.seed_hi, tid, kCThreads);
 
-  int g_next = 0;  // next ring stage to consume (block-uniform)
   bool failed = false;
+  const int jrow = lane / NB, bq = lane % NB;  // this lane's (row, request) in a super-group
 
-  for (int ks = 0; ks < G && !failed; ++ks) {
+  for (int ks = 0; ks < G; ++ks) {
     const int buf = ks & 1;
     // (a) conditioning vectors e_b = W1[x_{k-1}] (Eq 5 lookup), fp32 in shared memory
-    for (int i = tid; i < NB * r; i += kThreads) {
+    for (int i = tid; i < NB * r; i += kCThreads) {
       const int b = i / r, j = i - b * r;
       float val = 0.f;
       if (b < B && ms->valid[b]) val = to_f<WT>(((const WT*)p.W1)[(size_t)ms->cond[b] * r + j]);
       ebuf[i] = val;
     }
-    __syncthreads();
-    // (b) Eq 7 and the prefix survival for the owned request
+    csync();
+    // (b) Eq 7 and the prefix survival for the owned request (shared memory only)
     if (conf && cta < B && warp == 0) {
       float acc = 0.f;
-      for (int j = lane; j < r; j += 32)
-        acc += to_f<WT>(((const WT*)p.w)[p.d + j]) * ebuf[cta * r + j];
+      for (int j = lane; j < r; j += 32) acc += wsm[j] * ebuf[cta * r + j];
       acc = warp_sum(acc);
       if (lane == 0) {
         const size_t o = (size_t)cta * G + ks;
@@ -267,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
         }
       }
     }
-    // (c) this lane's slice of every e_b in registers
+    // (c) this lane's K-chunks of every e_b in registers
     float ereg[NB][NCV][VEC];
 #pragma unroll
     for (int b = 0; b < NB; ++b)
@@ -278,15 +403,14 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
         for (int i = 0; i < VEC; ++i) ereg[b][t][i] = cv < VR ? ebuf[b * r + cv * VEC + i] : 0.f;
       }
     // (d) U_k (and target) rows of the slice
-    if (p.u_bulk) {
+    if (ubulk) {
       const bool ok = mbar_wait(&ufull[buf], (uint32_t)((ks >> 1) & 1));
-      if (__syncthreads_or(!ok)) {
+      if (csync_or(!ok)) {
         failed = true;
         break;
       }
-      u_waited = ks + 1;
-    } else {
-      for (int i = tid; i < B * SL; i += kThreads) {
+    } else if (SL > 0) {
+      for (int i = tid; i < B * SL; i += kCThreads) {
         const int b = i / SL, vl = i - b * SL;
         const size_t src = ((size_t)b * G + ks) * V + v0 + vl;
         if (p.u_bf16)
@@ -295,68 +419,65 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
           ((float*)ubuf)[(size_t)(buf * NB + b) * SLM + vl] = ((const float*)p.U)[src];
         if (tgt) tbuf[(size_t)(buf * NB + b) * SLM + vl] = p.target[src];
       }
-      __syncthreads();
+      csync();
     }
 
-    // (e) stream the slice: bias dot products, logits, sampling, normalisers
-    const int idx = lane >> (5 - LNV);
-    const bool owner = (lane & OWN_MASK) == 0;
-    const int jr = idx / NB, bq = idx % NB;
+    // (e) this warp's stages: bias dot products, logits, sampling, normalisers
     Slot st;
-    st.best = -INFINITY;
-    st.tok = 0xFFFFFFFFu;
-    st.m = -INFINITY;
-    st.l = 0.f;
-    st.mt = -INFINITY;
-    st.lt = 0.f;
+    slot_init(st);
     const uint8_t* ub = ubuf + (size_t)(buf * NB + bq) * SLM * ues;
     const float* tb = tbuf + (size_t)(buf * NB + bq) * SLM;
-    for (int s = 0; s < nst; ++s) {
-      const int g = g_next;
+    const float* gb = gbuf + (size_t)bq * SLM;
+    bool wfail = false;
+    for (int s = warp; s < nst; s += kCWarps) {
+      const int g = ks * nst + s;
       const int slot = g % NS;
-      const bool ok = mbar_wait(&full[slot], (uint32_t)((g / NS) & 1));
-      if (__syncthreads_or(!ok)) {
-        failed = true;
+      if (!mbar_wait(&full[slot], (uint32_t)((g / NS) & 1))) {
+        wfail = true;
         break;
       }
       const int rows = min(R, SL - s * R);
-      const uint8_t* stg = ring + (size_t)slot * kStageBytes;
-      for (int grp = warp; grp * 4 < rows; grp += kWarps) {
-        float part[NV];
+      const uint8_t* stg = ring + (size_t)slot * p.stage_bytes;
+      for (int r0 = 0; r0 < rows; r0 += SR) {
+        float part[32];
 #pragma unroll
-        for (int i = 0; i < NV; ++i) part[i] = 0.f;
+        for (int i = 0; i < 32; ++i) part[i] = 0.f;
 #pragma unroll
         for (int t = 0; t < NCV; ++t) {
           const int cv = lane + 32 * t;
           if (cv < VR) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (grp * 4 + j < rows) {
-                const uint4 q = *(const uint4*)(stg + (size_t)(grp * 4 + j) * row_bytes + cv * 16);
+            for (int j = 0; j < SR; ++j) {
+              if (r0 + j < rows) {
+                const uint4 q = *(const uint4*)(stg + (size_t)(r0 + j) * row_bytes + cv * 16);
                 float wv[VEC];
                 Vec<WT>::unpack(q, wv);
 #pragma unroll
-                for (int b = 0; b < NB; ++b)
+                for (int b = 0; b < NB; ++b) {
+                  float a0 = part[j * NB + b], a1 = 0.f;
 #pragma unroll
-                  for (int i = 0; i < VEC; ++i) part[j * NB + b] = fmaf(wv[i], ereg[b][t][i], part[j * NB + b]);
+                  for (int i = 0; i < VEC; i += 2) {
+                    a0 = fmaf(wv[i], ereg[b][t][i], a0);
+                    a1 = fmaf(wv[i + 1], ereg[b][t][i + 1], a1);
+                  }
+                  part[j * NB + b] = a0 + a1;
+                }
               }
             }
           }
         }
-        const float bias = transpose_reduce<NV>(part, lane);
-        const int row = grp * 4 + jr;
-        const int v = v0 + s * R + row;
-        const U4 q = philox4x32_10((uint32_t)(v >> 2), (uint32_t)ks, (uint32_t)bq, kNoiseTag,
-                                   p.seed_lo, p.seed_hi);
-        if (owner && bq < B && row < rows) {
-          const int vl = v - v0;
+        const float bias = transpose_reduce32(part, lane);
+        const int row = r0 + jrow;
+        if (bq < B && row < rows) {
+          const int vl = s * R + row;
+          const int v = v0 + vl;
           const float uval = p.u_bf16 ? __uint_as_float((uint32_t)((const uint16_t*)ub)[vl] << 16)
                                       : ((const float*)ub)[vl];
           const float z = uval + bias;
           if (p.logits) p.logits[((size_t)bq * G + ks) * V + v] = z;
           const float y = z * p.invT;
           lse_push(st.m, st.l, y);
-          const float sc = y + gumbel_from_uniform(bits_to_uniform(pick(q, v & 3)));
+          const float sc = y + gb[vl];
           if (sc > st.best) {  // v grows along this lane's sequence: ties keep the smaller v
             st.best = sc;
             st.tok = (uint32_t)v;
@@ -367,63 +488,55 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
           }
         }
       }
-      ++g_next;
-      __syncthreads();
-      if (tid == 0 && g + NS < total) issue_stage(g + NS);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
     }
-    if (failed) break;
-
-    // (f) block-level merge in a fixed order, then publish this block's candidate
-    if (owner) slots[warp * 16 + idx] = st;
-    __syncthreads();
-    if (tid < B) {
-      const int b = tid;
-      Slot a;
-      a.best = -INFINITY;
-      a.tok = 0xFFFFFFFFu;
-      a.m = -INFINITY;
-      a.l = 0.f;
-      a.mt = -INFINITY;
-      a.lt = 0.f;
-      for (int w = 0; w < kWarps; ++w)
-        for (int j = 0; j < 4; ++j) {
-          const Slot& q = slots[w * 16 + j * NB + b];
-          best_merge(a.best, a.tok, q.best, q.tok);
-          lse_merge(a.m, a.l, q.m, q.l);
-          lse_merge(a.mt, a.lt, q.mt, q.lt);
-        }
-      if (SL > 0 && ms->valid[b]) atomicMax(&p.keys[(size_t)ks * B + b], make_key(a.best, a.tok));
-      p.ml[((size_t)ks * B + b) * nCTA + cta] = make_float2(a.m, a.l);
-      if (tgt) p.mlt[((size_t)ks * B + b) * nCTA + cta] = make_float2(a.mt, a.lt);
-    }
-
-    // (g) every block has published step ks
-    if (!grid_barrier(hdr, (unsigned)(ks + 1), &ms->flag)) {
+    if (csync_or(wfail)) {
       failed = true;
       break;
     }
 
-    // (h) x_k, next conditioning token, per-request outputs of step ks
+    // (f) merge lanes of the same request (fixed butterfly), then warps in a fixed order
+#pragma unroll
+    for (int o = NB; o < 32; o <<= 1) {
+      const Slot q = slot_shfl(st, o);
+      slot_merge(st, q);
+    }
+    if (lane < NB) slots[warp * 4 + lane] = st;
+    csync();
+    if (tid < B) {
+      const int b = tid;
+      Slot a;
+      slot_init(a);
+      for (int w = 0; w < kCWarps; ++w) slot_merge(a, slots[w * 4 + b]);
+      if (SL > 0 && ms->valid[b]) {
+        atomicMax(&p.keys[(size_t)ks * B + b], make_key(a.best, a.tok));
+        // if this block's candidate wins, every block gathers its W1 row next: warm L2 now
+        prefetch_l2((const uint8_t*)p.W1 + (size_t)a.tok * row_bytes, (uint32_t)row_bytes);
+      }
+      p.ml[((size_t)ks * B + b) * nCTA + cta] = make_float2(a.m, a.l);
+      if (tgt) p.mlt[((size_t)ks * B + b) * nCTA + cta] = make_float2(a.mt, a.lt);
+    }
+
+    // (g) every block has published step ks; the next step's noise is made while waiting
+    c_grid_arrive(hdr);
+    if (ks + 1 < G) fill_noise<NB>(gbuf, SLM, SL, v0, B, ks + 1, p.seed_lo, p.seed_hi, tid, kCThreads);
+    if (!c_grid_wait(hdr, (unsigned)(ks + 1), &ms->flag)) {
+      failed = true;
+      break;
+    }
+
+    // (h) x_k and the next conditioning token
     if (tid < B) {
       const int b = tid;
       const bool was_valid = ms->valid[b];
       const int xk = was_valid ? (int)key_token(ld_acquire64(&p.keys[(size_t)ks * B + b])) : -1;
-      ms->xk[b] = xk;
       int nxt = p.forced ? p.forced[(size_t)b * G + ks] : xk;
       const bool ok = was_valid && nxt >= 0 && nxt < V;
       if (was_valid && !ok && cta == 0) atomicMax(&hdr->status, kErrInvalid);
       ms->cond[b] = ok ? nxt : 0;
       ms->valid[b] = ok;
-    }
-    if (cta < B && warp == 0) {  // the owned request's token and log-normaliser
-      const int b = cta;
-      const float2 ml = warp_merge_ml(p.ml + ((size_t)ks * B + b) * nCTA, nCTA, lane);
-      if (lane == 0) {
-        const int xk = (int)key_token(ld_acquire64(&p.keys[(size_t)ks * B + b]));
-        const bool vb = xk >= 0 && xk < V;
-        p.tokens[(size_t)b * G + ks] = vb ? xk : -1;
-        p.lse[(size_t)b * G + ks] = vb ? ml.x + logf(ml.y) : NAN;
-      }
+      if (cta == b) p.tokens[(size_t)b * G + ks] = was_valid ? xk : -1;
     }
     if (tgt) {
       // Eq 8 second pass over the slice: needs the global normalisers of p^d and p^t
@@ -435,62 +548,63 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
           ms->Lt[warp] = t.x + logf(t.y);
         }
       }
-      __syncthreads();
+      csync();
       for (int b = 0; b < B; ++b) {
         const float Ld = ms->Ld[b], Lt = ms->Lt[b];
         float acc = 0.f;
-        for (int vl = tid; vl < SL; vl += kThreads)
+        for (int vl = tid; vl < SL; vl += kCThreads)
           acc += fabsf(__expf(ybuf[(size_t)b * SLM + vl] - Ld) -
                        __expf(tbuf[(size_t)(buf * NB + b) * SLM + vl] * p.invT - Lt));
         acc = warp_sum(acc);
-        if (lane == 0) slots[warp].best = acc;
-        __syncthreads();
+        if (lane == 0) ms->red[warp] = acc;
+        csync();
         if (tid == 0) {
           float s = 0.f;
-          for (int w = 0; w < kWarps; ++w) s += slots[w].best;
+          for (int w = 0; w < kCWarps; ++w) s += ms->red[w];
           p.l1p[((size_t)ks * B + b) * nCTA + cta] = s;
         }
-        __syncthreads();
+        csync();
       }
-      // the previous step's partial L1 sums are complete: the owner finishes Eq 8
-      if (ks > 0 && cta < B && warp == 0) {
-        const float s = warp_sum_strided(p.l1p + ((size_t)(ks - 1) * B + cta) * nCTA, nCTA, lane);
+    }
+    csync();
+    // (i) U/target buffer `buf` is free again for step ks + 2
+    if (ubulk && tid == 0) mbar_arrive(&uempty[buf]);
+  }
+
+  if (failed) {
+    // unwind: stop the producer (it drains its own copies), record the timeout
+    ms->abort = 1;
+    if (tid == 0) atomicMax(&hdr->status, kErrTimeout);
+    return;
+  }
+
+  // the owned request's log-normalisers, and Eq 8 of every step but the last (whose partial
+  // sums are complete only once every block is done): one warp per step
+  if (cta < B) {
+    const int b = cta;
+    for (int k = warp; k < G; k += kCWarps) {
+      const float2 ml = warp_merge_ml(p.ml + ((size_t)k * B + b) * nCTA, nCTA, lane);
+      const bool vb = p.tokens[(size_t)b * G + k] >= 0;
+      if (lane == 0) p.lse[(size_t)b * G + k] = vb ? ml.x + logf(ml.y) : NAN;
+      if (tgt && k + 1 < G) {
+        const float s = warp_sum_strided(p.l1p + ((size_t)k * B + b) * nCTA, nCTA, lane);
         if (lane == 0) {
-          const size_t o = (size_t)cta * G + ks - 1;
-          const bool vb = p.tokens[o] >= 0;
+          const size_t o = (size_t)b * G + k;
           p.l1[o] = vb ? s : NAN;
           p.cstar[o] = vb ? fminf(1.f, fmaxf(0.f, 1.f - 0.5f * s)) : NAN;
         }
       }
     }
-    __syncthreads();
-    // (i) U/target buffer `buf` is free again: fetch step ks + 2 into it
-    if (p.u_bulk && ks + 2 < G) {
-      if (tid == 0) issue_u(ks + 2);
-      u_issued = ks + 3;
-    }
-  }
-
-  if (failed) {
-    // unwind: record the timeout, wait (bounded) for this block's copies still in flight
-    if (tid == 0) {
-      atomicMax(&hdr->status, kErrTimeout);
-      const int g_end = min(total, g_next + NS);
-      for (int g = g_next; g < g_end; ++g) mbar_wait(&full[g % NS], (uint32_t)((g / NS) & 1));
-      for (int k = u_waited; k < u_issued; ++k) mbar_wait(&ufull[k & 1], (uint32_t)((k >> 1) & 1));
-    }
-    __syncthreads();
-    return;
   }
 
   // last block out: Eq 8 of the final step, then leave the workspace ready for the next call
-  __syncthreads();
+  csync();
   if (tid == 0) {
     __threadfence();
     const unsigned old = atomicAdd(&hdr->exit_count, 1u);
     ms->last = (old == (unsigned)nCTA - 1u);
   }
-  __syncthreads();
+  csync();
   if (ms->last) {
     __threadfence();
     if (tgt && warp < B) {
@@ -503,8 +617,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
         p.cstar[o] = vb ? fminf(1.f, fmaxf(0.f, 1.f - 0.5f * s)) : NAN;
       }
     }
-    for (int i = tid; i < G * B; i += kThreads) p.keys[i] = 0ull;
-    __syncthreads();
+    for (int i = tid; i < G * B; i += kCThreads) p.keys[i] = 0ull;
+    csync();
     if (tid == 0) {
       hdr->arrive = 0;
       hdr->exit_count = 0;
@@ -538,6 +652,23 @@ int nb_of(int B) { return B <= 1 ? 1 : B <= 2 ? 2 : 4; }
 int draft_cc_supported(int B, int r, int w_bf16) {
   const int row_bytes = r * (w_bf16 ? 2 : 4);
   return B >= 1 && B <= 4 && row_bytes % 16 == 0 && row_bytes <= 1024;
+}
+
+// Ring geometry: stages of at least 16 KB holding a multiple of 32 W2 rows, as many stages as
+// the shared memory left after the per-step buffers allows (at most 16).
+bool draft_cc_configure(DraftParams& p, size_t smem_optin) {
+  const int row_bytes = p.r * (p.w_bf16 ? 2 : 4);
+  int rows = 16384 / row_bytes;
+  rows = rows < 32 ? 32 : rows / 32 * 32;
+  p.stage_bytes = rows * row_bytes;
+  p.nstages = 0;
+  const size_t base = cc_layout(p, nb_of(p.B)).total;
+  const size_t avail = smem_optin > base + 64 ? smem_optin - base - 64 : 0;
+  p.nstages = (int)(avail / ((size_t)p.stage_bytes + 16));
+  if (p.nstages > 16) p.nstages = 16;
+  if (p.nstages < 2) return false;
+  p.smem_bytes = cc_layout(p, nb_of(p.B)).total;
+  return p.smem_bytes <= smem_optin;
 }
 
 size_t draft_cc_smem_bytes(const DraftParams& p) { return cc_layout(p, nb_of(p.B)).total; }
