@@ -62,14 +62,16 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 struct WsLayout {
-  size_t keys, ml, mlt, l1p, rnn_s, rnn_a, rnn_gh, total;
+  size_t keys, hdot, ml, mlt, l1p, rnn_s, rnn_a, rnn_gh, total;
 };
 
 WsLayout ws_layout(int head, int B, int G, int r, int nCTA) {
   WsLayout L;
   size_t off = sizeof(WsHeader);
   L.keys = off;
-  off = align256(off + (size_t)G * B * 8);
+  off = align256(off + (size_t)G * B * nCTA * 8);
+  L.hdot = off;
+  off = align256(off + (size_t)G * B * 4);
   L.ml = off;
   off = align256(off + (size_t)G * B * nCTA * 8);
   L.mlt = off;
@@ -181,6 +183,7 @@ dspark_status run_draft(const DraftArgs& a) {
   uint8_t* ws = (uint8_t*)a.ws;
   p.hdr = (WsHeader*)ws;
   p.keys = (unsigned long long*)(ws + L.keys);
+  p.hdot = (float*)(ws + L.hdot);
   p.ml = (float2*)(ws + L.ml);
   p.mlt = (float2*)(ws + L.mlt);
   p.l1p = (float*)(ws + L.l1p);

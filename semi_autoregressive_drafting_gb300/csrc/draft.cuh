@@ -38,7 +38,8 @@ struct DraftParams {
   float* s_out;
   // workspace
   WsHeader* hdr;
-  unsigned long long* keys;  // [gamma][B]
+  unsigned long long* keys;  // [gamma][B][nCTA] per-block tagged argmax keys (zero between calls)
+  float* hdot;               // [B][gamma] Eq 7 hidden halves w[0:d] . h[b][k]
   float2* ml;                // [gamma][B][nCTA] (max, sum exp) of y per block
   float2* mlt;               // [gamma][B][nCTA] same for the target
   float* l1p;                // [gamma][B][nCTA] partial L1 distances

@@ -12,8 +12,9 @@
 //     flight while the grid agrees on x_k.  W2 is fetched with an L2 evict-last policy, so the
 //     steps after the first find it in L2 when it fits;
 //   * U_k and target rows of the slice arrive by bulk copy ahead of their step;
-//   * stages go round-robin to 8 consumer warps.  A warp takes 32/NB rows at a time, every
-//     lane accumulating a 16-byte K-chunk of each row for each request (32 independent sums),
+//   * stages go round-robin to the consumer warps (16 for NB <= 2, else 8).  A warp takes
+//     32/NB rows at a time, every lane accumulating a 16-byte K-chunk of each row for each
+//     request (32 independent sums; bf16 operands go straight into mixed-precision FMAs),
 //     then one transposing shuffle reduction leaves lane l with the full dot product of
 //     (row l/NB, request l%NB), and every lane fuses +U_k, /T, the online (max, sum-exp), the
 //     Gumbel-max update and, with a target, the target's (max, sum-exp);
@@ -29,9 +30,7 @@
 namespace dspark {
 namespace {
 
-constexpr int kCWarps = 8;                   // consumer warps
-constexpr int kCThreads = kCWarps * 32;      // consumer threads (named barrier 1)
-constexpr int kThreads = kCThreads + 32;     // + one producer warp
+constexpr int kMaxCW = 16;  // most consumer warps of any variant
 constexpr int kMaxG = 16;
 
 struct Slot {  // running state of one (request, vocab subset)
@@ -43,13 +42,14 @@ struct Slot {  // running state of one (request, vocab subset)
 struct Misc {
   int cond[4];        // conditioning token of the next step per request
   int valid[4];       // request still valid
-  float hdot[kMaxG];  // w[0:d] . h[b][k] for the owned request
+  float edot[kMaxG];  // w[d:d+r] . W1[x_{k-1}] of the owned request, per step
   float S_run;        // running prefix survival of the owned request
   float Ld[4], Lt[4];
-  float red[kCWarps];
+  float red[kMaxCW];
   int flag;
   int last;
   volatile int abort;
+  volatile int stage_tag[16];  // which global stage each ring slot currently holds
 };
 
 struct CCLayout {
@@ -78,7 +78,7 @@ __host__ __device__ inline CCLayout cc_layout(const DraftParams& p, int NB) {
   L.wsm = off;
   off = align_up(off + (size_t)p.r * 4, 128);
   L.slots = off;
-  off = align_up(off + kCWarps * 4 * sizeof(Slot), 128);
+  off = align_up(off + kMaxCW * 4 * sizeof(Slot), 128);
   L.misc = off;
   off = align_up(off + sizeof(Misc), 128);
   L.bars = off;
@@ -88,9 +88,11 @@ __host__ __device__ inline CCLayout cc_layout(const DraftParams& p, int NB) {
 }
 
 // ------------------------------------------------------------------ consumer-only barriers
+template <int NT>
 __device__ __forceinline__ void csync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kCThreads) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
 }
+template <int NT>
 __device__ __forceinline__ int csync_or(int pred) {
   int r;
   asm volatile(
@@ -99,18 +101,20 @@ __device__ __forceinline__ int csync_or(int pred) {
       "bar.red.or.pred q, 1, %2, p;\n\t"
       "selp.s32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(pred), "n"(kCThreads)
+      : "r"(pred), "n"(NT)
       : "memory");
   return r;
 }
 // grid barrier among the consumer threads of every block (the producer warp never takes part)
+template <int NT>
 __device__ __forceinline__ void c_grid_arrive(WsHeader* hdr) {
-  csync();
+  csync<NT>();
   if (threadIdx.x == 0) {
     __threadfence();
     red_release_add(&hdr->arrive, 1u);
   }
 }
+template <int NT>
 __device__ __forceinline__ bool c_grid_wait(WsHeader* hdr, unsigned n, int* s_flag) {
   if (threadIdx.x == 0) {
     int ok = 1;
@@ -128,7 +132,7 @@ __device__ __forceinline__ bool c_grid_wait(WsHeader* hdr, unsigned n, int* s_fl
     __threadfence();
     *s_flag = ok;
   }
-  csync();
+  csync<NT>();
   return *s_flag != 0;
 }
 
@@ -143,12 +147,131 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
   return true;
 }
 
-// Sum 32 values per lane across the warp: lane l ends with the total of value index l.
-__device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
+// Wait until ring slot `slot` holds stage g and its bytes have landed.  A warp consumes every
+// CW-th stage, so it may reach a slot before the slot's previous use has completed; the phase
+// parity alone would then be ambiguous, so the producer tags the slot with the stage it holds
+// before arming it, and the parity is only read once the tag matches.
+__device__ __forceinline__ bool wait_stage(volatile int* tag, uint64_t* full, int slot, int g,
+                                           int NS) {
+  if (tag[slot] != g) {
+    const unsigned long long t0 = globaltimer();
+    while (tag[slot] != g) {
+      if (globaltimer() - t0 > kWaitLimitNs) return false;
+      __nanosleep(32);
+    }
+  }
+  return mbar_wait(full + slot, (uint32_t)((g / NS) & 1));
+}
+
+__device__ __forceinline__ float ld_act(const void* p, size_t i, int bf16) {
+  return bf16 ? __bfloat162float(((const __nv_bfloat16*)p)[i]) : ((const float*)p)[i];
+}
+
+// Tagged argmax key of one block for one (step, request):
+//   bits 63..32  orderable fp32 perturbed score (larger is better),
+//   bits 31..24  step tag k+1 (the key's slot is zero until this launch publishes it),
+//   bits 23..0   0xFFFFFF - v (so equal scores prefer the smaller v; V <= 2^24).
+// A block with nothing to offer publishes score bits 0, below every finite score.
+__device__ __forceinline__ unsigned long long tagged_key(float score, uint32_t v, int ks) {
+  return ((unsigned long long)orderable(score) << 32) | ((unsigned long long)(ks + 1) << 24) |
+         (unsigned long long)(0xFFFFFFu - v);
+}
+__device__ __forceinline__ unsigned long long tagged_key_empty(int ks) {
+  return (unsigned long long)(ks + 1) << 24;
+}
+__device__ __forceinline__ uint32_t tagged_token(unsigned long long key) {
+  return 0xFFFFFFu - (uint32_t)(key & 0xFFFFFFull);
+}
+__device__ __forceinline__ void st_release64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ float ld_acquire_f32(const float* p) {
+  float v;
+  asm volatile("ld.acquire.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid barrier and argmax in one: wait (bounded) until every block has published its tagged
+// key for step ks, then return the largest.  One warp; each lane covers every 32nd block.
+__device__ __forceinline__ bool poll_keys(const unsigned long long* keys, int n, int ks, int lane,
+                                          unsigned long long* best) {
+  const unsigned long long tag = (unsigned long long)(ks + 1);
+  unsigned long long t0 = 0;
+  for (;;) {
+    unsigned long long m = 0;
+    bool mine = true;
+    for (int i = lane; i < n; i += 32) {
+      const unsigned long long k = ld_acquire64(keys + i);
+      mine = mine && ((k >> 24) & 0xFF) == tag;
+      m = k > m ? k : m;
+    }
+    if (__all_sync(0xffffffffu, mine)) {
 #pragma unroll
-  for (int step = 0; step < 5; ++step) {
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long q = __shfl_xor_sync(0xffffffffu, m, o);
+        m = q > m ? q : m;
+      }
+      *best = m;
+      return true;
+    }
+    if (t0 == 0) t0 = globaltimer();
+    else if (globaltimer() - t0 > kWaitLimitNs) return false;
+    __nanosleep(32);
+  }
+}
+
+// Eq 7 hidden halves w[0:d] . h[b][k], one (b, k) pair per block in turn, block-wide dot
+// products with 16-byte loads, written to the workspace for the owner of request b.
+template <typename WT, int NT>
+__device__ void hidden_dots(const DraftParams& p, Misc* ms, int tid, int cta, int nCTA) {
+  const int npairs = p.B * p.gamma;
+  for (int i = cta; i < npairs; i += nCTA) {
+    float acc = 0.f;
+    const size_t base = (size_t)i * p.d;
+    if (p.u_bf16 && sizeof(WT) == 2) {
+      for (int j = tid * 8; j < p.d; j += NT * 8) {
+        const uint4 hq = *(const uint4*)((const __nv_bfloat16*)p.h + base + j);
+        const uint4 wq = *(const uint4*)((const WT*)p.w + j);
+        float hv[8], wv[8];
+        Vec<__nv_bfloat16>::unpack(hq, hv);
+        Vec<__nv_bfloat16>::unpack(wq, wv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(hv[e], wv[e], acc);
+      }
+    } else {
+      for (int j = tid; j < p.d; j += NT)
+        acc += to_f<WT>(((const WT*)p.w)[j]) * ld_act(p.h, base + j, p.u_bf16);
+    }
+    acc = warp_sum(acc);
+    if ((tid & 31) == 0) ms->red[tid >> 5] = acc;
+    csync<NT>();
+    if (tid == 0) {
+      float s = 0.f;
+      for (int w = 0; w < NT / 32; ++w) s += ms->red[w];
+      p.hdot[i] = s;
+    }
+    csync<NT>();
+  }
+}
+
+template <int N>
+struct Log2 {
+  static constexpr int v = 1 + Log2<N / 2>::v;
+};
+template <>
+struct Log2<1> {
+  static constexpr int v = 0;
+};
+
+// Sum N values per lane (N a power of two <= 32) across the warp: lane l ends with the total
+// of value index l >> (5 - log2 N); each index is held by 32/N neighbouring lanes.
+template <int N>
+__device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
+  constexpr int L = Log2<N>::v;
+#pragma unroll
+  for (int step = 0; step < L; ++step) {
     const int o = 16 >> step;
-    const int c = 32 >> step;
+    const int c = N >> step;
     const bool upper = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < c / 2; ++i) {
@@ -157,11 +280,9 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
       v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
   }
+#pragma unroll
+  for (int o = 16 >> L; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
   return v[0];
-}
-
-__device__ __forceinline__ float ld_act(const void* p, size_t i, int bf16) {
-  return bf16 ? __bfloat162float(((const __nv_bfloat16*)p)[i]) : ((const float*)p)[i];
 }
 
 // (max, sum-exp) of all blocks' partials for one (step, request), merged by one warp in a
@@ -228,8 +349,51 @@ __device__ __forceinline__ Slot slot_shfl(const Slot& s, int o) {
   return q;
 }
 
-template <typename WT, int NB, int NCV>
-__global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams p) {
+// Row dot-product accumulation for one 16-byte W2 chunk against this lane's K-chunk of e.
+// bf16: the packed mixed-precision FMA reads both bf16 operands from register halves and
+// accumulates in fp32 (bf16 -> fp32 is exact, so this equals converting first).
+template <typename WT>
+struct Dot;
+template <>
+struct Dot<__nv_bfloat16> {
+  using E = uint32_t;  // e kept as packed bf16 pairs
+  static constexpr int NE = 4;
+  __device__ __forceinline__ static E load_e(const float* ebuf, int idx2) {
+    // ebuf holds fp32 copies of bf16 values: repack two of them exactly
+    return (__float_as_uint(ebuf[2 * idx2]) >> 16) | (__float_as_uint(ebuf[2 * idx2 + 1]) & 0xFFFF0000u);
+  }
+  __device__ __forceinline__ static float run(const uint4& q, const E (&e)[NE], float acc) {
+    float a0 = acc, a1 = 0.f;
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      asm("{\n\t.reg .b16 wl, wh, el, eh;\n\t"
+          "mov.b32 {wl, wh}, %2;\n\t"
+          "mov.b32 {el, eh}, %3;\n\t"
+          "fma.rn.f32.bf16 %0, wl, el, %0;\n\t"
+          "fma.rn.f32.bf16 %1, wh, eh, %1;\n\t}"
+          : "+f"(a0), "+f"(a1)
+          : "r"(w[i]), "r"(e[i]));
+    return a0 + a1;
+  }
+};
+template <>
+struct Dot<float> {
+  using E = float;
+  static constexpr int NE = 4;
+  __device__ __forceinline__ static E load_e(const float* ebuf, int idx) { return ebuf[idx]; }
+  __device__ __forceinline__ static float run(const uint4& q, const E (&e)[NE], float acc) {
+    float a0 = fmaf(__uint_as_float(q.x), e[0], acc), a1 = __uint_as_float(q.y) * e[1];
+    a0 = fmaf(__uint_as_float(q.z), e[2], a0);
+    a1 = fmaf(__uint_as_float(q.w), e[3], a1);
+    return a0 + a1;
+  }
+};
+
+template <typename WT, int NB, int NCV, int CW>
+__global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftParams p) {
+  constexpr int kCWarps = CW;
+  constexpr int kCThreads = CW * 32;
   extern __shared__ __align__(1024) uint8_t smem[];
   const CCLayout Lay = cc_layout(p, NB);
   uint8_t* ring = smem + Lay.ring;
@@ -247,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
   uint64_t* uempty = ufull + 2;
 
   constexpr int VEC = Vec<WT>::N;
-  constexpr int SR = 32 / NB;  // rows per super-group: SR rows x NB requests = 32 sums
+  constexpr int SR = 8 / NB;  // rows per sub-group: SR rows x NB requests = 8 sums per lane
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nCTA = gridDim.x, cta = blockIdx.x;
   const int B = p.B, G = p.gamma, V = p.V, r = p.r;
@@ -273,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], 4);  // the four warps sharing a stage
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ufull[i], 1);
@@ -282,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
     fence_mbar_init();
     ms->S_run = 1.f;
     ms->abort = 0;
+    for (int i = 0; i < 16; ++i) ms->stage_tag[i] = -1;
   }
   if (tid < 4) {
     const int b = tid;
@@ -329,6 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
         }
         const int rows = min(R, SL - s * R);
         const uint32_t bytes = (uint32_t)(rows * row_bytes);
+        ms->stage_tag[slot] = g;
         mbar_expect_tx(&full[slot], bytes);
         bulk_g2s(ring + (size_t)slot * p.stage_bytes,
                  (const uint8_t*)p.W2 + (size_t)(v0 + s * R) * row_bytes, bytes, &full[slot], pol_w);
@@ -345,24 +511,18 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
   }
 
   // =========================================================== consumer warps
-  // Eq 7 inputs of the owned request (request b is owned by block b): the hidden half
-  // w[0:d].h[b][k] for every k, and w[d:d+r] kept in shared memory for the per-step half.
-  if (conf && cta < B) {
+  if (conf && cta < B)
     for (int j = tid; j < r; j += kCThreads) wsm[j] = to_f<WT>(((const WT*)p.w)[p.d + j]);
-    for (int k = warp; k < G; k += kCWarps) {
-      const size_t base = ((size_t)cta * G + k) * p.d;
-      float acc = 0.f;
-#pragma unroll 4
-      for (int j = lane; j < p.d; j += 32)
-        acc += to_f<WT>(((const WT*)p.w)[j]) * ld_act(p.h, base + j, p.u_bf16);
-      acc = warp_sum(acc);
-      if (lane == 0) ms->hdot[k] = acc;
-    }
-  }
+  if (conf && G == 1) hidden_dots<WT, kCThreads>(p, ms, tid, cta, nCTA);
   fill_noise<NB>(gbuf, SLM, SL, v0, B, 0, p.seed_lo, p.seed_hi, tid, kCThreads);
 
   bool failed = false;
-  const int jrow = lane / NB, bq = lane % NB;  // this lane's (row, request) in a super-group
+  // after the 8-value reduction lane l holds value (l >> 2) = (row, request) = (idx/NB, idx%NB);
+  // lanes 4 idx own it
+  const int idx8 = lane >> 2, jrow = idx8 / NB, bq = idx8 % NB;
+  const bool owner = (lane & 3) == 0;
+  constexpr int kGroups = kCWarps / 4;
+  const int grp = warp / 4, qw = warp % 4;
 
   for (int ks = 0; ks < G; ++ks) {
     const int buf = ks & 1;
@@ -373,39 +533,23 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
       if (b < B && ms->valid[b]) val = to_f<WT>(((const WT*)p.W1)[(size_t)ms->cond[b] * r + j]);
       ebuf[i] = val;
     }
-    csync();
-    // (b) Eq 7 and the prefix survival for the owned request (shared memory only)
-    if (conf && cta < B && warp == 0) {
-      float acc = 0.f;
-      for (int j = lane; j < r; j += 32) acc += wsm[j] * ebuf[cta * r + j];
-      acc = warp_sum(acc);
-      if (lane == 0) {
-        const size_t o = (size_t)cta * G + ks;
-        if (ms->valid[cta]) {
-          const float cv = sigmoidf_acc(ms->hdot[ks] + acc);
-          ms->S_run *= cv;
-          p.c[o] = cv;
-          p.S[o] = ms->S_run;
-        } else {
-          p.c[o] = NAN;
-          p.S[o] = NAN;
-        }
-      }
-    }
-    // (c) this lane's K-chunks of every e_b in registers
-    float ereg[NB][NCV][VEC];
+    csync<kCThreads>();
+    // (b) this lane's K-chunks of every e_b in registers
+    using DT = Dot<WT>;
+    typename DT::E ereg[NB][NCV][DT::NE];
 #pragma unroll
     for (int b = 0; b < NB; ++b)
 #pragma unroll
       for (int t = 0; t < NCV; ++t) {
         const int cv = lane + 32 * t;
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) ereg[b][t][i] = cv < VR ? ebuf[b * r + cv * VEC + i] : 0.f;
+        for (int i = 0; i < DT::NE; ++i)
+          ereg[b][t][i] = cv < VR ? DT::load_e(ebuf + b * r + cv * VEC, i) : typename DT::E(0);
       }
-    // (d) U_k (and target) rows of the slice
+    // (c) U_k (and target) rows of the slice
     if (ubulk) {
       const bool ok = mbar_wait(&ufull[buf], (uint32_t)((ks >> 1) & 1));
-      if (csync_or(!ok)) {
+      if (csync_or<kCThreads>(!ok)) {
         failed = true;
         break;
       }
@@ -419,56 +563,57 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
           ((float*)ubuf)[(size_t)(buf * NB + b) * SLM + vl] = ((const float*)p.U)[src];
         if (tgt) tbuf[(size_t)(buf * NB + b) * SLM + vl] = p.target[src];
       }
-      csync();
+      csync<kCThreads>();
     }
 
-    // (e) this warp's stages: bias dot products, logits, sampling, normalisers
+    // (d) this warp's stages: bias dot products, logits, sampling, normalisers
     Slot st;
     slot_init(st);
     const uint8_t* ub = ubuf + (size_t)(buf * NB + bq) * SLM * ues;
     const float* tb = tbuf + (size_t)(buf * NB + bq) * SLM;
     const float* gb = gbuf + (size_t)bq * SLM;
     bool wfail = false;
-    for (int s = warp; s < nst; s += kCWarps) {
+    // Four warps share each stage: warp q of a group takes rows [q R/4, (q+1) R/4) in
+    // sub-groups of SR rows, so a slot is handed back a quarter of a stage's work after its
+    // bytes land.  Stages go round-robin to the groups.
+    for (int s = grp; s < nst; s += kGroups) {
       const int g = ks * nst + s;
       const int slot = g % NS;
-      if (!mbar_wait(&full[slot], (uint32_t)((g / NS) & 1))) {
+      if (!wait_stage(ms->stage_tag, full, slot, g, NS)) {
         wfail = true;
         break;
       }
       const int rows = min(R, SL - s * R);
+      const int rq0 = qw * (R / 4), rq1 = min(rows, rq0 + R / 4);
       const uint8_t* stg = ring + (size_t)slot * p.stage_bytes;
-      for (int r0 = 0; r0 < rows; r0 += SR) {
-        float part[32];
+      if (rq1 <= rq0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+      }
+      for (int r0 = rq0; r0 < rq1; r0 += SR) {
+        float part[8];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) part[i] = 0.f;
+        for (int i = 0; i < 8; ++i) part[i] = 0.f;
+        // No per-row guard here (a data-dependent guard serialises the loads): rows past the
+        // end of a short stage read in-bounds stale ring bytes and are masked in the epilogue;
+        // lanes past the row width read a chunk of the same row against zero e values.
 #pragma unroll
         for (int t = 0; t < NCV; ++t) {
-          const int cv = lane + 32 * t;
-          if (cv < VR) {
+          const int cv = min(lane + 32 * t, VR - 1);
 #pragma unroll
-            for (int j = 0; j < SR; ++j) {
-              if (r0 + j < rows) {
-                const uint4 q = *(const uint4*)(stg + (size_t)(r0 + j) * row_bytes + cv * 16);
-                float wv[VEC];
-                Vec<WT>::unpack(q, wv);
+          for (int j = 0; j < SR; ++j) {
+            const uint4 q = *(const uint4*)(stg + (size_t)(r0 + j) * row_bytes + cv * 16);
 #pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                  float a0 = part[j * NB + b], a1 = 0.f;
-#pragma unroll
-                  for (int i = 0; i < VEC; i += 2) {
-                    a0 = fmaf(wv[i], ereg[b][t][i], a0);
-                    a1 = fmaf(wv[i + 1], ereg[b][t][i + 1], a1);
-                  }
-                  part[j * NB + b] = a0 + a1;
-                }
-              }
-            }
+            for (int b = 0; b < NB; ++b) part[j * NB + b] = DT::run(q, ereg[b][t], part[j * NB + b]);
           }
         }
-        const float bias = transpose_reduce32(part, lane);
+        if (r0 + SR >= rq1) {  // this warp's bytes of the stage are in registers: hand it back
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+        const float bias = transpose_reduce<8>(part, lane);
         const int row = r0 + jrow;
-        if (bq < B && row < rows) {
+        if (owner && bq < B && row < rq1) {
           const int vl = s * R + row;
           const int v = v0 + vl;
           const float uval = p.u_bf16 ? __uint_as_float((uint32_t)((const uint16_t*)ub)[vl] << 16)
@@ -488,56 +633,74 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
     }
-    if (csync_or(wfail)) {
+    if (csync_or<kCThreads>(wfail)) {
       failed = true;
       break;
     }
 
-    // (f) merge lanes of the same request (fixed butterfly), then warps in a fixed order
+    // (e) merge lanes of the same request (fixed butterfly), then warps (fixed butterfly), and
+    // publish this block's candidate for step ks: (max, sum-exp) partials first, then the
+    // tagged argmax key with release semantics -- the key doubles as the barrier arrival
 #pragma unroll
-    for (int o = NB; o < 32; o <<= 1) {
+    for (int o = 4 * NB; o < 32; o <<= 1) {
       const Slot q = slot_shfl(st, o);
       slot_merge(st, q);
     }
-    if (lane < NB) slots[warp * 4 + lane] = st;
-    csync();
-    if (tid < B) {
-      const int b = tid;
+    if (lane < 4 * NB && owner) slots[warp * 4 + (lane >> 2)] = st;
+    csync<kCThreads>();
+    if (warp < B) {
+      const int b = warp;
       Slot a;
-      slot_init(a);
-      for (int w = 0; w < kCWarps; ++w) slot_merge(a, slots[w * 4 + b]);
-      if (SL > 0 && ms->valid[b]) {
-        atomicMax(&p.keys[(size_t)ks * B + b], make_key(a.best, a.tok));
-        // if this block's candidate wins, every block gathers its W1 row next: warm L2 now
-        prefetch_l2((const uint8_t*)p.W1 + (size_t)a.tok * row_bytes, (uint32_t)row_bytes);
+      if (lane < kCWarps) a = slots[lane * 4 + b];
+      else slot_init(a);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const Slot q = slot_shfl(a, o);
+        slot_merge(a, q);
       }
-      p.ml[((size_t)ks * B + b) * nCTA + cta] = make_float2(a.m, a.l);
-      if (tgt) p.mlt[((size_t)ks * B + b) * nCTA + cta] = make_float2(a.mt, a.lt);
+      if (lane == 0) {
+        const size_t o = ((size_t)ks * B + b) * nCTA + cta;
+        p.ml[o] = make_float2(a.m, a.l);
+        if (tgt) p.mlt[o] = make_float2(a.mt, a.lt);
+        const bool has = SL > 0 && ms->valid[b];
+        st_release64(&p.keys[o], has ? tagged_key(a.best, a.tok, ks) : tagged_key_empty(ks));
+        // if this block's candidate wins, every block gathers its W1 row next: warm L2 now
+        if (has) prefetch_l2((const uint8_t*)p.W1 + (size_t)a.tok * row_bytes, (uint32_t)row_bytes);
+      }
     }
 
-    // (g) every block has published step ks; the next step's noise is made while waiting
-    c_grid_arrive(hdr);
+    // (f) while the other blocks finish: next step's noise, Eq 7's embedding half of this step
+    // (owned request), the hidden halves (first step); then every block's key for step ks
     if (ks + 1 < G) fill_noise<NB>(gbuf, SLM, SL, v0, B, ks + 1, p.seed_lo, p.seed_hi, tid, kCThreads);
-    if (!c_grid_wait(hdr, (unsigned)(ks + 1), &ms->flag)) {
+    if (conf && cta < B && warp == kCWarps - 1) {
+      float acc = 0.f;
+      for (int j = lane; j < r; j += 32) acc += wsm[j] * ebuf[cta * r + j];
+      acc = warp_sum(acc);
+      if (lane == 0) ms->edot[ks] = acc;
+    }
+    if (conf && ks == 0 && G > 1) hidden_dots<WT, kCThreads>(p, ms, tid, cta, nCTA);
+    bool ok = true;
+    if (warp < B) {
+      const int b = warp;
+      unsigned long long best = 0;
+      ok = poll_keys(p.keys + ((size_t)ks * B + b) * nCTA, nCTA, ks, lane, &best);
+      if (lane == 0 && ok) {
+        const bool was_valid = ms->valid[b];
+        const int xk = was_valid ? (int)tagged_token(best) : -1;
+        const int nxt = p.forced ? p.forced[(size_t)b * G + ks] : xk;
+        const bool nv = was_valid && nxt >= 0 && nxt < V;
+        if (was_valid && !nv && cta == 0) atomicMax(&hdr->status, kErrInvalid);
+        ms->cond[b] = nv ? nxt : 0;
+        ms->valid[b] = nv;
+        if (cta == b) p.tokens[(size_t)b * G + ks] = was_valid ? xk : -1;
+      }
+    }
+    if (csync_or<kCThreads>(!ok)) {
       failed = true;
       break;
     }
 
-    // (h) x_k and the next conditioning token
-    if (tid < B) {
-      const int b = tid;
-      const bool was_valid = ms->valid[b];
-      const int xk = was_valid ? (int)key_token(ld_acquire64(&p.keys[(size_t)ks * B + b])) : -1;
-      int nxt = p.forced ? p.forced[(size_t)b * G + ks] : xk;
-      const bool ok = was_valid && nxt >= 0 && nxt < V;
-      if (was_valid && !ok && cta == 0) atomicMax(&hdr->status, kErrInvalid);
-      ms->cond[b] = ok ? nxt : 0;
-      ms->valid[b] = ok;
-      if (cta == b) p.tokens[(size_t)b * G + ks] = was_valid ? xk : -1;
-    }
     if (tgt) {
       // Eq 8 second pass over the slice: needs the global normalisers of p^d and p^t
       if (warp < B) {
@@ -548,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
           ms->Lt[warp] = t.x + logf(t.y);
         }
       }
-      csync();
+      csync<kCThreads>();
       for (int b = 0; b < B; ++b) {
         const float Ld = ms->Ld[b], Lt = ms->Lt[b];
         float acc = 0.f;
@@ -557,17 +720,16 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
                        __expf(tbuf[(size_t)(buf * NB + b) * SLM + vl] * p.invT - Lt));
         acc = warp_sum(acc);
         if (lane == 0) ms->red[warp] = acc;
-        csync();
+        csync<kCThreads>();
         if (tid == 0) {
           float s = 0.f;
           for (int w = 0; w < kCWarps; ++w) s += ms->red[w];
           p.l1p[((size_t)ks * B + b) * nCTA + cta] = s;
         }
-        csync();
+        csync<kCThreads>();
       }
     }
-    csync();
-    // (i) U/target buffer `buf` is free again for step ks + 2
+    // (g) U/target buffer `buf` is free again for step ks + 2
     if (ubulk && tid == 0) mbar_arrive(&uempty[buf]);
   }
 
@@ -578,10 +740,22 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
     return;
   }
 
-  // the owned request's log-normalisers, and Eq 8 of every step but the last (whose partial
-  // sums are complete only once every block is done): one warp per step
+  // the owned request: Eq 7 and S_k for every step, log-normalisers, and Eq 8 of every step
+  // but the last (whose partial sums are complete only once every block is done)
   if (cta < B) {
     const int b = cta;
+    if (conf && tid == 0) {
+      float surv = 1.f;
+      bool vb = true;
+      for (int k = 0; k < G; ++k) {
+        const size_t o = (size_t)b * G + k;
+        vb = vb && p.tokens[o] >= 0;
+        const float cv = vb ? sigmoidf_acc(ld_acquire_f32(&p.hdot[o]) + ms->edot[k]) : NAN;
+        surv = vb ? surv * cv : NAN;
+        p.c[o] = cv;
+        p.S[o] = surv;
+      }
+    }
     for (int k = warp; k < G; k += kCWarps) {
       const float2 ml = warp_merge_ml(p.ml + ((size_t)k * B + b) * nCTA, nCTA, lane);
       const bool vb = p.tokens[(size_t)b * G + k] >= 0;
@@ -598,13 +772,13 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
   }
 
   // last block out: Eq 8 of the final step, then leave the workspace ready for the next call
-  csync();
+  csync<kCThreads>();
   if (tid == 0) {
     __threadfence();
     const unsigned old = atomicAdd(&hdr->exit_count, 1u);
     ms->last = (old == (unsigned)nCTA - 1u);
   }
-  csync();
+  csync<kCThreads>();
   if (ms->last) {
     __threadfence();
     if (tgt && warp < B) {
@@ -617,10 +791,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
         p.cstar[o] = vb ? fminf(1.f, fmaxf(0.f, 1.f - 0.5f * s)) : NAN;
       }
     }
-    for (int i = tid; i < G * B; i += kCThreads) p.keys[i] = 0ull;
-    csync();
+    for (int i = tid; i < G * B * nCTA; i += kCThreads) p.keys[i] = 0ull;
+    csync<kCThreads>();
     if (tid == 0) {
-      hdr->arrive = 0;
       hdr->exit_count = 0;
       __threadfence();
     }
@@ -629,7 +802,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_cc_kernel(const DraftParams
 
 template <typename WT, int NB, int NCV>
 cudaError_t launch_t(DraftParams& p, int nblocks, cudaStream_t stream) {
-  auto kern = draft_cc_kernel<WT, NB, NCV>;
+  constexpr int CW = NB <= 2 ? 16 : 8;
+  constexpr int kThreads = CW * 32 + 32;
+  auto kern = draft_cc_kernel<WT, NB, NCV, CW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)p.smem_bytes);
   if (e != cudaSuccess) return e;

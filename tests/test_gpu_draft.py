@@ -85,6 +85,14 @@ def test_bf16_rank_512():
     _run_case(wl)
 
 
+def test_ring_reuse_more_stages_than_slots():
+    # every block streams more W2 stages than the ring has slots, so slots are reused within a
+    # step and warps reach a slot before its previous use completes
+    wl = inputs.WORKLOADS["qwen3_4b_markov"].with_(V=80000, d=128, B=1, seed=36)
+    _run_case(wl, want_logits=False)
+    _run_case(wl.with_(B=2, seed=37), want_logits=False)
+
+
 @pytest.mark.slow
 def test_qwen3_4b_markov_full():
     ties, _ = _run_case(inputs.WORKLOADS["qwen3_4b_markov"], want_logits=False)
