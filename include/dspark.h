@@ -42,7 +42,8 @@
  *   g_v = -ln(-ln u_v), ties to the smaller v.  u_v = (2*(bits >> 9) + 1) * 2^-24 where bits is
  *   word (v mod 4) of Philox4x32-10 (Salmon et al., SC'11) with key (lo32(seed), hi32(seed))
  *   and counter (floor(v/4), k-1, b, 0x44535052).  The same seed, shapes and inputs give the
- *   same tokens on every run (no atomics decide a value; reductions run in a fixed order).
+ *   same tokens on every run: the cross-block argmax is order-independent and every sum runs in
+ *   a fixed order.
  */
 #ifndef DSPARK_H
 #define DSPARK_H
@@ -67,15 +68,20 @@ typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
 
 typedef enum { DSPARK_HEAD_MARKOV = 0, DSPARK_HEAD_RNN = 1 } dspark_head;
 
+/* dspark_workspace_bytes flags */
+#define DSPARK_WS_TARGET 1 /* the calls will pass target logits (Eq 8 labels) */
+
 /*
- * Bytes of workspace the draft calls need for this problem.  The workspace is caller-owned
- * device memory, 256-byte aligned, that must be ZEROED ONCE before its first use; every
+ * Bytes of workspace the draft calls need for this problem (`flags`: DSPARK_WS_TARGET when
+ * target logits will be passed; at B > 4 that reserves room for y, B * V floats).  The
+ * workspace is caller-owned device memory, 256-byte aligned, that must be ZEROED ONCE before
+ * its first use; every
  * successful call leaves it ready for the next call.  One workspace serves one call at a time:
  * calls that share a workspace must be ordered (same stream, or events).  After a call whose
  * device status is not DSPARK_OK, call dspark_get_status() before reusing the workspace.
  * Returns 0 for arguments the draft calls would reject.
  */
-size_t dspark_workspace_bytes(int head, int B, int gamma, int V, int r, int d);
+size_t dspark_workspace_bytes(int head, int B, int gamma, int V, int r, int d, int flags);
 
 /*
  * One semi-autoregressive draft block with the Markov head [P1 s1 Eq 4, Eq 5, Eq 7, Eq 8;

@@ -51,9 +51,10 @@ class Workspace:
     """Zero-initialised device scratch for the draft calls; reusable across calls of the same
     or smaller shape, one call at a time (stream order)."""
 
-    def __init__(self, head: int, B: int, gamma: int, V: int, r: int, d: int, device=None):
+    def __init__(self, head: int, B: int, gamma: int, V: int, r: int, d: int, device=None,
+                 target: bool = False):
         lib = _lib.load()
-        n = lib.dspark_workspace_bytes(head, B, gamma, V, r, d)
+        n = lib.dspark_workspace_bytes(head, B, gamma, V, r, d, 1 if target else 0)
         if n == 0:
             raise ValueError("invalid draft shape for a workspace")
         self.nbytes = int(n)
@@ -88,7 +89,7 @@ class DraftPlan:
         d = h.shape[2] if h is not None else 0
         dev = U.device
         if workspace is None:
-            workspace = Workspace(head, B, gamma, V, r, d, device=dev)
+            workspace = Workspace(head, B, gamma, V, r, d, device=dev, target=target is not None)
         f32 = dict(dtype=torch.float32, device=dev)
         o = dict(out or {})
         conf = h is not None and w is not None

@@ -62,10 +62,11 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 struct WsLayout {
-  size_t keys, hdot, ml, mlt, l1p, rnn_s, rnn_a, rnn_gh, total;
+  size_t keys, hdot, ml, mlt, l1p, rnn_s, rnn_a, rnn_gh, ybuf, total;
 };
 
-WsLayout ws_layout(int head, int B, int G, int r, int nCTA) {
+// flags: DSPARK_WS_TARGET reserves the y buffer the tensor-core path needs for Eq 8
+WsLayout ws_layout(int head, int B, int G, int V, int r, int nCTA, int flags) {
   WsLayout L;
   size_t off = sizeof(WsHeader);
   L.keys = off;
@@ -84,6 +85,8 @@ WsLayout ws_layout(int head, int B, int G, int r, int nCTA) {
   off = align256(off + (head == 1 ? (size_t)B * r * 4 : 0));
   L.rnn_gh = off;
   off = align256(off + (head == 1 ? (size_t)B * G * 3 * r * 4 : 0));
+  L.ybuf = off;
+  off = align256(off + ((flags & DSPARK_WS_TARGET) && B > 4 ? (size_t)B * V * 4 : 0));
   L.total = off;
   return L;
 }
@@ -94,9 +97,10 @@ bool shape_ok(int head, int B, int G, int V, int r, int d) {
 }
 
 int path_of(int head, int B, int r, int w_bf16) {
-  (void)head;
+  if (head == 1) return -1;  // the RNN head is not in this build yet
   if (draft_cc_supported(B, r, w_bf16)) return 0;
-  return -1;  // tensor-core path: not in this build yet
+  if (draft_tc_supported(B, r, w_bf16)) return 1;
+  return -1;
 }
 
 struct DraftArgs {
@@ -140,14 +144,14 @@ dspark_status run_draft(const DraftArgs& a) {
   DevInfo di;
   if (!dev_info(&di)) return fail(DSPARK_ERR_CUDA, "cannot query the current device");
   const int nCTA = di.sms;
-  const WsLayout L = ws_layout(a.head, a.B, a.G, a.r, nCTA);
+  const WsLayout L = ws_layout(a.head, a.B, a.G, a.V, a.r, nCTA, a.target ? DSPARK_WS_TARGET : 0);
   if (!a.ws || !aligned(a.ws, 256) || a.ws_bytes < L.total)
     return fail(DSPARK_ERR_WORKSPACE, "workspace must be 256-byte aligned and >= %zu bytes", L.total);
   const int w_bf16 = a.wdt == DSPARK_BF16, u_bf16 = a.udt == DSPARK_BF16;
   const int path = path_of(a.head, a.B, a.r, w_bf16);
-  if (path < 0 || a.head == 1)
-    return fail(DSPARK_ERR_UNSUPPORTED, "no kernel for head=%d B=%d r=%d in this build", a.head,
-                a.B, a.r);
+  if (path < 0)
+    return fail(DSPARK_ERR_UNSUPPORTED, "no kernel for head=%d B=%d r=%d dtype=%d in this build",
+                a.head, a.B, a.r, (int)a.wdt);
 
   DraftParams p;
   std::memset(&p, 0, sizeof p);
@@ -190,6 +194,7 @@ dspark_status run_draft(const DraftArgs& a) {
   p.rnn_s = (float*)(ws + L.rnn_s);
   p.rnn_a = (float*)(ws + L.rnn_a);
   p.rnn_gh = (float*)(ws + L.rnn_gh);
+  p.ybuf = (float*)(ws + L.ybuf);
 
   const int units = (a.V + 7) / 8;
   p.slice_max = ((units + nCTA - 1) / nCTA) * 8;
@@ -202,6 +207,12 @@ dspark_status run_draft(const DraftArgs& a) {
       return fail(DSPARK_ERR_UNSUPPORTED, "vocab slice too large for shared memory");
     cudaError_t e = launch_draft_cc(p, nCTA, stream);
     if (e != cudaSuccess) return cuda_fail(e, "draft_cc launch");
+  } else {
+    if (a.V > (1 << 24) - 1) return fail(DSPARK_ERR_UNSUPPORTED, "V too large for the tensor-core path");
+    if (!draft_tc_configure(p, (size_t)di.smem_optin))
+      return fail(DSPARK_ERR_UNSUPPORTED, "rank too large for shared memory");
+    cudaError_t e = launch_draft_tc(p, nCTA, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "draft_tc launch");
   }
   return DSPARK_OK;
 }
@@ -210,11 +221,11 @@ dspark_status run_draft(const DraftArgs& a) {
 
 extern "C" {
 
-size_t dspark_workspace_bytes(int head, int B, int gamma, int V, int r, int d) {
+size_t dspark_workspace_bytes(int head, int B, int gamma, int V, int r, int d, int flags) {
   if (!shape_ok(head, B, gamma, V, r, d)) return 0;
   DevInfo di;
   if (!dev_info(&di)) return 0;
-  return ws_layout(head, B, gamma, r, di.sms).total;
+  return ws_layout(head, B, gamma, V, r, di.sms, flags).total;
 }
 
 dspark_status dspark_markov_draft(int B, int gamma, int V, int r, int d, float T, uint64_t seed,
@@ -308,7 +319,7 @@ int dspark_draft_path(int head, int B, int V, int r, dspark_dtype wdt) {
 int dspark_draft_launches(int head, int B, int V, int r, dspark_dtype wdt) {
   const int p = dspark_draft_path(head, B, V, r, wdt);
   if (p < 0) return -1;
-  return 1;
+  return 1;  // one persistent launch on either path
 }
 
 }  // extern "C"

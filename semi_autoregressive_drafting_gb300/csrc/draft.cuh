@@ -46,11 +46,13 @@ struct DraftParams {
   float* rnn_s;              // [2][B][r] RNN state ping-pong
   float* rnn_a;              // [B][r] RNN conditioning vector tanh(o) for the current step
   float* rnn_gh;             // [B][gamma][3r] RNN h-part of the joint projection
+  float* ybuf;               // [B][V] y of the current step (tensor-core path with a target)
   // launch geometry (set by the host)
   int stage_bytes;     // bytes per ring stage (a multiple of 32 W2 rows)
   int nstages;         // ring depth
   int slice_max;       // largest vocab slice of any block (multiple of 8)
   int u_bulk;          // 1: U/target rows are 16-byte aligned and copied with TMA bulk copies
+  int tc_na;           // tensor-core path: A-operand buffers
   size_t smem_bytes;
 };
 
@@ -59,5 +61,8 @@ cudaError_t launch_draft_cc(DraftParams& p, int nblocks, cudaStream_t stream);
 size_t draft_cc_smem_bytes(const DraftParams& p);
 bool draft_cc_configure(DraftParams& p, size_t smem_optin);
 int draft_cc_supported(int B, int r, int w_bf16);
+cudaError_t launch_draft_tc(DraftParams& p, int nblocks, cudaStream_t stream);
+bool draft_tc_configure(DraftParams& p, size_t smem_optin);
+int draft_tc_supported(int B, int r, int w_bf16);
 
 }  // namespace dspark

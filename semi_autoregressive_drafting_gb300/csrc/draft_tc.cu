@@ -1,0 +1,612 @@
+// draft_tc.cu -- persistent tensor-core draft kernel for larger batches (bf16 weights, B > 4).
+//
+// Same block of the DSpark sequential head as draft_cc.cu ("DSpark -- paper verification",
+// section 1, Eqs 4, 5, 7, 8), but once B is large the bias product e W2^T (e = the gathered
+// W1 rows, [B x r]) is a real dense contraction, so it runs on the 5th-generation tensor cores:
+//   * MMA tile: M = 128 requests (one batch chunk), N = 128 vocab entries, K = r in 64-wide
+//     slabs; A (the gathered W1 rows) is written into shared memory in the 128-byte-swizzled
+//     K-major layout by the epilogue warps, B (W2 rows, stored [V][r]) arrives by 2-D TMA;
+//     the fp32 accumulator lives in TMEM (4 buffers of 128 columns);
+//   * warp 0 produces W2 slabs (runs ahead across tiles, chunks and steps), warp 1 issues the
+//     MMAs from one thread and owns TMEM, warps 4..11 are the epilogue: two warps per TMEM lane
+//     quarter, each taking 64 of a tile's 128 columns for its 32 requests;
+//   * the epilogue fuses +U_k, /T, the online (max, sum-exp), and Gumbel-max sampling with an
+//     exact skip: with w = 1 - u (exact from the Philox bits) and q = exp(y - best), an entry
+//     with w >= 1.001 q cannot beat the running best (-ln u >= w, so its score is below
+//     best - 0.0009), so the two logarithms run only for the rare entries that might;
+//   * per step, each block publishes one candidate per request with a 64-bit atomicMax on an
+//     order-independent key, then a bounded grid barrier; the Eq 8 label runs its second pass
+//     over the block's slice after the barrier from y saved in the workspace.
+#include <cuda.h>
+
+#include "draft.cuh"
+#include "tc.cuh"
+
+namespace dspark {
+namespace {
+
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 4 * 32 + kEpiThreads;  // producer, MMA, two spare warps, epilogue
+constexpr int kM = 128;                          // requests per chunk
+constexpr int kNT = 128;                         // vocab entries per tile
+constexpr int kSlab = 16384;                     // bytes of one 128 x 64 bf16 swizzled slab
+constexpr int kAcc = 4;                          // TMEM accumulators of kNT columns
+constexpr int kTmemCols = kAcc * kNT;            // 512
+
+struct TSlot {
+  float best;
+  uint32_t tok;
+  float m, l, mt, lt;
+};
+
+struct TMisc {
+  uint32_t tmem_base;
+  int flag;
+  int last;
+  volatile int abort;
+  float red[kEpiWarps];
+};
+
+struct TCLayout {
+  size_t a, ring, scratch, misc, bars, total;
+  int nslab, na, nstage;
+};
+
+__host__ __device__ inline size_t align_up_t(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline TCLayout tc_layout(int r, int na, int nstage) {
+  TCLayout L;
+  L.nslab = (r + 63) / 64;
+  L.na = na;
+  L.nstage = nstage;
+  size_t off = 0;
+  L.a = off;
+  off += (size_t)na * L.nslab * kSlab;
+  L.ring = off;
+  off += (size_t)nstage * kSlab;
+  L.scratch = off;
+  off = align_up_t(off + kM * sizeof(TSlot), 128);
+  L.misc = off;
+  off = align_up_t(off + sizeof(TMisc), 128);
+  L.bars = off;
+  off += (size_t)(2 * nstage + 2 * kAcc + 2 * na + 2) * 8;
+  L.total = align_up_t(off, 1024) + 1024;  // + slack to align the dynamic base to 1024
+  return L;
+}
+
+template <int NT>
+__device__ __forceinline__ void esync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+template <int NT>
+__device__ __forceinline__ int esync_or(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "n"(NT)
+      : "memory");
+  return r;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort || globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ float ld_u(const void* p, size_t i, int bf16) {
+  return bf16 ? __bfloat162float(((const __nv_bfloat16*)p)[i]) : ((const float*)p)[i];
+}
+
+__device__ __forceinline__ void tslot_init(TSlot& s) {
+  s.best = -INFINITY;
+  s.tok = 0xFFFFFFFFu;
+  s.m = -INFINITY;
+  s.l = 0.f;
+  s.mt = -INFINITY;
+  s.lt = 0.f;
+}
+
+// (max, sum-exp) of all blocks' partials, merged by one warp in a fixed order
+__device__ __forceinline__ float2 merge_ml(const float2* part, int n, int lane) {
+  float m = -INFINITY, l = 0.f;
+  for (int i = lane; i < n; i += 32) {
+    const float2 q = part[i];
+    lse_merge(m, l, q.x, q.y);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+    lse_merge(m, l, m2, l2);
+  }
+  return make_float2(m, l);
+}
+
+// Conditioning token of step ks for request b and whether the request is still valid.
+__device__ __forceinline__ int cond_token(const DraftParams& p, int b, int ks, bool* valid) {
+  const int V = p.V, G = p.gamma;
+  int x = p.x0[b];
+  bool ok = x >= 0 && x < V;
+  if (p.forced) {
+    for (int j = 0; j < ks && ok; ++j) {
+      const int f = p.forced[(size_t)b * G + j];
+      ok = f >= 0 && f < V;
+    }
+    if (ks > 0 && ok) x = p.forced[(size_t)b * G + ks - 1];
+  } else if (ks > 0 && ok) {
+    x = (int)key_token(ld_acquire64(&p.keys[(size_t)(ks - 1) * p.B + b]));
+    ok = x >= 0 && x < V;
+  }
+  *valid = ok;
+  return ok ? x : 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    draft_tc_kernel(const DraftParams p, const __grid_constant__ CUtensorMap tmap_w2, int na,
+                    int nstage) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const TCLayout Lay = tc_layout(p.r, na, nstage);
+  uint8_t* abuf = smem + Lay.a;
+  uint8_t* ring = smem + Lay.ring;
+  TSlot* scratch = (TSlot*)(smem + Lay.scratch);
+  TMisc* ms = (TMisc*)(smem + Lay.misc);
+  uint64_t* full = (uint64_t*)(smem + Lay.bars);
+  uint64_t* empty = full + nstage;
+  uint64_t* acc_full = empty + nstage;
+  uint64_t* acc_empty = acc_full + kAcc;
+  uint64_t* a_full = acc_empty + kAcc;
+  uint64_t* a_empty = a_full + na;
+  uint64_t* tmem_done = a_empty + na;
+  uint64_t* mma_done = tmem_done + 1;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nCTA = gridDim.x, cta = blockIdx.x;
+  const int B = p.B, G = p.gamma, V = p.V, r = p.r;
+  const int nslab = Lay.nslab;
+  const int nchunk = (B + kM - 1) / kM;
+  const bool tgt = p.target != nullptr;
+  WsHeader* hdr = p.hdr;
+
+  // vocab tiles of this block
+  const int ntile_all = (V + kNT - 1) / kNT;
+  const int t0 = (int)(((long long)ntile_all * cta) / nCTA);
+  const int t1 = (int)(((long long)ntile_all * (cta + 1)) / nCTA);
+  const int ntile = t1 - t0;
+  const int sl0 = t0 * kNT, sl1 = min(V, t1 * kNT);  // vocab slice [sl0, sl1)
+
+  if (tid == 0) {
+    for (int i = 0; i < nstage; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < kAcc; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpiWarps);
+    }
+    for (int i = 0; i < na; ++i) {
+      mbar_init(&a_full[i], 1);
+      mbar_init(&a_empty[i], 1);
+    }
+    mbar_init(tmem_done, kEpiWarps);
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+    ms->abort = 0;
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&ms->tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();  // last block-wide barrier: roles split from here
+  tc::fence_after_sync();
+  const uint32_t tmem = ms->tmem_base;
+
+  // =========================================================== producer: W2 slabs
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();
+      int g = 0;
+      bool stop = false;
+      for (int ks = 0; ks < G && !stop; ++ks)
+        for (int c = 0; c < nchunk && !stop; ++c)
+          for (int t = 0; t < ntile && !stop; ++t)
+            for (int s = 0; s < nslab; ++s, ++g) {
+              const int slot = g % nstage;
+              if (g >= nstage &&
+                  !wait_or_abort(&empty[slot], (uint32_t)(((g / nstage) - 1) & 1), &ms->abort)) {
+                stop = true;
+                break;
+              }
+              mbar_expect_tx(&full[slot], kSlab);
+              tc::tma_load_2d(ring + (size_t)slot * kSlab, &tmap_w2, s * 64, (t0 + t) * kNT,
+                              &full[slot], pol);
+            }
+      if (stop) atomicMax(&hdr->status, kErrTimeout);
+      for (int k = max(0, g - nstage); k < g; ++k)  // every copy must land before exit
+        mbar_wait(&full[k % nstage], (uint32_t)((k / nstage) & 1));
+    }
+    return;
+  }
+
+  // =========================================================== MMA issuer + TMEM owner
+  if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16_f32(kM, kNT);
+      int g = 0, acc_i = 0;
+      bool stop = false;
+      for (int ks = 0; ks < G && !stop; ++ks)
+        for (int c = 0; c < nchunk && !stop; ++c) {
+          const int u = ks * nchunk + c, ab = u % na;
+          if (!wait_or_abort(&a_full[ab], (uint32_t)((u / na) & 1), &ms->abort)) {
+            stop = true;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t a_base = smem_u32(abuf + (size_t)ab * nslab * kSlab);
+          for (int t = 0; t < ntile && !stop; ++t, ++acc_i) {
+            const int acc = acc_i % kAcc;
+            if (acc_i >= kAcc &&
+                !wait_or_abort(&acc_empty[acc], (uint32_t)(((acc_i / kAcc) - 1) & 1), &ms->abort)) {
+              stop = true;
+              break;
+            }
+            tc::fence_after_sync();
+            for (int s = 0; s < nslab; ++s, ++g) {
+              const int slot = g % nstage;
+              if (!wait_or_abort(&full[slot], (uint32_t)((g / nstage) & 1), &ms->abort)) {
+                stop = true;
+                break;
+              }
+              tc::fence_after_sync();
+              const uint32_t b_base = smem_u32(ring + (size_t)slot * kSlab);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                tc::mma_bf16(tmem + acc * kNT, tc::sdesc_sw128(a_base + s * kSlab + kk * 32),
+                             tc::sdesc_sw128(b_base + kk * 32), idesc, (s | kk) != 0);
+              tc::mma_commit(&empty[slot]);
+            }
+            if (!stop) tc::mma_commit(&acc_full[acc]);
+          }
+          if (!stop) tc::mma_commit(&a_empty[ab]);
+        }
+      if (stop) atomicMax(&hdr->status, kErrTimeout);
+      tc::mma_commit(mma_done);  // arrives once every MMA issued above has completed
+      mbar_wait(mma_done, 0);
+    }
+    __syncwarp();
+    // TMEM is freed only after the epilogue is done reading it
+    if (lane == 0) wait_or_abort(tmem_done, 0, &ms->abort);
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
+  if (warp < 4) return;
+
+  // =========================================================== epilogue warps
+  const int et = tid - 128;          // 0..255
+  const int ew = warp - 4;           // 0..7
+  const int q = warp & 3;            // TMEM lane quarter
+  const int hcol = ew >> 2;          // column half of each tile
+  const int m = 32 * q + lane;       // request within a chunk (TMEM lane)
+  const int gm = et & (kM - 1), gh = et >> 7;  // gather role: row, half of the row's chunks
+  const int nchk = r / 8;            // 16-byte chunks of a W1 row
+  int acc_i = 0;
+  bool failed = false;
+
+  for (int ks = 0; ks < G && !failed; ++ks) {
+    for (int c = 0; c < nchunk && !failed; ++c) {
+      const int u = ks * nchunk + c, ab = u % na;
+      // ---- A operand: the chunk's conditioning rows W1[x_{k-1}], swizzled K-major bf16
+      if (u >= na) {
+        const bool ok = wait_or_abort(&a_empty[ab], (uint32_t)(((u / na) - 1) & 1), &ms->abort);
+        if (esync_or<kEpiThreads>(!ok)) {
+          failed = true;
+          break;
+        }
+      }
+      {
+        const int b = c * kM + gm;
+        bool valid = false;
+        const int x = b < B ? cond_token(p, b, ks, &valid) : 0;
+        const uint4* src = (const uint4*)((const __nv_bfloat16*)p.W1 + (size_t)x * r);
+        uint8_t* dst = abuf + (size_t)ab * nslab * kSlab + (gm >> 3) * 1024 + (gm & 7) * 128;
+        for (int j = gh; j < nslab * 8; j += 2) {
+          const uint4 val = (valid && j < nchk) ? src[j] : make_uint4(0, 0, 0, 0);
+          *(uint4*)(dst + (j >> 3) * kSlab + (((j & 7) ^ (gm & 7)) << 4)) = val;
+        }
+      }
+      fence_proxy_async_smem();
+      esync<kEpiThreads>();
+      if (et == 0) mbar_arrive(&a_full[ab]);
+
+      // ---- tiles: bias from TMEM, logits, sampling, normalisers
+      const int b = c * kM + m;
+      const bool row_ok = b < B;
+      TSlot st;
+      tslot_init(st);
+      float C = INFINITY;  // exp(m - best) of this thread's running state
+      for (int t = 0; t < ntile; ++t, ++acc_i) {
+        const int acc = acc_i % kAcc;
+        const bool ok = wait_or_abort(&acc_full[acc], (uint32_t)((acc_i / kAcc) & 1), &ms->abort);
+        if (!__all_sync(0xffffffffu, ok)) {
+          failed = true;
+          break;
+        }
+        tc::fence_after_sync();
+        uint32_t bias[2][32];
+        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + acc * kNT + hcol * 64;
+        tc::tmem_ld32(ta, bias[0]);
+        tc::tmem_ld32(ta + 32, bias[1]);
+        tc::tmem_ld_wait();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        const int vb = (t0 + t) * kNT + hcol * 64;  // first vocab entry of this thread's 64
+        if (!row_ok || vb >= V) continue;
+        const size_t urow = ((size_t)b * G + ks) * V;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const int v = vb + hh * 32 + j;
+            const U4 rq = philox4x32_10((uint32_t)(v >> 2), (uint32_t)ks, (uint32_t)b, kNoiseTag,
+                                        p.seed_lo, p.seed_hi);
+            const uint32_t words[4] = {rq.x, rq.y, rq.z, rq.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int vv = v + e;
+              if (vv >= V) continue;
+              const float z = ld_u(p.U, urow + vv, p.u_bf16) + __uint_as_float(bias[hh][j + e]);
+              if (p.logits) p.logits[urow + vv] = z;
+              const float y = z * p.invT;
+              float pe;
+              if (y > st.m) {
+                st.l = st.l * __expf(st.m - y) + 1.f;
+                st.m = y;
+                pe = 1.f;
+                C = __expf(st.m - st.best);
+              } else {
+                pe = __expf(y - st.m);
+                st.l += pe;
+              }
+              // exact skip: w = 1 - u; -ln u >= w, so w >= 1.001 exp(y - best) rules it out
+              const float w = bits_to_uniform(~words[e]);
+              if (!(w >= 1.001f * (pe * C))) {
+                const float sc = y + gumbel_from_uniform(bits_to_uniform(words[e]));
+                if (sc > st.best) {  // vv grows along this thread's sequence: ties keep the smaller
+                  st.best = sc;
+                  st.tok = (uint32_t)vv;
+                  C = __expf(st.m - st.best);
+                }
+              }
+              if (tgt) {
+                lse_push(st.mt, st.lt, p.target[urow + vv] * p.invT);
+                p.ybuf[(size_t)b * V + vv] = y;
+              }
+            }
+          }
+        }
+      }
+      if (esync_or<kEpiThreads>(failed)) {
+        failed = true;
+        break;
+      }
+      // ---- merge the two column halves of each request, publish the block's candidate
+      if (hcol == 1) scratch[m] = st;
+      esync<kEpiThreads>();
+      if (hcol == 0 && row_ok) {
+        const TSlot& o = scratch[m];
+        best_merge(st.best, st.tok, o.best, o.tok);
+        lse_merge(st.m, st.l, o.m, o.l);
+        lse_merge(st.mt, st.lt, o.mt, o.lt);
+        bool valid = false;
+        cond_token(p, b, ks, &valid);
+        if (valid && ntile > 0 && sl1 > sl0) atomicMax(&p.keys[(size_t)ks * B + b], make_key(st.best, st.tok));
+        p.ml[((size_t)ks * B + b) * nCTA + cta] = make_float2(st.m, st.l);
+        if (tgt) p.mlt[((size_t)ks * B + b) * nCTA + cta] = make_float2(st.mt, st.lt);
+      }
+      esync<kEpiThreads>();
+    }
+    if (failed) break;
+
+    // ---- every block has published step ks
+    esync<kEpiThreads>();
+    if (et == 0) {
+      int ok = 1;
+      __threadfence();
+      red_release_add(&hdr->arrive, 1u);
+      const unsigned target = (unsigned)(ks + 1) * gridDim.x;
+      if (ld_acquire(&hdr->arrive) < target) {
+        const unsigned long long tw = globaltimer();
+        while (ld_acquire(&hdr->arrive) < target) {
+          if (globaltimer() - tw > kWaitLimitNs) {
+            ok = 0;
+            break;
+          }
+          __nanosleep(32);
+        }
+      }
+      __threadfence();
+      ms->flag = ok;
+    }
+    esync<kEpiThreads>();
+    if (!ms->flag) {
+      failed = true;
+      break;
+    }
+
+    if (tgt) {
+      // ---- Eq 8 second pass over this block's slice, all requests: normalisers of p^d, p^t
+      for (int b = 0; b < B; ++b) {
+        if (ew == (b % kEpiWarps)) {
+          const float2 a = merge_ml(p.ml + ((size_t)ks * B + b) * nCTA, nCTA, lane);
+          const float2 tt = merge_ml(p.mlt + ((size_t)ks * B + b) * nCTA, nCTA, lane);
+          float acc = 0.f;
+          const float Ld = a.x + logf(a.y), Lt = tt.x + logf(tt.y);
+          const size_t trow = ((size_t)b * G + ks) * V;
+          for (int v = sl0 + lane; v < sl1; v += 32)
+            acc += fabsf(__expf(p.ybuf[(size_t)b * V + v] - Ld) - __expf(p.target[trow + v] * p.invT - Lt));
+          acc = warp_sum(acc);
+          if (lane == 0) p.l1p[((size_t)ks * B + b) * nCTA + cta] = acc;
+        }
+      }
+      esync<kEpiThreads>();
+    }
+  }
+
+  // release TMEM to its owner (also on the failure path)
+  tc::fence_before_sync();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(tmem_done);
+  if (failed) {
+    ms->abort = 1;
+    if (et == 0) atomicMax(&hdr->status, kErrTimeout);
+    return;
+  }
+
+  // ---- owned requests (b % nCTA == cta): tokens, log-normalisers, Eq 7 / S_k, Eq 8
+  for (int b = cta + ew * nCTA; b < B; b += kEpiWarps * nCTA) {
+    float surv = 1.f;
+    bool alive = true;
+    for (int k = 0; k < G; ++k) {
+      const size_t o = (size_t)b * G + k;
+      bool valid = false;
+      const int x = cond_token(p, b, k, &valid);
+      if (alive && !valid && lane == 0) atomicMax(&hdr->status, kErrInvalid);
+      alive = alive && valid;
+      const int tok = alive ? (int)key_token(ld_acquire64(&p.keys[(size_t)k * B + b])) : -1;
+      const float2 ml = merge_ml(p.ml + ((size_t)k * B + b) * nCTA, nCTA, lane);
+      if (p.h && p.w) {
+        float acc = 0.f;
+        for (int j = lane; j < p.d; j += 32)
+          acc += ld_u(p.w, j, 1) * ld_u(p.h, o * p.d + j, p.u_bf16);
+        for (int j = lane; j < r; j += 32)
+          acc += ld_u(p.w, (size_t)p.d + j, 1) * ld_u(p.W1, (size_t)x * r + j, 1);
+        acc = warp_sum(acc);
+        const float cv = alive ? sigmoidf_acc(acc) : NAN;
+        surv = alive ? surv * cv : NAN;
+        if (lane == 0) {
+          p.c[o] = cv;
+          p.S[o] = surv;
+        }
+      }
+      if (lane == 0) {
+        p.tokens[o] = tok;
+        p.lse[o] = alive ? ml.x + logf(ml.y) : NAN;
+      }
+      if (tgt && k + 1 < G) {
+        float s = 0.f;
+        for (int i = lane; i < nCTA; i += 32) s += p.l1p[((size_t)k * B + b) * nCTA + i];
+        s = warp_sum(s);
+        if (lane == 0) {
+          p.l1[o] = alive ? s : NAN;
+          p.cstar[o] = alive ? fminf(1.f, fmaxf(0.f, 1.f - 0.5f * s)) : NAN;
+        }
+      }
+    }
+  }
+
+  // last block out: Eq 8 of the final step; leave the workspace ready for the next call
+  esync<kEpiThreads>();
+  if (et == 0) {
+    __threadfence();
+    const unsigned old = atomicAdd(&hdr->exit_count, 1u);
+    ms->last = (old == (unsigned)nCTA - 1u);
+  }
+  esync<kEpiThreads>();
+  if (ms->last) {
+    __threadfence();
+    if (tgt)
+      for (int b = ew; b < B; b += kEpiWarps) {
+        float s = 0.f;
+        for (int i = lane; i < nCTA; i += 32) s += p.l1p[((size_t)(G - 1) * B + b) * nCTA + i];
+        s = warp_sum(s);
+        if (lane == 0) {
+          const size_t o = (size_t)b * G + G - 1;
+          const bool vb = ((volatile int32_t*)p.tokens)[o] >= 0;
+          p.l1[o] = vb ? s : NAN;
+          p.cstar[o] = vb ? fminf(1.f, fmaxf(0.f, 1.f - 0.5f * s)) : NAN;
+        }
+      }
+    for (int i = et; i < G * B; i += kEpiThreads) p.keys[i] = 0ull;
+    esync<kEpiThreads>();
+    if (et == 0) {
+      hdr->arrive = 0;
+      hdr->exit_count = 0;
+      __threadfence();
+    }
+  }
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiled)f;
+  }
+  return fn;
+}
+
+}  // namespace
+
+int draft_tc_supported(int B, int r, int w_bf16) { return w_bf16 && B >= 1 && r % 8 == 0 && r <= 512; }
+
+bool draft_tc_configure(DraftParams& p, size_t smem_optin) {
+  // two A buffers when they fit next to at least 4 ring stages, else one
+  for (int na = 2; na >= 1; --na) {
+    for (int ns = 8; ns >= 3; --ns) {
+      const TCLayout L = tc_layout(p.r, na, ns);
+      if (L.total <= smem_optin) {
+        p.tc_na = na;
+        p.nstages = ns;
+        p.smem_bytes = L.total;
+        return true;
+      }
+    }
+  }
+  return false;
+}
+
+cudaError_t launch_draft_tc(DraftParams& p, int nblocks, cudaStream_t stream) {
+  EncodeTiled enc = encoder();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap tmap;
+  const cuuint64_t gdim[2] = {(cuuint64_t)p.r, (cuuint64_t)p.V};
+  const cuuint64_t gstride[1] = {(cuuint64_t)p.r * 2};
+  const cuuint32_t box[2] = {64, kNT};
+  const cuuint32_t estride[2] = {1, 1};
+  CUresult cr = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.W2), gdim,
+                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(draft_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)p.smem_bytes);
+  if (e != cudaSuccess) return e;
+  int na = p.tc_na, ns = p.nstages;
+  void* args[] = {(void*)&p, (void*)&tmap, (void*)&na, (void*)&ns};
+  return cudaLaunchCooperativeKernel((const void*)draft_tc_kernel, dim3(nblocks), dim3(kThreads),
+                                     args, p.smem_bytes, stream);
+}
+
+}  // namespace dspark

@@ -95,3 +95,33 @@ def compare_floats(out, o, rows=None, logits=True):
     if o.s_final is not None and out.s_out is not None:
         errs["s_out"] = close("s_out", sel(out.s_out.cpu().numpy()), o.s_final)
     return errs
+
+
+def run_case(wl, *, target_noise=None, want_logits=True, rows=None, check_free=True, ds=None):
+    """Free-running and teacher-forced GPU draft against the oracle on the same inputs."""
+    if target_noise is not None:
+        wl = wl.with_(target_noise=target_noise)
+    t = inputs.generate(wl)
+    d = to_dev(t)
+    o = oracle_draft(wl, t, rows=rows, want_z=want_logits)
+    assert o.status == 0
+    has_t = d.get("target") is not None
+    ws = ds.Workspace(0, wl.B, wl.gamma, wl.V, wl.r, wl.d, target=has_t)
+    kw = dict(T=wl.T, seed=wl.seed, h=d["h"], w=d["w"], target=d.get("target"), workspace=ws)
+    sel = (lambda a: a) if rows is None else (lambda a: a[rows])
+    ties = 0
+    if check_free:
+        free = ds.markov_draft(d["W1"], d["W2"], d["U"], d["x0"], **kw)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
+        ties += check_tokens_free(sel(free.tokens.cpu().numpy()), o)
+    forced = np.zeros((wl.B, wl.gamma), np.int32)
+    forced[rows if rows is not None else slice(None)] = o.tokens
+    tf = ds.markov_draft(d["W1"], d["W2"], d["U"], d["x0"], forced=torch.from_numpy(forced).cuda(),
+                         want_logits=want_logits, **kw)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    ties += check_tokens_forced(sel(tf.tokens.cpu().numpy()), o)
+    errs = compare_floats(tf, o, rows=rows, logits=want_logits)
+    print(f"{wl.name} B={wl.B} V={wl.V} r={wl.r}: near-ties {ties}, max errors {errs}")
+    return ties, errs

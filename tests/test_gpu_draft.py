@@ -19,32 +19,8 @@ pytestmark = pytest.mark.gpu
 TINY = inputs.WORKLOADS["tiny_markov"]
 
 
-def _run_case(wl, *, target_noise=None, want_logits=True, rows=None, check_free=True):
-    if target_noise is not None:
-        wl = wl.with_(target_noise=target_noise)
-    t = inputs.generate(wl)
-    d = parity.to_dev(t)
-    o = parity.oracle_draft(wl, t, rows=rows, want_z=want_logits)
-    assert o.status == 0
-    ws = ds.Workspace(0, wl.B, wl.gamma, wl.V, wl.r, wl.d)
-    kw = dict(T=wl.T, seed=wl.seed, h=d["h"], w=d["w"], target=d.get("target"), workspace=ws)
-    sel = (lambda a: a) if rows is None else (lambda a: a[rows])
-    ties = 0
-    if check_free:
-        free = ds.markov_draft(d["W1"], d["W2"], d["U"], d["x0"], **kw)
-        torch.cuda.synchronize()
-        assert ws.status() == 0
-        ties += parity.check_tokens_free(sel(free.tokens.cpu().numpy()), o)
-    forced = np.zeros((wl.B, wl.gamma), np.int32)
-    forced[rows if rows is not None else slice(None)] = o.tokens
-    tf = ds.markov_draft(d["W1"], d["W2"], d["U"], d["x0"], forced=torch.from_numpy(forced).cuda(),
-                         want_logits=want_logits, **kw)
-    torch.cuda.synchronize()
-    assert ws.status() == 0
-    ties += parity.check_tokens_forced(sel(tf.tokens.cpu().numpy()), o)
-    errs = parity.compare_floats(tf, o, rows=rows, logits=want_logits)
-    print(f"{wl.name} B={wl.B} V={wl.V}: near-ties {ties}, max errors {errs}")
-    return ties, errs
+def _run_case(wl, **kw):
+    return parity.run_case(wl, ds=ds, **kw)
 
 
 def test_tiny_markov_workload():
@@ -119,7 +95,7 @@ def test_invalid_anchor_sets_status():
 def test_repeat_runs_are_bit_identical():
     wl = inputs.WORKLOADS["qwen3_4b_markov"].with_(V=50000, d=256, B=4, seed=41)
     t = parity.to_dev(inputs.generate(wl.with_(target_noise=1.0)))
-    ws = ds.Workspace(0, wl.B, wl.gamma, wl.V, wl.r, wl.d)
+    ws = ds.Workspace(0, wl.B, wl.gamma, wl.V, wl.r, wl.d, target=True)
     runs = [ds.markov_draft(t["W1"], t["W2"], t["U"], t["x0"], h=t["h"], w=t["w"],
                             target=t["target"], seed=7, workspace=ws) for _ in range(3)]
     torch.cuda.synchronize()
