@@ -8,8 +8,9 @@
 //     K-major layout by the epilogue warps, B (W2 rows, stored [V][r]) arrives by 2-D TMA;
 //     the fp32 accumulator lives in TMEM (4 buffers of 128 columns);
 //   * warp 0 produces W2 slabs (runs ahead across tiles, chunks and steps), warp 1 issues the
-//     MMAs from one thread and owns TMEM, warps 4..11 are the epilogue: two warps per TMEM lane
-//     quarter, each taking 64 of a tile's 128 columns for its 32 requests;
+//     MMAs from one thread and owns TMEM, warps 4..19 are the epilogue: four warps per TMEM
+//     lane quarter, each taking 32 of a tile's 128 columns for its 32 requests, with U and the
+//     target fetched as 16-byte vectors issued before the accumulator wait;
 //   * the epilogue fuses +U_k, /T, the online (max, sum-exp), and Gumbel-max sampling with an
 //     exact skip: with w = 1 - u (exact from the Philox bits) and q = exp(y - best), an entry
 //     with w >= 1.001 q cannot beat the running best (-ln u >= w, so its score is below
@@ -25,7 +26,7 @@
 namespace dspark {
 namespace {
 
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = 4 * 32 + kEpiThreads;  // producer, MMA, two spare warps, epilogue
 constexpr int kM = 128;                          // requests per chunk
@@ -66,7 +67,7 @@ __host__ __device__ inline TCLayout tc_layout(int r, int na, int nstage) {
   L.ring = off;
   off += (size_t)nstage * kSlab;
   L.scratch = off;
-  off = align_up_t(off + kM * sizeof(TSlot), 128);
+  off = align_up_t(off + 3 * kM * sizeof(TSlot), 128);
   L.misc = off;
   off = align_up_t(off + sizeof(TMisc), 128);
   L.bars = off;
@@ -294,13 +295,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) return;
 
   // =========================================================== epilogue warps
-  const int et = tid - 128;          // 0..255
-  const int ew = warp - 4;           // 0..7
+  const int et = tid - 128;          // 0..511
+  const int ew = warp - 4;           // 0..15
   const int q = warp & 3;            // TMEM lane quarter
-  const int hcol = ew >> 2;          // column half of each tile
+  const int cq = ew >> 2;            // 32-column quarter of each tile
   const int m = 32 * q + lane;       // request within a chunk (TMEM lane)
-  const int gm = et & (kM - 1), gh = et >> 7;  // gather role: row, half of the row's chunks
+  const int gm = et & (kM - 1), gh = et >> 7;  // gather role: row, quarter of the row's chunks
   const int nchk = r / 8;            // 16-byte chunks of a W1 row
+  // 16-byte vector loads of U (bf16) and the target need 16-byte aligned rows
+  const bool vec_u = p.u_bf16 && (V % 8) == 0;
+  const bool vec_t = (V % 4) == 0;
   int acc_i = 0;
   bool failed = false;
 
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int x = b < B ? cond_token(p, b, ks, &valid) : 0;
         const uint4* src = (const uint4*)((const __nv_bfloat16*)p.W1 + (size_t)x * r);
         uint8_t* dst = abuf + (size_t)ab * nslab * kSlab + (gm >> 3) * 1024 + (gm & 7) * 128;
-        for (int j = gh; j < nslab * 8; j += 2) {
+        for (int j = gh; j < nslab * 8; j += 4) {
           const uint4 val = (valid && j < nchk) ? src[j] : make_uint4(0, 0, 0, 0);
           *(uint4*)(dst + (j >> 3) * kSlab + (((j & 7) ^ (gm & 7)) << 4)) = val;
         }
@@ -333,67 +337,92 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- tiles: bias from TMEM, logits, sampling, normalisers
       const int b = c * kM + m;
       const bool row_ok = b < B;
+      const size_t urow = ((size_t)b * G + ks) * V;
       TSlot st;
       tslot_init(st);
       float C = INFINITY;  // exp(m - best) of this thread's running state
       for (int t = 0; t < ntile; ++t, ++acc_i) {
         const int acc = acc_i % kAcc;
+        const int vb = (t0 + t) * kNT + cq * 32;  // first vocab entry of this thread's 32
+        const bool whole = row_ok && vb + 32 <= V;
+        // U and target of this thread's 32 entries, in flight while the MMA finishes
+        uint4 uq[4];
+        if (whole && vec_u) {
+          const uint4* up = (const uint4*)((const __nv_bfloat16*)p.U + urow + vb);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) uq[i] = __ldcs(up + i);
+        }
         const bool ok = wait_or_abort(&acc_full[acc], (uint32_t)((acc_i / kAcc) & 1), &ms->abort);
         if (!__all_sync(0xffffffffu, ok)) {
           failed = true;
           break;
         }
         tc::fence_after_sync();
-        uint32_t bias[2][32];
-        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + acc * kNT + hcol * 64;
-        tc::tmem_ld32(ta, bias[0]);
-        tc::tmem_ld32(ta + 32, bias[1]);
+        uint32_t bias[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + acc * kNT + cq * 32, bias);
         tc::tmem_ld_wait();
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
-        const int vb = (t0 + t) * kNT + hcol * 64;  // first vocab entry of this thread's 64
         if (!row_ok || vb >= V) continue;
-        const size_t urow = ((size_t)b * G + ks) * V;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int j = 0; j < 32; j += 4) {
+          const int v = vb + j;
+          const U4 rq = philox4x32_10((uint32_t)(v >> 2), (uint32_t)ks, (uint32_t)b, kNoiseTag,
+                                      p.seed_lo, p.seed_hi);
+          const uint32_t words[4] = {rq.x, rq.y, rq.z, rq.w};
+          float yq[4];
+          float4 tq4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (tgt && whole && vec_t) tq4 = __ldcs((const float4*)(p.target + urow + v));
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            const int v = vb + hh * 32 + j;
-            const U4 rq = philox4x32_10((uint32_t)(v >> 2), (uint32_t)ks, (uint32_t)b, kNoiseTag,
-                                        p.seed_lo, p.seed_hi);
-            const uint32_t words[4] = {rq.x, rq.y, rq.z, rq.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int vv = v + e;
-              if (vv >= V) continue;
-              const float z = ld_u(p.U, urow + vv, p.u_bf16) + __uint_as_float(bias[hh][j + e]);
-              if (p.logits) p.logits[urow + vv] = z;
-              const float y = z * p.invT;
-              float pe;
-              if (y > st.m) {
-                st.l = st.l * __expf(st.m - y) + 1.f;
-                st.m = y;
-                pe = 1.f;
+          for (int e = 0; e < 4; ++e) {
+            const int vv = v + e;
+            float uval, tval = 0.f;
+            if (whole && vec_u) {
+              const uint32_t wd = ((const uint32_t*)&uq[(j + e) >> 3])[((j + e) & 7) >> 1];
+              uval = __uint_as_float(((j + e) & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
+            } else {
+              uval = vv < V ? ld_u(p.U, urow + vv, p.u_bf16) : 0.f;
+            }
+            if (tgt) {
+              if (whole && vec_t) tval = ((const float*)&tq4)[e];
+              else tval = vv < V ? p.target[urow + vv] : 0.f;
+            }
+            yq[e] = 0.f;
+            if (vv >= V) continue;
+            const float z = uval + __uint_as_float(bias[j + e]);
+            if (p.logits) p.logits[urow + vv] = z;
+            const float y = z * p.invT;
+            yq[e] = y;
+            float pe;
+            if (y > st.m) {
+              st.l = st.l * __expf(st.m - y) + 1.f;
+              st.m = y;
+              pe = 1.f;
+              C = __expf(st.m - st.best);
+            } else {
+              pe = __expf(y - st.m);
+              st.l += pe;
+            }
+            // exact skip: w = 1 - u; -ln u >= w, so w >= 1.001 exp(y - best) rules it out
+            const float w = bits_to_uniform(~words[e]);
+            if (!(w >= 1.001f * (pe * C))) {
+              const float sc = y + gumbel_from_uniform(bits_to_uniform(words[e]));
+              if (sc > st.best) {  // vv grows along this thread's sequence: ties keep the smaller
+                st.best = sc;
+                st.tok = (uint32_t)vv;
                 C = __expf(st.m - st.best);
-              } else {
-                pe = __expf(y - st.m);
-                st.l += pe;
               }
-              // exact skip: w = 1 - u; -ln u >= w, so w >= 1.001 exp(y - best) rules it out
-              const float w = bits_to_uniform(~words[e]);
-              if (!(w >= 1.001f * (pe * C))) {
-                const float sc = y + gumbel_from_uniform(bits_to_uniform(words[e]));
-                if (sc > st.best) {  // vv grows along this thread's sequence: ties keep the smaller
-                  st.best = sc;
-                  st.tok = (uint32_t)vv;
-                  C = __expf(st.m - st.best);
-                }
-              }
-              if (tgt) {
-                lse_push(st.mt, st.lt, p.target[urow + vv] * p.invT);
-                p.ybuf[(size_t)b * V + vv] = y;
-              }
+            }
+            if (tgt) lse_push(st.mt, st.lt, tval * p.invT);
+          }
+          if (tgt) {
+            if (whole && vec_t) {
+              *(float4*)(p.ybuf + (size_t)b * V + v) = make_float4(yq[0], yq[1], yq[2], yq[3]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (v + e < V) p.ybuf[(size_t)b * V + v + e] = yq[e];
             }
           }
         }
@@ -402,14 +431,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         failed = true;
         break;
       }
-      // ---- merge the two column halves of each request, publish the block's candidate
-      if (hcol == 1) scratch[m] = st;
+      // ---- merge the column quarters of each request in a fixed order, publish the candidate
+      if (cq > 0) scratch[(cq - 1) * kM + m] = st;
       esync<kEpiThreads>();
-      if (hcol == 0 && row_ok) {
-        const TSlot& o = scratch[m];
-        best_merge(st.best, st.tok, o.best, o.tok);
-        lse_merge(st.m, st.l, o.m, o.l);
-        lse_merge(st.mt, st.lt, o.mt, o.lt);
+      if (cq == 0 && row_ok) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+          const TSlot& o = scratch[i * kM + m];
+          best_merge(st.best, st.tok, o.best, o.tok);
+          lse_merge(st.m, st.l, o.m, o.l);
+          lse_merge(st.mt, st.lt, o.mt, o.lt);
+        }
         bool valid = false;
         cond_token(p, b, ks, &valid);
         if (valid && ntile > 0 && sl1 > sl0) atomicMax(&p.keys[(size_t)ks * B + b], make_key(st.best, st.tok));
