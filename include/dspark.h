@@ -120,8 +120,10 @@ dspark_status dspark_markov_draft(int B, int gamma, int V, int r, int d, float T
  *   s_k = sigmoid(g) * s_{k-1} + (1 - sigmoid(g)) * tanh(c),  B_k = tanh(o) . W2^T.
  * B_k is built from z_k, i.e. from s_{k-1}.  s0: [B][r] fp32 initial state or NULL for zeros.
  * s_out: [B][r] fp32 final state s_gamma, or NULL.  Eq 7 is unchanged (uses W1[x_{k-1}]).
- * h is required (it feeds Eq 6); w may be NULL (then c, S are NULL).  All other arguments,
- * outputs and errors as dspark_markov_draft.
+ * h is required (it feeds Eq 6, d > 0); w may be NULL (then c, S are NULL).  Weights and
+ * activations must be bf16 (DSPARK_ERR_UNSUPPORTED otherwise): the h_k columns of the joint
+ * projection are computed for all (b, k) up front by a tensor-core GEMM, a second launch on the
+ * same stream.  All other arguments, outputs and errors as dspark_markov_draft.
  */
 dspark_status dspark_rnn_draft(int B, int gamma, int V, int r, int d, float T, uint64_t seed,
                                dspark_dtype wdt, const void* W1, const void* W2, const void* w,

@@ -62,7 +62,7 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 struct WsLayout {
-  size_t keys, hdot, ml, mlt, l1p, rnn_s, rnn_a, rnn_gh, ybuf, total;
+  size_t keys, hdot, ml, mlt, l1p, rnn_s, rnn_a, rnn_gh, rnn_flag, ybuf, total;
 };
 
 // flags: DSPARK_WS_TARGET reserves the y buffer the tensor-core path needs for Eq 8
@@ -79,12 +79,15 @@ WsLayout ws_layout(int head, int B, int G, int V, int r, int nCTA, int flags) {
   off = align256(off + (size_t)G * B * nCTA * 8);
   L.l1p = off;
   off = align256(off + (size_t)G * B * nCTA * 4);
+  const bool rnn = head == 1;
   L.rnn_s = off;
-  off = align256(off + (head == 1 ? (size_t)2 * B * r * 4 : 0));
+  off = align256(off + (rnn ? (size_t)B * r * 4 : 0));
   L.rnn_a = off;
-  off = align256(off + (head == 1 ? (size_t)B * r * 4 : 0));
+  off = align256(off + (rnn ? (size_t)G * B * r * 4 : 0));
   L.rnn_gh = off;
-  off = align256(off + (head == 1 ? (size_t)B * G * 3 * r * 4 : 0));
+  off = align256(off + (rnn ? (size_t)kRnnMaxSplit * B * G * 3 * r * 4 : 0));
+  L.rnn_flag = off;
+  off = align256(off + (rnn ? (size_t)G * B * 4 : 0));
   L.ybuf = off;
   off = align256(off + ((flags & DSPARK_WS_TARGET) && B > 4 ? (size_t)B * V * 4 : 0));
   L.total = off;
@@ -97,7 +100,7 @@ bool shape_ok(int head, int B, int G, int V, int r, int d) {
 }
 
 int path_of(int head, int B, int r, int w_bf16) {
-  if (head == 1) return -1;  // the RNN head is not in this build yet
+  if (head == 1 && !w_bf16) return -1;  // the RNN pre-pass is a bf16 tensor-core GEMM
   if (draft_cc_supported(B, r, w_bf16)) return 0;
   if (draft_tc_supported(B, r, w_bf16)) return 1;
   return -1;
@@ -133,9 +136,14 @@ dspark_status run_draft(const DraftArgs& a) {
       (a.Wj && !aligned(a.Wj, 16)))
     return fail(DSPARK_ERR_INVALID, "W1, W2, U, h, Wj and target must be 16-byte aligned");
   const bool conf = a.h && a.w;
+  if (a.head == 1 && (a.wdt != DSPARK_BF16 || a.udt != DSPARK_BF16))
+    return fail(DSPARK_ERR_UNSUPPORTED, "the RNN head runs on bf16 weights and activations");
   if (a.head == 0 && ((a.h != nullptr) != (a.w != nullptr)))
     return fail(DSPARK_ERR_INVALID, "h and w go together for the Markov head");
-  if (a.head == 1 && (!a.Wj || !a.h)) return fail(DSPARK_ERR_INVALID, "the RNN head needs Wj and h");
+  if (a.head == 1 && (!a.Wj || !a.h || a.d == 0))
+    return fail(DSPARK_ERR_INVALID, "the RNN head needs Wj, h and d > 0");
+  if (a.head == 1 && a.h && !a.w && (a.c || a.S))
+    return fail(DSPARK_ERR_INVALID, "c and S need the confidence weight w");
   if (conf && a.d == 0) return fail(DSPARK_ERR_INVALID, "confidence needs d > 0");
   if ((a.c != nullptr) != conf || (a.S != nullptr) != conf)
     return fail(DSPARK_ERR_INVALID, "c and S are given exactly when h and w are");
@@ -194,6 +202,7 @@ dspark_status run_draft(const DraftArgs& a) {
   p.rnn_s = (float*)(ws + L.rnn_s);
   p.rnn_a = (float*)(ws + L.rnn_a);
   p.rnn_gh = (float*)(ws + L.rnn_gh);
+  p.rnn_flag = (unsigned*)(ws + L.rnn_flag);
   p.ybuf = (float*)(ws + L.ybuf);
 
   const int units = (a.V + 7) / 8;
@@ -201,6 +210,16 @@ dspark_status run_draft(const DraftArgs& a) {
   const int ues = u_bf16 ? 2 : 4;
   p.u_bulk = ((size_t)a.V * ues) % 16 == 0 && (!a.target || ((size_t)a.V * 4) % 16 == 0);
   cudaStream_t stream = (cudaStream_t)a.stream;
+
+  if (a.head == 1) {
+    // the h_k columns of Eq 6's joint projection, for every (request, position), up front
+    int ks = 0;
+    cudaError_t e = launch_gemm_tc(a.h, a.d, (const __nv_bfloat16*)a.Wj + 2 * a.r, 2 * a.r + a.d,
+                                   a.B * a.G, 3 * a.r, a.d, p.rnn_gh, kRnnMaxSplit, nCTA, &ks,
+                                   &p.hdr->status, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "rnn pre-pass launch");
+    p.rnn_ks = ks;
+  }
 
   if (path == 0) {
     if (!draft_cc_configure(p, (size_t)di.smem_optin))
@@ -319,7 +338,7 @@ int dspark_draft_path(int head, int B, int V, int r, dspark_dtype wdt) {
 int dspark_draft_launches(int head, int B, int V, int r, dspark_dtype wdt) {
   const int p = dspark_draft_path(head, B, V, r, wdt);
   if (p < 0) return -1;
-  return 1;  // one persistent launch on either path
+  return head == 1 ? 2 : 1;  // one persistent launch (+ the RNN head's pre-pass GEMM)
 }
 
 }  // extern "C"

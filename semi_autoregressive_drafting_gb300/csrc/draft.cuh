@@ -43,9 +43,11 @@ struct DraftParams {
   float2* ml;                // [gamma][B][nCTA] (max, sum exp) of y per block
   float2* mlt;               // [gamma][B][nCTA] same for the target
   float* l1p;                // [gamma][B][nCTA] partial L1 distances
-  float* rnn_s;              // [2][B][r] RNN state ping-pong
-  float* rnn_a;              // [B][r] RNN conditioning vector tanh(o) for the current step
-  float* rnn_gh;             // [B][gamma][3r] RNN h-part of the joint projection
+  float* rnn_s;              // [B][r] RNN state s_k, private to the request's owner block
+  float* rnn_a;              // [gamma][B][r] RNN conditioning vectors tanh(o_k)
+  float* rnn_gh;             // [ks][B*gamma][3r] split-K partials of h Wj[:, 2r:]^T
+  unsigned* rnn_flag;        // [gamma][B] step tags: rnn_a[k][b] is published
+  int rnn_ks;                // number of split-K partial planes in rnn_gh
   float* ybuf;               // [B][V] y of the current step (tensor-core path with a target)
   // launch geometry (set by the host)
   int stage_bytes;     // bytes per ring stage (a multiple of 32 W2 rows)
@@ -64,5 +66,9 @@ int draft_cc_supported(int B, int r, int w_bf16);
 cudaError_t launch_draft_tc(DraftParams& p, int nblocks, cudaStream_t stream);
 bool draft_tc_configure(DraftParams& p, size_t smem_optin);
 int draft_tc_supported(int B, int r, int w_bf16);
+cudaError_t launch_gemm_tc(const void* A, int lda, const void* Bm, int ldb, int M, int N, int K,
+                           float* part, int max_split, int nsm, int* ksplit_out, unsigned* status,
+                           cudaStream_t stream);
+constexpr int kRnnMaxSplit = 8;
 
 }  // namespace dspark

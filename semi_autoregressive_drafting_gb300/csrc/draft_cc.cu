@@ -25,7 +25,10 @@
 //     warm when every block gathers it after the barrier;
 //   * the Eq 8 label needs both normalisers, so its L1 sum runs right after the barrier from y
 //     and target values kept in shared memory.
+#include <type_traits>
+
 #include "draft.cuh"
+#include "rnn.cuh"
 
 namespace dspark {
 namespace {
@@ -53,7 +56,7 @@ struct Misc {
 };
 
 struct CCLayout {
-  size_t ring, ubuf, tbuf, ybuf, gbuf, ebuf, wsm, slots, misc, bars, total;
+  size_t ring, ubuf, tbuf, ybuf, gbuf, ebuf, wsm, rbuf, sbuf, u3, slots, misc, bars, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -77,6 +80,13 @@ __host__ __device__ inline CCLayout cc_layout(const DraftParams& p, int NB) {
   off = align_up(off + (size_t)NB * p.r * 4, 128);
   L.wsm = off;
   off = align_up(off + (size_t)p.r * 4, 128);
+  const bool rnn = p.head == 1;
+  L.rbuf = off;  // RNN: a_k of every request
+  off = align_up(off + (rnn ? (size_t)NB * p.r * 4 : 0), 128);
+  L.sbuf = off;  // RNN: the owned request's state s_k
+  off = align_up(off + (rnn ? (size_t)p.r * 4 : 0), 128);
+  L.u3 = off;    // RNN: the owned request's projection Wj z_k
+  off = align_up(off + (rnn ? (size_t)3 * p.r * 4 : 0), 128);
   L.slots = off;
   off = align_up(off + kMaxCW * 4 * sizeof(Slot), 128);
   L.misc = off;
@@ -390,7 +400,26 @@ struct Dot<float> {
   }
 };
 
-template <typename WT, int NB, int NCV, int CW>
+// RNN head: the conditioning vector a_k is fp32, so W2 is widened and multiplied in fp32.
+template <typename WT>
+struct DotF {
+  using E = float;
+  static constexpr int NE = Vec<WT>::N;
+  __device__ __forceinline__ static E load_e(const float* ebuf, int idx) { return ebuf[idx]; }
+  __device__ __forceinline__ static float run(const uint4& q, const E (&e)[NE], float acc) {
+    float w[NE];
+    Vec<WT>::unpack(q, w);
+    float a0 = acc, a1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < NE; i += 2) {
+      a0 = fmaf(w[i], e[i], a0);
+      a1 = fmaf(w[i + 1], e[i + 1], a1);
+    }
+    return a0 + a1;
+  }
+};
+
+template <typename WT, int NB, int NCV, int CW, bool RNN>
 __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftParams p) {
   constexpr int kCWarps = CW;
   constexpr int kCThreads = CW * 32;
@@ -403,6 +432,9 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
   float* gbuf = (float*)(smem + Lay.gbuf);
   float* ebuf = (float*)(smem + Lay.ebuf);
   float* wsm = (float*)(smem + Lay.wsm);
+  float* rbuf = (float*)(smem + Lay.rbuf);
+  float* sbuf = (float*)(smem + Lay.sbuf);
+  float* u3 = (float*)(smem + Lay.u3);
   Slot* slots = (Slot*)(smem + Lay.slots);
   Misc* ms = (Misc*)(smem + Lay.misc);
   uint64_t* full = (uint64_t*)(smem + Lay.bars);
@@ -513,6 +545,8 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
   // =========================================================== consumer warps
   if (conf && cta < B)
     for (int j = tid; j < r; j += kCThreads) wsm[j] = to_f<WT>(((const WT*)p.w)[p.d + j]);
+  if (RNN && cta < B)
+    for (int j = tid; j < r; j += kCThreads) sbuf[j] = p.s0 ? p.s0[(size_t)cta * r + j] : 0.f;
   if (conf && G == 1) hidden_dots<WT, kCThreads>(p, ms, tid, cta, nCTA);
   fill_noise<NB>(gbuf, SLM, SL, v0, B, 0, p.seed_lo, p.seed_hi, tid, kCThreads);
 
@@ -534,8 +568,28 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
       ebuf[i] = val;
     }
     csync<kCThreads>();
-    // (b) this lane's K-chunks of every e_b in registers
-    using DT = Dot<WT>;
+    if (RNN) {
+      // (a') Eq 6 for the owned request, published for every block; then collect a_k of all
+      if (cta < B) {
+        rnn_row_update<kCThreads>(p, cta, ks, sbuf, ebuf + cta * r, u3,
+                                  p.rnn_a + ((size_t)ks * B + cta) * r, tid);
+        if (tid == 0) st_release_u32(&p.rnn_flag[(size_t)ks * B + cta], (unsigned)(ks + 1));
+      }
+      bool okf = true;
+      if (warp < B && lane == 0) okf = wait_flag(&p.rnn_flag[(size_t)ks * B + warp], (unsigned)(ks + 1));
+      if (csync_or<kCThreads>(!okf)) {
+        failed = true;
+        break;
+      }
+      for (int i = tid; i < NB * r; i += kCThreads) {
+        const int b = i / r;
+        rbuf[i] = b < B ? ld_acquire_f32(&p.rnn_a[((size_t)ks * B + b) * r + (i - b * r)]) : 0.f;
+      }
+      csync<kCThreads>();
+    }
+    // (b) this lane's K-chunks of every e_b (RNN: a_k) in registers
+    using DT = typename std::conditional<RNN, DotF<WT>, Dot<WT>>::type;
+    const float* cvec = RNN ? rbuf : ebuf;
     typename DT::E ereg[NB][NCV][DT::NE];
 #pragma unroll
     for (int b = 0; b < NB; ++b)
@@ -544,7 +598,7 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
         const int cv = lane + 32 * t;
 #pragma unroll
         for (int i = 0; i < DT::NE; ++i)
-          ereg[b][t][i] = cv < VR ? DT::load_e(ebuf + b * r + cv * VEC, i) : typename DT::E(0);
+          ereg[b][t][i] = cv < VR ? DT::load_e(cvec + b * r + cv * VEC, i) : typename DT::E(0);
       }
     // (c) U_k (and target) rows of the slice
     if (ubulk) {
@@ -740,6 +794,9 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
     return;
   }
 
+  if (RNN && cta < B && p.s_out)
+    for (int j = tid; j < r; j += kCThreads) p.s_out[(size_t)cta * r + j] = sbuf[j];
+
   // the owned request: Eq 7 and S_k for every step, log-normalisers, and Eq 8 of every step
   // but the last (whose partial sums are complete only once every block is done)
   if (cta < B) {
@@ -792,6 +849,8 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
       }
     }
     for (int i = tid; i < G * B * nCTA; i += kCThreads) p.keys[i] = 0ull;
+    if (RNN)
+      for (int i = tid; i < G * B; i += kCThreads) p.rnn_flag[i] = 0u;
     csync<kCThreads>();
     if (tid == 0) {
       hdr->exit_count = 0;
@@ -804,7 +863,7 @@ template <typename WT, int NB, int NCV>
 cudaError_t launch_t(DraftParams& p, int nblocks, cudaStream_t stream) {
   constexpr int CW = NB <= 2 ? 16 : 8;
   constexpr int kThreads = CW * 32 + 32;
-  auto kern = draft_cc_kernel<WT, NB, NCV, CW>;
+  auto kern = p.head == 1 ? draft_cc_kernel<WT, NB, NCV, CW, true> : draft_cc_kernel<WT, NB, NCV, CW, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)p.smem_bytes);
   if (e != cudaSuccess) return e;

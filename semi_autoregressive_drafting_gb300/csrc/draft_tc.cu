@@ -21,6 +21,7 @@
 #include <cuda.h>
 
 #include "draft.cuh"
+#include "rnn.cuh"
 #include "tc.cuh"
 
 namespace dspark {
@@ -50,24 +51,28 @@ struct TMisc {
 };
 
 struct TCLayout {
-  size_t a, ring, scratch, misc, bars, total;
-  int nslab, na, nstage;
+  size_t a, ring, scratch, rnnbuf, misc, bars, total;
+  int nslab, na, nstage, aslabs;
 };
 
 __host__ __device__ inline size_t align_up_t(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline TCLayout tc_layout(int r, int na, int nstage) {
+// RNN head: each A buffer holds the bf16 high halves of a_k, then the low halves.
+__host__ __device__ inline TCLayout tc_layout(int r, int na, int nstage, bool rnn) {
   TCLayout L;
   L.nslab = (r + 63) / 64;
+  L.aslabs = L.nslab * (rnn ? 2 : 1);
   L.na = na;
   L.nstage = nstage;
   size_t off = 0;
   L.a = off;
-  off += (size_t)na * L.nslab * kSlab;
+  off += (size_t)na * L.aslabs * kSlab;
   L.ring = off;
   off += (size_t)nstage * kSlab;
   L.scratch = off;
   off = align_up_t(off + 3 * kM * sizeof(TSlot), 128);
+  L.rnnbuf = off;  // RNN: e (r), s (r), Wj z (3r) of the request being updated
+  off = align_up_t(off + (rnn ? (size_t)5 * r * 4 : 0), 128);
   L.misc = off;
   off = align_up_t(off + sizeof(TMisc), 128);
   L.bars = off;
@@ -101,6 +106,12 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
     if (*abort || globaltimer() - t0 > kWaitLimitNs) return false;
   }
   return true;
+}
+
+__device__ __forceinline__ float ld_acquire_f32(const float* p) {
+  float v;
+  asm volatile("ld.acquire.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ float ld_u(const void* p, size_t i, int bf16) {
@@ -151,12 +162,16 @@ __device__ __forceinline__ int cond_token(const DraftParams& p, int b, int ks, b
   return ok ? x : 0;
 }
 
+template <bool RNN>
 __global__ void __launch_bounds__(kThreads, 1)
     draft_tc_kernel(const DraftParams p, const __grid_constant__ CUtensorMap tmap_w2, int na,
                     int nstage) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const TCLayout Lay = tc_layout(p.r, na, nstage);
+  const TCLayout Lay = tc_layout(p.r, na, nstage, RNN);
+  float* r_e = (float*)(smem + Lay.rnnbuf);
+  float* r_s = r_e + p.r;
+  float* r_u = r_s + p.r;
   uint8_t* abuf = smem + Lay.a;
   uint8_t* ring = smem + Lay.ring;
   TSlot* scratch = (TSlot*)(smem + Lay.scratch);
@@ -253,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc::fence_after_sync();
-          const uint32_t a_base = smem_u32(abuf + (size_t)ab * nslab * kSlab);
+          const uint32_t a_base = smem_u32(abuf + (size_t)ab * Lay.aslabs * kSlab);
           for (int t = 0; t < ntile && !stop; ++t, ++acc_i) {
             const int acc = acc_i % kAcc;
             if (acc_i >= kAcc &&
@@ -274,6 +289,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int kk = 0; kk < 4; ++kk)
                 tc::mma_bf16(tmem + acc * kNT, tc::sdesc_sw128(a_base + s * kSlab + kk * 32),
                              tc::sdesc_sw128(b_base + kk * 32), idesc, (s | kk) != 0);
+              if (RNN) {  // a_k = hi + lo: the low halves against the same W2 slab
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  tc::mma_bf16(tmem + acc * kNT,
+                               tc::sdesc_sw128(a_base + (nslab + s) * kSlab + kk * 32),
+                               tc::sdesc_sw128(b_base + kk * 32), idesc, 1u);
+              }
               tc::mma_commit(&empty[slot]);
             }
             if (!stop) tc::mma_commit(&acc_full[acc]);
@@ -309,6 +331,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool failed = false;
 
   for (int ks = 0; ks < G && !failed; ++ks) {
+    if (RNN) {
+      // Eq 6 for the requests this block owns (b = cta mod grid), published for every block
+      for (int b = cta; b < B; b += nCTA) {
+        bool valid = false;
+        const int x = cond_token(p, b, ks, &valid);
+        for (int j = et; j < r; j += kEpiThreads) {
+          r_e[j] = __bfloat162float(((const __nv_bfloat16*)p.W1)[(size_t)x * r + j]);
+          r_s[j] = ks == 0 ? (p.s0 ? p.s0[(size_t)b * r + j] : 0.f) : p.rnn_s[(size_t)b * r + j];
+        }
+        esync<kEpiThreads>();
+        rnn_row_update<kEpiThreads>(p, b, ks, r_s, r_e, r_u, p.rnn_a + ((size_t)ks * B + b) * r, et);
+        for (int j = et; j < r; j += kEpiThreads) p.rnn_s[(size_t)b * r + j] = r_s[j];
+        esync<kEpiThreads>();
+        if (et == 0) st_release_u32(&p.rnn_flag[(size_t)ks * B + b], (unsigned)(ks + 1));
+      }
+    }
     for (int c = 0; c < nchunk && !failed; ++c) {
       const int u = ks * nchunk + c, ab = u % na;
       // ---- A operand: the chunk's conditioning rows W1[x_{k-1}], swizzled K-major bf16
@@ -319,16 +357,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
+      bool gok = true;
       {
         const int b = c * kM + gm;
         bool valid = false;
         const int x = b < B ? cond_token(p, b, ks, &valid) : 0;
-        const uint4* src = (const uint4*)((const __nv_bfloat16*)p.W1 + (size_t)x * r);
-        uint8_t* dst = abuf + (size_t)ab * nslab * kSlab + (gm >> 3) * 1024 + (gm & 7) * 128;
-        for (int j = gh; j < nslab * 8; j += 4) {
-          const uint4 val = (valid && j < nchk) ? src[j] : make_uint4(0, 0, 0, 0);
-          *(uint4*)(dst + (j >> 3) * kSlab + (((j & 7) ^ (gm & 7)) << 4)) = val;
+        uint8_t* dst = abuf + (size_t)ab * Lay.aslabs * kSlab + (gm >> 3) * 1024 + (gm & 7) * 128;
+        if (!RNN) {
+          const uint4* src = (const uint4*)((const __nv_bfloat16*)p.W1 + (size_t)x * r);
+          for (int j = gh; j < nslab * 8; j += 4) {
+            const uint4 val = (valid && j < nchk) ? src[j] : make_uint4(0, 0, 0, 0);
+            *(uint4*)(dst + (j >> 3) * kSlab + (((j & 7) ^ (gm & 7)) << 4)) = val;
+          }
+        } else {
+          if (b < B) gok = wait_flag(&p.rnn_flag[(size_t)ks * B + b], (unsigned)(ks + 1));
+          const float* src = p.rnn_a + ((size_t)ks * B + b) * r;
+          for (int j = gh; j < nslab * 8; j += 4) {
+            uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
+            if (gok && valid && j < nchk) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float a0 = ld_acquire_f32(src + 8 * j + 2 * e);
+                const float a1 = ld_acquire_f32(src + 8 * j + 2 * e + 1);
+                const __nv_bfloat16 h0 = __float2bfloat16_rn(a0), h1 = __float2bfloat16_rn(a1);
+                const __nv_bfloat16 l0 = __float2bfloat16_rn(a0 - __bfloat162float(h0));
+                const __nv_bfloat16 l1 = __float2bfloat16_rn(a1 - __bfloat162float(h1));
+                hi[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                lo[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+              }
+            }
+            const int off = (j >> 3) * kSlab + (((j & 7) ^ (gm & 7)) << 4);
+            *(uint4*)(dst + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *(uint4*)(dst + nslab * kSlab + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
         }
+      }
+      if (esync_or<kEpiThreads>(!gok)) {
+        failed = true;
+        break;
       }
       fence_proxy_async_smem();
       esync<kEpiThreads>();
@@ -549,6 +615,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (RNN && p.s_out)
+    for (int b = cta; b < B; b += nCTA)
+      for (int j = et; j < r; j += kEpiThreads) p.s_out[(size_t)b * r + j] = p.rnn_s[(size_t)b * r + j];
+
   // last block out: Eq 8 of the final step; leave the workspace ready for the next call
   esync<kEpiThreads>();
   if (et == 0) {
@@ -572,6 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     for (int i = et; i < G * B; i += kEpiThreads) p.keys[i] = 0ull;
+    if (RNN)
+      for (int i = et; i < G * B; i += kEpiThreads) p.rnn_flag[i] = 0u;
     esync<kEpiThreads>();
     if (et == 0) {
       hdr->arrive = 0;
@@ -607,7 +679,7 @@ bool draft_tc_configure(DraftParams& p, size_t smem_optin) {
   // two A buffers when they fit next to at least 4 ring stages, else one
   for (int na = 2; na >= 1; --na) {
     for (int ns = 8; ns >= 3; --ns) {
-      const TCLayout L = tc_layout(p.r, na, ns);
+      const TCLayout L = tc_layout(p.r, na, ns, p.head == 1);
       if (L.total <= smem_optin) {
         p.tc_na = na;
         p.nstages = ns;
@@ -632,13 +704,13 @@ cudaError_t launch_draft_tc(DraftParams& p, int nblocks, cudaStream_t stream) {
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(draft_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const void* kern = p.head == 1 ? (const void*)draft_tc_kernel<true> : (const void*)draft_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)p.smem_bytes);
   if (e != cudaSuccess) return e;
   int na = p.tc_na, ns = p.nstages;
   void* args[] = {(void*)&p, (void*)&tmap, (void*)&na, (void*)&ns};
-  return cudaLaunchCooperativeKernel((const void*)draft_tc_kernel, dim3(nblocks), dim3(kThreads),
-                                     args, p.smem_bytes, stream);
+  return cudaLaunchCooperativeKernel(kern, dim3(nblocks), dim3(kThreads), args, p.smem_bytes, stream);
 }
 
 }  // namespace dspark

@@ -97,28 +97,37 @@ def compare_floats(out, o, rows=None, logits=True):
     return errs
 
 
-def run_case(wl, *, target_noise=None, want_logits=True, rows=None, check_free=True, ds=None):
+def run_case(wl, *, target_noise=None, want_logits=True, rows=None, check_free=True, ds=None,
+             s0_scale=None):
     """Free-running and teacher-forced GPU draft against the oracle on the same inputs."""
     if target_noise is not None:
         wl = wl.with_(target_noise=target_noise)
     t = inputs.generate(wl)
+    rnn = wl.head == "rnn"
+    if rnn and s0_scale is not None:
+        g = torch.Generator().manual_seed(wl.seed + 1000)
+        t["s0"] = torch.randn(wl.B, wl.r, generator=g) * s0_scale
     d = to_dev(t)
     o = oracle_draft(wl, t, rows=rows, want_z=want_logits)
     assert o.status == 0
     has_t = d.get("target") is not None
-    ws = ds.Workspace(0, wl.B, wl.gamma, wl.V, wl.r, wl.d, target=has_t)
-    kw = dict(T=wl.T, seed=wl.seed, h=d["h"], w=d["w"], target=d.get("target"), workspace=ws)
+    ws = ds.Workspace(1 if rnn else 0, wl.B, wl.gamma, wl.V, wl.r, wl.d, target=has_t)
+    kw = dict(T=wl.T, seed=wl.seed, w=d["w"], target=d.get("target"), workspace=ws)
+    if rnn:
+        call = lambda **k: ds.rnn_draft(d["W1"], d["W2"], d["Wj"], d["U"], d["h"], d["x0"],
+                                        s0=d.get("s0"), **kw, **k)
+    else:
+        call = lambda **k: ds.markov_draft(d["W1"], d["W2"], d["U"], d["x0"], h=d["h"], **kw, **k)
     sel = (lambda a: a) if rows is None else (lambda a: a[rows])
     ties = 0
     if check_free:
-        free = ds.markov_draft(d["W1"], d["W2"], d["U"], d["x0"], **kw)
+        free = call()
         torch.cuda.synchronize()
         assert ws.status() == 0
         ties += check_tokens_free(sel(free.tokens.cpu().numpy()), o)
     forced = np.zeros((wl.B, wl.gamma), np.int32)
     forced[rows if rows is not None else slice(None)] = o.tokens
-    tf = ds.markov_draft(d["W1"], d["W2"], d["U"], d["x0"], forced=torch.from_numpy(forced).cuda(),
-                         want_logits=want_logits, **kw)
+    tf = call(forced=torch.from_numpy(forced).cuda(), want_logits=want_logits)
     torch.cuda.synchronize()
     assert ws.status() == 0
     ties += check_tokens_forced(sel(tf.tokens.cpu().numpy()), o)

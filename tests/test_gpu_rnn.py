@@ -1,0 +1,46 @@
+"""GPU parity of the RNN-head draft (Eq 6) against the fp64 oracle.
+
+The sequential update runs in fp32 on the CUDA cores, the h_k columns of the joint projection
+come from the tensor-core pre-pass GEMM, and the bias product uses fp32 a_k = tanh(o_k) (small
+batches) or a bf16 high/low split of a_k on the tensor cores (larger batches).  Same rules as
+the Markov tests: tokens bit-exact up to counted near-ties, floats (and the final state) within
+2e-3.
+"""
+import pytest
+
+import semi_autoregressive_drafting_gb300 as ds
+from semi_autoregressive_drafting_gb300 import inputs
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+RNN = inputs.WORKLOADS["rnn_head"]
+
+
+@pytest.mark.parametrize("B", [1, 3])
+def test_rnn_small_batch(B):
+    wl = RNN.with_(B=B, V=12000, d=128, seed=100 + B)
+    assert ds.draft_path(1, B, wl.V, wl.r) == 0
+    parity.run_case(wl, ds=ds, s0_scale=0.5)
+
+
+def test_rnn_small_batch_rank64_target():
+    parity.run_case(RNN.with_(B=2, V=8008, r=64, d=64, seed=104), ds=ds, target_noise=1.0)
+
+
+@pytest.mark.parametrize("B", [8, 64])
+def test_rnn_tensor_core(B):
+    wl = RNN.with_(B=B, V=10000, d=256, seed=110 + B)
+    assert ds.draft_path(1, B, wl.V, wl.r) == 1
+    parity.run_case(wl, ds=ds, s0_scale=0.5)
+
+
+def test_rnn_tensor_core_two_chunks_target():
+    parity.run_case(RNN.with_(B=130, V=9000, d=128, seed=120), ds=ds, target_noise=1.0,
+                    want_logits=False)
+
+
+@pytest.mark.slow
+def test_rnn_head_full_sampled_rows():
+    ties, _ = parity.run_case(RNN, ds=ds, rows=[0, 50, 127], want_logits=False)
+    assert ties <= 1
