@@ -167,6 +167,34 @@ dspark_status dspark_prefix_schedule(int B, int gamma, const float* S, const dou
                                      int32_t* len, double* theta, void* stream);
 
 /*
+ * The Markov draft of dspark_markov_draft for callers that cannot allocate device memory.  The
+ * paper has no counterpart: this is a deployment variant of the same computation.  Callers such
+ * as plugins inside another framework's memory pool, serving engines that forbid allocation on
+ * their decode path, or code handed only pre-allocated input and output buffers cannot create a
+ * workspace; this call keeps the draft's scratch in a 1 MiB array built into the library, which
+ * every GPU that loads the library holds until the process exits.
+ *   - Arguments and outputs are those of dspark_markov_draft, minus the workspace.
+ *   - status: optional device int32 that receives this call's device status (DSPARK_OK, or the
+ *     DSPARK_ERR_INVALID / DSPARK_ERR_TIMEOUT cases described for dspark_markov_draft), written on
+ *     `stream` after the draft; NULL to skip.
+ *   - Limit: problems whose dspark_workspace_bytes(0, B, gamma, V, r, d, flags) exceeds 1 MiB are
+ *     rejected with DSPARK_ERR_WORKSPACE (in practice the small-batch path, B <= 4).
+ *   - The first call on each device looks up the array's device address (once per device, with
+ *     that device current); make that first call before any stream capture.
+ *   - Allocates nothing: each call clears the part of the array it uses (the array keeps the
+ *     previous call's contents) and enqueues the draft.  All calls on a device share the one
+ *     array, so calls that overlap on the GPU (different streams without ordering) race.
+ */
+dspark_status dspark_markov_draft_noalloc(int B, int gamma, int V, int r, int d, float T,
+                                          uint64_t seed, dspark_dtype wdt, const void* W1,
+                                          const void* W2, const void* w, dspark_dtype udt,
+                                          const void* U, const void* h, const int32_t* x0,
+                                          const int32_t* forced, const float* target,
+                                          int32_t* tokens, float* lse, float* c, float* S,
+                                          float* cstar, float* l1, float* logits, int32_t* status,
+                                          void* stream);
+
+/*
  * Synchronises `stream`, returns the device status word of `workspace` (the most severe error
  * any draft call recorded since the last read, DSPARK_OK if none) and resets the workspace so
  * the next call starts clean.  DSPARK_ERR_CUDA if the synchronisation itself fails.

@@ -26,6 +26,8 @@ SIGNATURES = {
                                 P, P, P, P, P, P, P, P, SZ, P]),
     "dspark_rnn_draft": (I, [I, I, I, I, I, F, U64, I, P, P, P, P, I, P, P, P, P, P, P,
                              P, P, P, P, P, P, P, P, P, SZ, P]),
+    "dspark_markov_draft_noalloc": (I, [I, I, I, I, I, F, U64, I, P, P, P, I, P, P, P, P, P,
+                                        P, P, P, P, P, P, P, P, P]),
     "dspark_confidence": (I, [I, I, I, I, I, I, P, P, I, P, P, P, P, P, P]),
     "dspark_tv_label": (I, [I, I, F, P, P, P, P, P]),
     "dspark_prefix_schedule": (I, [I, I, P, P, P, P, P]),

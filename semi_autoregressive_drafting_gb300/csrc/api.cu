@@ -238,6 +238,10 @@ dspark_status run_draft(const DraftArgs& a) {
 
 }  // namespace
 
+namespace dspark {
+void set_last_error(const char* msg) { g_err = msg; }
+}  // namespace dspark
+
 extern "C" {
 
 size_t dspark_workspace_bytes(int head, int B, int gamma, int V, int r, int d, int flags) {
