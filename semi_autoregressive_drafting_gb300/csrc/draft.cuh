@@ -52,6 +52,7 @@ struct DraftParams {
   // launch geometry (set by the host)
   int stage_bytes;     // bytes per ring stage (a multiple of 32 W2 rows)
   int nstages;         // ring depth
+  int nres;            // stages of each block's slice kept in TMEM after the first step
   int slice_max;       // largest vocab slice of any block (multiple of 8)
   int u_bulk;          // 1: U/target rows are 16-byte aligned and copied with TMA bulk copies
   int tc_na;           // tensor-core path: A-operand buffers

@@ -29,6 +29,7 @@
 
 #include "draft.cuh"
 #include "rnn.cuh"
+#include "tc.cuh"
 
 namespace dspark {
 namespace {
@@ -53,6 +54,7 @@ struct Misc {
   int last;
   volatile int abort;
   volatile int stage_tag[16];  // which global stage each ring slot currently holds
+  uint32_t tmem_base;          // TMEM columns caching the first stages of the slice
 };
 
 struct CCLayout {
@@ -175,6 +177,29 @@ __device__ __forceinline__ bool wait_stage(volatile int* tag, uint64_t* full, in
 
 __device__ __forceinline__ float ld_act(const void* p, size_t i, int bf16) {
   return bf16 ? __bfloat162float(((const __nv_bfloat16*)p)[i]) : ((const float*)p)[i];
+}
+
+// 32 lanes x 32 columns of 32-bit values from registers into TMEM (this warp's lane quarter).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Global index of stage s of step ks in the producer's issue order: every stage on the first
+// step, then only the stages that are not cached in TMEM.
+__device__ __forceinline__ int stage_index(int ks, int s, int nst, int nres) {
+  return ks == 0 ? s : nst + (ks - 1) * (nst - nres) + (s - nres);
 }
 
 // Tagged argmax key of one block for one (step, request):
@@ -463,7 +488,6 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
   const int R = p.stage_bytes / row_bytes;  // rows per stage, a multiple of 32
   const int NS = p.nstages;
   const int nst = (SL + R - 1) / R;
-  const int total = G * nst;
   const bool ubulk = p.u_bulk && SL > 0;
 
   if (tid == 0) {
@@ -488,7 +512,14 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
     ms->valid[b] = ok;
     if (b < B && !ok) atomicMax(&hdr->status, kErrInvalid);
   }
+  const int nres = min(p.nres, nst);  // stages of the slice cached in TMEM after the first step
+  if (nres > 0 && warp == 0) {
+    tc::tmem_alloc(&ms->tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
   __syncthreads();  // the last block-wide barrier: from here the producer warp runs on its own
+  tc::fence_after_sync();
 
   // =========================================================== producer warp
   if (warp == kCWarps) {
@@ -497,9 +528,9 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
       const uint64_t pol_w = policy_evict_last();  // W2 is re-read every step: keep it in L2
       int issued = 0, u_issued = 0;
       bool stop = false;
-      for (int g = 0; g < total && !stop; ++g) {
-        const int ks = g / nst, s = g - ks * nst;
-        if (s == 0 && ubulk) {  // U_k (and target) rows of step ks
+      int g = 0;
+      for (int ks = 0; ks < G && !stop; ++ks) {
+        if (ubulk) {  // U_k (and target) rows of step ks
           const int buf = ks & 1;
           if (ks >= 2 &&
               !mbar_wait_or_abort(&uempty[buf], (uint32_t)(((ks - 2) >> 1) & 1), &ms->abort)) {
@@ -518,19 +549,22 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
           }
           u_issued = ks + 1;
         }
-        const int slot = g % NS;
-        if (g >= NS &&
-            !mbar_wait_or_abort(&empty[slot], (uint32_t)(((g - NS) / NS) & 1), &ms->abort)) {
-          stop = true;
-          break;
+        for (int s = (ks == 0 ? 0 : nres); s < nst; ++s, ++g) {
+          const int slot = g % NS;
+          if (g >= NS &&
+              !mbar_wait_or_abort(&empty[slot], (uint32_t)(((g - NS) / NS) & 1), &ms->abort)) {
+            stop = true;
+            break;
+          }
+          const int rows = min(R, SL - s * R);
+          const uint32_t bytes = (uint32_t)(rows * row_bytes);
+          ms->stage_tag[slot] = g;
+          mbar_expect_tx(&full[slot], bytes);
+          bulk_g2s(ring + (size_t)slot * p.stage_bytes,
+                   (const uint8_t*)p.W2 + (size_t)(v0 + s * R) * row_bytes, bytes, &full[slot],
+                   pol_w);
+          issued = g + 1;
         }
-        const int rows = min(R, SL - s * R);
-        const uint32_t bytes = (uint32_t)(rows * row_bytes);
-        ms->stage_tag[slot] = g;
-        mbar_expect_tx(&full[slot], bytes);
-        bulk_g2s(ring + (size_t)slot * p.stage_bytes,
-                 (const uint8_t*)p.W2 + (size_t)(v0 + s * R) * row_bytes, bytes, &full[slot], pol_w);
-        issued = g + 1;
       }
       if (stop) atomicMax(&hdr->status, kErrTimeout);
       // every copy this warp started must land before the block may exit
@@ -627,18 +661,83 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
     const float* tb = tbuf + (size_t)(buf * NB + bq) * SLM;
     const float* gb = gbuf + (size_t)bq * SLM;
     bool wfail = false;
+    // +U_k, /T, online (max, sum-exp), Gumbel-max update for slice entry vl of request bq
+    auto epilogue = [&](int vl, float bias) {
+      const int v = v0 + vl;
+      const float uval = p.u_bf16 ? __uint_as_float((uint32_t)((const uint16_t*)ub)[vl] << 16)
+                                  : ((const float*)ub)[vl];
+      const float z = uval + bias;
+      if (p.logits) p.logits[((size_t)bq * G + ks) * V + v] = z;
+      const float y = z * p.invT;
+      lse_push(st.m, st.l, y);
+      const float sc = y + gb[vl];
+      if (sc > st.best) {  // v grows along this lane's sequence: ties keep the smaller v
+        st.best = sc;
+        st.tok = (uint32_t)v;
+      }
+      if (tgt) {
+        lse_push(st.mt, st.lt, tb[vl] * p.invT);
+        ybuf[(size_t)bq * SLM + vl] = y;
+      }
+    };
     // Four warps share each stage: warp q of a group takes rows [q R/4, (q+1) R/4) in
     // sub-groups of SR rows, so a slot is handed back a quarter of a stage's work after its
     // bytes land.  Stages go round-robin to the groups.
     for (int s = grp; s < nst; s += kGroups) {
-      const int g = ks * nst + s;
+      const int rows = min(R, SL - s * R);
+      const int rq0 = qw * (R / 4), rq1 = min(rows, rq0 + R / 4);
+      if (R == 32 && NCV == 1) {
+        // This warp's 8 rows of the stage, one 16-byte K-chunk per lane, staged in registers:
+        // from TMEM for a cached stage after the first step, else from the ring (and, on the
+        // first step, copied into TMEM for the later steps).
+        uint32_t wv[32];
+        const uint32_t taddr = ms->tmem_base + ((uint32_t)(32 * qw) << 16) + 32 * s;
+        if (ks > 0 && s < nres) {
+          tc::tmem_ld32(taddr, wv);
+          tc::tmem_ld_wait();
+        } else {
+          const int g = stage_index(ks, s, nst, nres);
+          const int slot = g % NS;
+          // warp-uniform verdict: the TMEM store below needs the whole warp
+          if (!__all_sync(0xffffffffu, wait_stage(ms->stage_tag, full, slot, g, NS))) {
+            wfail = true;
+            break;
+          }
+          const uint8_t* stg = ring + (size_t)slot * p.stage_bytes;
+          const int cv = min(lane, VR - 1);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *(uint4*)&wv[4 * j] = *(const uint4*)(stg + (size_t)(rq0 + j) * row_bytes + cv * 16);
+          if (ks == 0 && s < nres) {
+            tmem_st32(taddr, wv);
+            tmem_st_wait();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+#pragma unroll
+        for (int sg = 0; sg < 8 / SR; ++sg) {
+          float part[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) part[i] = 0.f;
+#pragma unroll
+          for (int j = 0; j < SR; ++j) {
+            const uint4 q = *(const uint4*)&wv[4 * (sg * SR + j)];
+#pragma unroll
+            for (int b = 0; b < NB; ++b) part[j * NB + b] = DT::run(q, ereg[b][0], part[j * NB + b]);
+          }
+          const float bias = transpose_reduce<8>(part, lane);
+          const int row = rq0 + sg * SR + jrow;
+          if (owner && bq < B && row < rq1) epilogue(s * R + row, bias);
+        }
+        continue;
+      }
+      const int g = stage_index(ks, s, nst, nres);
       const int slot = g % NS;
       if (!wait_stage(ms->stage_tag, full, slot, g, NS)) {
         wfail = true;
         break;
       }
-      const int rows = min(R, SL - s * R);
-      const int rq0 = qw * (R / 4), rq1 = min(rows, rq0 + R / 4);
       const uint8_t* stg = ring + (size_t)slot * p.stage_bytes;
       if (rq1 <= rq0) {
         __syncwarp();
@@ -667,25 +766,7 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
         }
         const float bias = transpose_reduce<8>(part, lane);
         const int row = r0 + jrow;
-        if (owner && bq < B && row < rq1) {
-          const int vl = s * R + row;
-          const int v = v0 + vl;
-          const float uval = p.u_bf16 ? __uint_as_float((uint32_t)((const uint16_t*)ub)[vl] << 16)
-                                      : ((const float*)ub)[vl];
-          const float z = uval + bias;
-          if (p.logits) p.logits[((size_t)bq * G + ks) * V + v] = z;
-          const float y = z * p.invT;
-          lse_push(st.m, st.l, y);
-          const float sc = y + gb[vl];
-          if (sc > st.best) {  // v grows along this lane's sequence: ties keep the smaller v
-            st.best = sc;
-            st.tok = (uint32_t)v;
-          }
-          if (tgt) {
-            lse_push(st.mt, st.lt, tb[vl] * p.invT);
-            ybuf[(size_t)bq * SLM + vl] = y;
-          }
-        }
+        if (owner && bq < B && row < rq1) epilogue(s * R + row, bias);
       }
     }
     if (csync_or<kCThreads>(wfail)) {
@@ -785,6 +866,16 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
     }
     // (g) U/target buffer `buf` is free again for step ks + 2
     if (ubulk && tid == 0) mbar_arrive(&uempty[buf]);
+  }
+
+  // TMEM is no longer read: hand it back (every consumer warp has waited for its own loads)
+  if (nres > 0) {
+    tc::fence_before_sync();
+    csync<kCThreads>();
+    if (warp == 0) {
+      tc::fence_after_sync();
+      tc::tmem_dealloc(ms->tmem_base, 512);
+    }
   }
 
   if (failed) {
@@ -901,6 +992,9 @@ bool draft_cc_configure(DraftParams& p, size_t smem_optin) {
   p.nstages = (int)(avail / ((size_t)p.stage_bytes + 16));
   if (p.nstages > 16) p.nstages = 16;
   if (p.nstages < 2) return false;
+  // 512-byte rows give every consumer warp 8 rows x one 16-byte chunk per lane of a stage, which
+  // is one 32-column TMEM block of its lane quarter: the 512 columns hold 16 stages
+  p.nres = row_bytes == 512 && p.stage_bytes == 32 * 512 ? 16 : 0;
   p.smem_bytes = cc_layout(p, nb_of(p.B)).total;
   return p.smem_bytes <= smem_optin;
 }
