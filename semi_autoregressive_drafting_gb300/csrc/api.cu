@@ -72,7 +72,7 @@ WsLayout ws_layout(int head, int B, int G, int V, int r, int nCTA, int flags) {
   L.keys = off;
   off = align256(off + (size_t)G * B * nCTA * 8);
   L.hdot = off;
-  off = align256(off + (size_t)G * B * 4);
+  off = align256(off + (size_t)2 * G * B * 4);
   L.ml = off;
   off = align256(off + (size_t)G * B * nCTA * 8);
   L.mlt = off;

@@ -39,7 +39,7 @@ struct DraftParams {
   // workspace
   WsHeader* hdr;
   unsigned long long* keys;  // [gamma][B][nCTA] per-block tagged argmax keys (zero between calls)
-  float* hdot;               // [B][gamma] Eq 7 hidden halves w[0:d] . h[b][k]
+  float* hdot;               // [2][B][gamma] Eq 7 halves: w[0:d] . h[b][k], w[d:] . W1[x_{k-1}]
   float2* ml;                // [gamma][B][nCTA] (max, sum exp) of y per block
   float2* mlt;               // [gamma][B][nCTA] same for the target
   float* l1p;                // [gamma][B][nCTA] partial L1 distances

@@ -35,7 +35,6 @@ namespace dspark {
 namespace {
 
 constexpr int kMaxCW = 16;  // most consumer warps of any variant
-constexpr int kMaxG = 16;
 
 struct Slot {  // running state of one (request, vocab subset)
   float best;
@@ -46,7 +45,6 @@ struct Slot {  // running state of one (request, vocab subset)
 struct Misc {
   int cond[4];        // conditioning token of the next step per request
   int valid[4];       // request still valid
-  float edot[kMaxG];  // w[d:d+r] . W1[x_{k-1}] of the owned request, per step
   float S_run;        // running prefix survival of the owned request
   float Ld[4], Lt[4];
   float red[kMaxCW];
@@ -55,6 +53,8 @@ struct Misc {
   volatile int abort;
   volatile int stage_tag[16];  // which global stage each ring slot currently holds
   uint32_t tmem_base;          // TMEM columns caching the first stages of the slice
+  float cbuf[64];              // last block: Eq 7 of every (request, step)
+  bool cvalid[64];             // last block: the step's token is valid
 };
 
 struct CCLayout {
@@ -220,27 +220,40 @@ __device__ __forceinline__ uint32_t tagged_token(unsigned long long key) {
 __device__ __forceinline__ void st_release64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ void st_relaxed64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 __device__ __forceinline__ float ld_acquire_f32(const float* p) {
   float v;
   asm volatile("ld.acquire.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
   return v;
 }
 
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // Grid barrier and argmax in one: wait (bounded) until every block has published its tagged
 // key for step ks, then return the largest.  One warp; each lane covers every 32nd block.
 __device__ __forceinline__ bool poll_keys(const unsigned long long* keys, int n, int ks, int lane,
-                                          unsigned long long* best) {
+                                          bool acquire, unsigned long long* best) {
   const unsigned long long tag = (unsigned long long)(ks + 1);
   unsigned long long t0 = 0;
   for (;;) {
     unsigned long long m = 0;
     bool mine = true;
     for (int i = lane; i < n; i += 32) {
-      const unsigned long long k = ld_acquire64(keys + i);
+      const unsigned long long k = ld_relaxed64(keys + i);
       mine = mine && ((k >> 24) & 0xFF) == tag;
       m = k > m ? k : m;
     }
     if (__all_sync(0xffffffffu, mine)) {
+      // with release stores behind the keys, one fence turns the relaxed loads into an
+      // acquire of everything those blocks wrote before publishing
+      if (acquire) fence_acq_rel_gpu();
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const unsigned long long q = __shfl_xor_sync(0xffffffffu, m, o);
@@ -368,22 +381,6 @@ __device__ __forceinline__ void slot_init(Slot& s) {
   s.mt = -INFINITY;
   s.lt = 0.f;
 }
-__device__ __forceinline__ void slot_merge(Slot& a, const Slot& q) {
-  best_merge(a.best, a.tok, q.best, q.tok);
-  lse_merge(a.m, a.l, q.m, q.l);
-  lse_merge(a.mt, a.lt, q.mt, q.lt);
-}
-__device__ __forceinline__ Slot slot_shfl(const Slot& s, int o) {
-  Slot q;
-  q.best = __shfl_xor_sync(0xffffffffu, s.best, o);
-  q.tok = __shfl_xor_sync(0xffffffffu, s.tok, o);
-  q.m = __shfl_xor_sync(0xffffffffu, s.m, o);
-  q.l = __shfl_xor_sync(0xffffffffu, s.l, o);
-  q.mt = __shfl_xor_sync(0xffffffffu, s.mt, o);
-  q.lt = __shfl_xor_sync(0xffffffffu, s.lt, o);
-  return q;
-}
-
 // Row dot-product accumulation for one 16-byte W2 chunk against this lane's K-chunk of e.
 // bf16: the packed mixed-precision FMA reads both bf16 operands from register halves and
 // accumulates in fp32 (bf16 -> fp32 is exact, so this equals converting first).
@@ -774,52 +771,91 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
       break;
     }
 
-    // (e) merge lanes of the same request (fixed butterfly), then warps (fixed butterfly), and
-    // publish this block's candidate for step ks: (max, sum-exp) partials first, then the
-    // tagged argmax key with release semantics -- the key doubles as the barrier arrival
+    // (e) merge lanes of the same request, then warps (fixed butterflies), and publish this
+    // block's candidate for step ks as a tagged argmax key with release semantics: the key is
+    // the grid barrier's arrival too.  With a target the second pass right after the barrier
+    // needs the global normalisers, so the (max, sum-exp) partials go out before the key;
+    // without one only the argmax is on the critical path and the partials follow the key.
+    unsigned long long key = st.tok != 0xFFFFFFFFu ? tagged_key(st.best, st.tok, ks) : 0ull;
 #pragma unroll
     for (int o = 4 * NB; o < 32; o <<= 1) {
-      const Slot q = slot_shfl(st, o);
-      slot_merge(st, q);
+      const unsigned long long q = __shfl_xor_sync(0xffffffffu, key, o);
+      key = q > key ? q : key;
+      lse_merge(st.m, st.l, __shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.l, o));
+      if (tgt)
+        lse_merge(st.mt, st.lt, __shfl_xor_sync(0xffffffffu, st.mt, o),
+                  __shfl_xor_sync(0xffffffffu, st.lt, o));
     }
-    if (lane < 4 * NB && owner) slots[warp * 4 + (lane >> 2)] = st;
+    if (lane < 4 * NB && owner) {
+      Slot& o = slots[warp * 4 + (lane >> 2)];
+      o.best = __uint_as_float((uint32_t)(key >> 32));
+      o.tok = (uint32_t)key;
+      o.m = st.m;
+      o.l = st.l;
+      o.mt = st.mt;
+      o.lt = st.lt;
+    }
     csync<kCThreads>();
     if (warp < B) {
       const int b = warp;
-      Slot a;
-      if (lane < kCWarps) a = slots[lane * 4 + b];
-      else slot_init(a);
+      const size_t o = ((size_t)ks * B + b) * nCTA + cta;
+      const bool has = SL > 0 && ms->valid[b];
+      unsigned long long kb = 0;
+      if (lane < kCWarps) {
+        const Slot& q = slots[lane * 4 + b];
+        kb = ((unsigned long long)__float_as_uint(q.best) << 32) | q.tok;
+      }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const Slot q = slot_shfl(a, o);
-        slot_merge(a, q);
+      for (int w = 16; w > 0; w >>= 1) {
+        const unsigned long long q = __shfl_xor_sync(0xffffffffu, kb, w);
+        kb = q > kb ? q : kb;
+      }
+      const unsigned long long pub = has && kb ? kb : tagged_key_empty(ks);
+      if (!tgt && lane == 0) st_relaxed64(&p.keys[o], pub);
+      float m = -INFINITY, l = 0.f, mt = -INFINITY, lt = 0.f;
+      if (lane < kCWarps) {
+        const Slot& q = slots[lane * 4 + b];
+        m = q.m;
+        l = q.l;
+        mt = q.mt;
+        lt = q.lt;
+      }
+#pragma unroll
+      for (int w = 16; w > 0; w >>= 1) {
+        lse_merge(m, l, __shfl_xor_sync(0xffffffffu, m, w), __shfl_xor_sync(0xffffffffu, l, w));
+        if (tgt)
+          lse_merge(mt, lt, __shfl_xor_sync(0xffffffffu, mt, w), __shfl_xor_sync(0xffffffffu, lt, w));
       }
       if (lane == 0) {
-        const size_t o = ((size_t)ks * B + b) * nCTA + cta;
-        p.ml[o] = make_float2(a.m, a.l);
-        if (tgt) p.mlt[o] = make_float2(a.mt, a.lt);
-        const bool has = SL > 0 && ms->valid[b];
-        st_release64(&p.keys[o], has ? tagged_key(a.best, a.tok, ks) : tagged_key_empty(ks));
+        p.ml[o] = make_float2(m, l);
+        if (tgt) {
+          p.mlt[o] = make_float2(mt, lt);
+          st_release64(&p.keys[o], pub);
+        }
         // if this block's candidate wins, every block gathers its W1 row next: warm L2 now
-        if (has) prefetch_l2((const uint8_t*)p.W1 + (size_t)a.tok * row_bytes, (uint32_t)row_bytes);
+        if (has && kb)
+          prefetch_l2((const uint8_t*)p.W1 + (size_t)tagged_token(kb) * row_bytes, (uint32_t)row_bytes);
       }
     }
 
     // (f) while the other blocks finish: next step's noise, Eq 7's embedding half of this step
     // (owned request), the hidden halves (first step); then every block's key for step ks
-    if (ks + 1 < G) fill_noise<NB>(gbuf, SLM, SL, v0, B, ks + 1, p.seed_lo, p.seed_hi, tid, kCThreads);
+    // (the polling warps b < B skip the noise so that they start polling at once)
+    if (ks + 1 < G && warp >= B)
+      fill_noise<NB>(gbuf, SLM, SL, v0, B, ks + 1, p.seed_lo, p.seed_hi, tid - 32 * B,
+                     kCThreads - 32 * B);
     if (conf && cta < B && warp == kCWarps - 1) {
       float acc = 0.f;
       for (int j = lane; j < r; j += 32) acc += wsm[j] * ebuf[cta * r + j];
       acc = warp_sum(acc);
-      if (lane == 0) ms->edot[ks] = acc;
+      if (lane == 0) p.hdot[(size_t)(B + cta) * G + ks] = acc;  // embedding half
     }
     if (conf && ks == 0 && G > 1) hidden_dots<WT, kCThreads>(p, ms, tid, cta, nCTA);
     bool ok = true;
     if (warp < B) {
       const int b = warp;
       unsigned long long best = 0;
-      ok = poll_keys(p.keys + ((size_t)ks * B + b) * nCTA, nCTA, ks, lane, &best);
+      ok = poll_keys(p.keys + ((size_t)ks * B + b) * nCTA, nCTA, ks, lane, tgt, &best);
       if (lane == 0 && ok) {
         const bool was_valid = ms->valid[b];
         const int xk = was_valid ? (int)tagged_token(best) : -1;
@@ -888,27 +924,15 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
   if (RNN && cta < B && p.s_out)
     for (int j = tid; j < r; j += kCThreads) p.s_out[(size_t)cta * r + j] = sbuf[j];
 
-  // the owned request: Eq 7 and S_k for every step, log-normalisers, and Eq 8 of every step
-  // but the last (whose partial sums are complete only once every block is done)
-  if (cta < B) {
+  // with a target the owned request's normalisers and Eq 8 of every step but the last are
+  // complete here (their partials went out before each key); the rest waits for the last block
+  if (tgt && cta < B) {
     const int b = cta;
-    if (conf && tid == 0) {
-      float surv = 1.f;
-      bool vb = true;
-      for (int k = 0; k < G; ++k) {
-        const size_t o = (size_t)b * G + k;
-        vb = vb && p.tokens[o] >= 0;
-        const float cv = vb ? sigmoidf_acc(ld_acquire_f32(&p.hdot[o]) + ms->edot[k]) : NAN;
-        surv = vb ? surv * cv : NAN;
-        p.c[o] = cv;
-        p.S[o] = surv;
-      }
-    }
     for (int k = warp; k < G; k += kCWarps) {
-      const float2 ml = warp_merge_ml(p.ml + ((size_t)k * B + b) * nCTA, nCTA, lane);
       const bool vb = p.tokens[(size_t)b * G + k] >= 0;
+      const float2 ml = warp_merge_ml(p.ml + ((size_t)k * B + b) * nCTA, nCTA, lane);
       if (lane == 0) p.lse[(size_t)b * G + k] = vb ? ml.x + logf(ml.y) : NAN;
-      if (tgt && k + 1 < G) {
+      if (k + 1 < G) {
         const float s = warp_sum_strided(p.l1p + ((size_t)k * B + b) * nCTA, nCTA, lane);
         if (lane == 0) {
           const size_t o = (size_t)b * G + k;
@@ -919,7 +943,10 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
     }
   }
 
-  // last block out: Eq 8 of the final step, then leave the workspace ready for the next call
+  // last block out: what needs every block's writes -- Eq 7 and S_k of every request (the
+  // hidden and embedding halves come from several blocks), the log-normalisers without a
+  // target, Eq 8 of the final step -- then leave the workspace ready for the next call
+  __threadfence();  // this thread's global writes are visible before the block counts itself out
   csync<kCThreads>();
   if (tid == 0) {
     __threadfence();
@@ -929,12 +956,40 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
   csync<kCThreads>();
   if (ms->last) {
     __threadfence();
+    const volatile int32_t* vtok = p.tokens;
+    if (conf) {
+      // one thread per (b, k) loads and squashes, then one per request runs the product
+      float* cbuf = ms->cbuf;
+      for (int i = tid; i < B * G; i += kCThreads) {
+        ms->cvalid[i] = vtok[i] >= 0;
+        cbuf[i] = sigmoidf_acc(p.hdot[i] + p.hdot[(size_t)B * G + i]);
+      }
+      csync<kCThreads>();
+      if (tid < B) {
+        float surv = 1.f;
+        bool vb = true;
+        for (int k = 0; k < G; ++k) {
+          const int o = tid * G + k;
+          vb = vb && ms->cvalid[o];
+          const float cv = vb ? cbuf[o] : NAN;
+          surv = vb ? surv * cv : NAN;
+          p.c[o] = cv;
+          p.S[o] = surv;
+        }
+      }
+    }
+    if (!tgt)
+      for (int i = warp; i < B * G; i += kCWarps) {
+        const int b = i / G, k = i - b * G;
+        const float2 ml = warp_merge_ml(p.ml + ((size_t)k * B + b) * nCTA, nCTA, lane);
+        if (lane == 0) p.lse[i] = vtok[i] >= 0 ? ml.x + logf(ml.y) : NAN;
+      }
     if (tgt && warp < B) {
       const int b = warp;
       const float s = warp_sum_strided(p.l1p + ((size_t)(G - 1) * B + b) * nCTA, nCTA, lane);
       if (lane == 0) {
         const size_t o = (size_t)b * G + G - 1;
-        const bool vb = ((volatile int32_t*)p.tokens)[o] >= 0;
+        const bool vb = vtok[o] >= 0;
         p.l1[o] = vb ? s : NAN;
         p.cstar[o] = vb ? fminf(1.f, fmaxf(0.f, 1.f - 0.5f * s)) : NAN;
       }
