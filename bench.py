@@ -304,8 +304,11 @@ def main():
         achieved = alg / (ms_step * 1e-3) / 1e9
         src = os.path.join(ROOT, "semi_autoregressive_drafting_gb300", "csrc", "draft_cc.cu")
         traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["source_sha"] == _sha(src) else None
-        launches = ds.draft_launches(0 if wl.head == "markov" else 1, B, wl.V, wl.r,
-                                     wl.dtype == "bf16")
+        head = 0 if wl.head == "markov" else 1
+        launches = ds.draft_launches(head, B, wl.V, wl.r, wl.dtype == "bf16")
+        path = ds.draft_path(head, B, wl.V, wl.r, wl.dtype == "bf16")
+        path_name = {0: "cuda-core", 1: "tcgen05, requests on M",
+                     2: "tcgen05, vocabulary on M"}.get(path, "none")
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -314,13 +317,12 @@ def main():
             "config": {"workload": wl.name, "B": B, "gamma": G, "V": wl.V, "r": wl.r, "d": wl.d,
                        "T": wl.T, "l2": "flushed between timed blocks (512 MB write)",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                       "path": "cuda-core" if ds.draft_path(0, B, wl.V, wl.r) == 0 else "tcgen05"},
+                       "path": path_name},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_kind": f"{peak_kind} copy bandwidth",
                          "algorithmic_bytes_per_launch": alg,
-                         "kernel": "draft_cc_kernel" if ds.draft_path(0, B, wl.V, wl.r) == 0
-                         else "draft_tc_kernel"},
+                         "kernel": "draft_tc_kernel" if path == 1 else "draft_cc_kernel"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": launches * args.steps,

@@ -205,8 +205,17 @@ dspark_status dspark_get_status(void* workspace, size_t workspace_bytes, void* s
 const char* dspark_last_error(void);
 
 /*
- * Which kernel path a draft call with these arguments takes: 0 = CUDA-core path (small B or
- * fp32 weights), 1 = tensor-core (tcgen05) path.  Negative for arguments it would reject.
+ * Which kernel path a draft call with these arguments takes on the current device:
+ *   0 = CUDA-core dot products (B <= 4; fp32 weights, or bf16 ranks the next one cannot take),
+ *   1 = tensor cores with the requests on the MMA's M dimension (bf16, any B),
+ *   2 = tensor cores with the vocabulary rows on M and the B <= 4 conditioning vectors on N
+ *       (bf16, r a multiple of 64 up to 256, at most 4096 vocabulary rows per SM).
+ * By default 2 when it can run the arguments and B >= 3, else the first of 0, 2, 1 that can
+ * (on GB300 the B <= 4 tensor-core MMA, N = 16, costs about as much as a full-width one, so it
+ * overtakes the CUDA cores only from B = 3).  The environment variable
+ * DSPARK_DRAFT_PATH = cuda-core | tensor | tensor-vocab, read at every call, forces one (a draft
+ * call then fails with DSPARK_ERR_UNSUPPORTED if that one cannot run the arguments; other
+ * values are ignored).  Negative for arguments it would reject.
  */
 int dspark_draft_path(int head, int B, int V, int r, dspark_dtype wdt);
 

@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -99,11 +100,27 @@ bool shape_ok(int head, int B, int G, int V, int r, int d) {
          r >= 8 && r <= 512 && r % 8 == 0 && d >= 0 && d % 8 == 0 && B <= (1 << 20);
 }
 
-int path_of(int head, int B, int r, int w_bf16) {
+int slice_max_of(int V, int nCTA) {
+  const int units = (V + 7) / 8;
+  return ((units + nCTA - 1) / nCTA) * 8;
+}
+
+// 0: CUDA-core dot products; 1: tensor cores with requests on M; 2: tensor cores with the
+// vocabulary on M.  DSPARK_DRAFT_PATH=cuda-core|tensor|tensor-vocab picks one (-1 if that one
+// cannot run these arguments); otherwise 2 for B = 3 or 4, else the first of 0, 2, 1 that can.
+int path_of(int head, int B, int V, int r, int w_bf16, int nCTA) {
   if (head == 1 && !w_bf16) return -1;  // the RNN pre-pass is a bf16 tensor-core GEMM
-  if (draft_cc_supported(B, r, w_bf16)) return 0;
-  if (draft_tc_supported(B, r, w_bf16)) return 1;
-  return -1;
+  const bool ok[3] = {draft_cc_supported(B, r, w_bf16) != 0, draft_tc_supported(B, r, w_bf16) != 0,
+                      draft_tcv_supported(B, r, w_bf16, slice_max_of(V, nCTA)) != 0};
+  if (const char* f = std::getenv("DSPARK_DRAFT_PATH")) {
+    const int want = !std::strcmp(f, "cuda-core") ? 0 : !std::strcmp(f, "tensor") ? 1
+                   : !std::strcmp(f, "tensor-vocab") ? 2 : -2;
+    if (want >= 0) return ok[want] ? want : -1;
+  }
+  // Measured on GB300 (r = 256, V = 151936): an M = 128, N = 16 MMA costs about as much as a
+  // full-width one, so the tensor cores pay off from B = 3 on; below that the CUDA cores win.
+  if (ok[2] && B >= 3) return 2;
+  return ok[0] ? 0 : ok[2] ? 2 : ok[1] ? 1 : -1;
 }
 
 struct DraftArgs {
@@ -156,7 +173,7 @@ dspark_status run_draft(const DraftArgs& a) {
   if (!a.ws || !aligned(a.ws, 256) || a.ws_bytes < L.total)
     return fail(DSPARK_ERR_WORKSPACE, "workspace must be 256-byte aligned and >= %zu bytes", L.total);
   const int w_bf16 = a.wdt == DSPARK_BF16, u_bf16 = a.udt == DSPARK_BF16;
-  const int path = path_of(a.head, a.B, a.r, w_bf16);
+  const int path = path_of(a.head, a.B, a.V, a.r, w_bf16, nCTA);
   if (path < 0)
     return fail(DSPARK_ERR_UNSUPPORTED, "no kernel for head=%d B=%d r=%d dtype=%d in this build",
                 a.head, a.B, a.r, (int)a.wdt);
@@ -221,7 +238,11 @@ dspark_status run_draft(const DraftArgs& a) {
     p.rnn_ks = ks;
   }
 
-  if (path == 0) {
+  if (path == 0 || path == 2) {
+    p.tcv = path == 2;
+    if (p.tcv && !draft_cc_configure(p, (size_t)di.smem_optin) && !std::getenv("DSPARK_DRAFT_PATH") &&
+        draft_cc_supported(a.B, a.r, w_bf16))
+      p.tcv = 0;  // the per-step buffers leave too little room for the slab ring: CUDA cores
     if (!draft_cc_configure(p, (size_t)di.smem_optin))
       return fail(DSPARK_ERR_UNSUPPORTED, "vocab slice too large for shared memory");
     cudaError_t e = launch_draft_cc(p, nCTA, stream);
@@ -336,7 +357,9 @@ const char* dspark_last_error(void) { return g_err.c_str(); }
 
 int dspark_draft_path(int head, int B, int V, int r, dspark_dtype wdt) {
   if (!shape_ok(head, B, 1, V, r, 0)) return -1;
-  return path_of(head, B, r, wdt == DSPARK_BF16);
+  DevInfo di;
+  const int nCTA = dev_info(&di) ? di.sms : 152;  // without a device: a GB300's count
+  return path_of(head, B, V, r, wdt == DSPARK_BF16, nCTA);
 }
 
 int dspark_draft_launches(int head, int B, int V, int r, dspark_dtype wdt) {

@@ -253,6 +253,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait with a suspend-time hint: the thread may sleep up to hint_ns inside the instruction
+// until the phase completes, instead of spinning on the issue slots other warps need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait of one lane, sleeping between polls, with the verdict given to the whole warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0 && !mbar_try_wait(bar, parity)) {
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait_sleep(bar, parity, 1000)) {
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok, 0);
+}
 // Bounded wait for the phase with the given parity; false when the time bound ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;

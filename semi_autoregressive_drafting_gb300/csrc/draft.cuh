@@ -1,6 +1,7 @@
 // draft.cuh -- parameters and host-side launch interface of the persistent draft kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -52,7 +53,10 @@ struct DraftParams {
   // launch geometry (set by the host)
   int stage_bytes;     // bytes per ring stage (a multiple of 32 W2 rows)
   int nstages;         // ring depth
-  int nres;            // stages of each block's slice kept in TMEM after the first step
+  int nres;            // W2 stages (CUDA cores) or 128x64 slabs (tensor cores) of each block's
+                       // slice kept in TMEM after the first step
+  int tcv;             // draft_cc: 1 = bias product on the tensor cores, vocabulary rows on M
+  int nres_s;          // tensor-core variant: slabs of the slice resident in shared memory
   int slice_max;       // largest vocab slice of any block (multiple of 8)
   int u_bulk;          // 1: U/target rows are 16-byte aligned and copied with TMA bulk copies
   int tc_na;           // tensor-core path: A-operand buffers
@@ -64,9 +68,13 @@ cudaError_t launch_draft_cc(DraftParams& p, int nblocks, cudaStream_t stream);
 size_t draft_cc_smem_bytes(const DraftParams& p);
 bool draft_cc_configure(DraftParams& p, size_t smem_optin);
 int draft_cc_supported(int B, int r, int w_bf16);
+int draft_tcv_supported(int B, int r, int w_bf16, int slice_max);
 cudaError_t launch_draft_tc(DraftParams& p, int nblocks, cudaStream_t stream);
 bool draft_tc_configure(DraftParams& p, size_t smem_optin);
 int draft_tc_supported(int B, int r, int w_bf16);
+// 2-D tensor map of a row-major bf16 matrix [rows][cols] (row stride ld elements) for TMA tile
+// loads of box_rows rows x 64 columns into the 128-byte-swizzled K-major layout.
+bool encode_bf16_2d(CUtensorMap* m, const void* base, int rows, int cols, int ld, int box_rows);
 cudaError_t launch_gemm_tc(const void* A, int lda, const void* Bm, int ldb, int M, int N, int K,
                            float* part, int max_split, int nsm, int* ksplit_out, unsigned* status,
                            cudaStream_t stream);

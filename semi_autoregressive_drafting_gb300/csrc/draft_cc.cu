@@ -27,6 +27,8 @@
 //     and target values kept in shared memory.
 #include <type_traits>
 
+#include <cstring>
+
 #include "draft.cuh"
 #include "rnn.cuh"
 #include "tc.cuh"
@@ -58,7 +60,7 @@ struct Misc {
 };
 
 struct CCLayout {
-  size_t ring, ubuf, tbuf, ybuf, gbuf, ebuf, wsm, rbuf, sbuf, u3, slots, misc, bars, total;
+  size_t ring, res, ebf, ubuf, tbuf, ybuf, gbuf, ebuf, wsm, rbuf, sbuf, u3, slots, misc, bars, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -70,6 +72,12 @@ __host__ __device__ inline CCLayout cc_layout(const DraftParams& p, int NB) {
   size_t off = 0;
   L.ring = off;
   off += (size_t)p.nstages * p.stage_bytes;
+  // tensor-core variant: resident slabs, then the MMA's B operand (16 rows x r bf16 in the
+  // 128-byte swizzle, one 2 KB block per 64 K); all 1024-byte aligned
+  L.res = off;
+  off += p.tcv ? (size_t)p.nres_s * p.stage_bytes : 0;
+  L.ebf = off;
+  off += p.tcv ? (size_t)(p.r / 64) * 2048 : 0;
   L.ubuf = off;
   off = align_up(off + 2 * NB * (size_t)p.slice_max * ues, 128);
   L.tbuf = off;
@@ -94,8 +102,10 @@ __host__ __device__ inline CCLayout cc_layout(const DraftParams& p, int NB) {
   L.misc = off;
   off = align_up(off + sizeof(Misc), 128);
   L.bars = off;
-  off += (size_t)(2 * p.nstages + 4) * 8;
-  L.total = align_up(off, 128);
+  // ring full/empty, U full/empty; tensor-core variant: efull, mdone, accfull[32], tready[16],
+  // rfull[16]
+  off += (size_t)(2 * p.nstages + 4 + (p.tcv ? 2 + 32 + 16 + 16 : 0)) * 8;
+  L.total = align_up(off, 128) + (p.tcv ? 1024 : 0);  // slack to align the base to 1024
   return L;
 }
 
@@ -114,6 +124,20 @@ __device__ __forceinline__ int csync_or(int pred) {
       "selp.s32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"(pred), "n"(NT)
+      : "memory");
+  return r;
+}
+// barrier of the four warps of consumer group g (named barrier 2 + g, 128 threads), returning
+// whether any of them passed a true predicate
+__device__ __forceinline__ int gsync_or(int g, int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, 128, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "r"(2 + g)
       : "memory");
   return r;
 }
@@ -179,21 +203,17 @@ __device__ __forceinline__ float ld_act(const void* p, size_t i, int bf16) {
   return bf16 ? __bfloat162float(((const __nv_bfloat16*)p)[i]) : ((const float*)p)[i];
 }
 
-// 32 lanes x 32 columns of 32-bit values from registers into TMEM (this warp's lane quarter).
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
+// TCV tile processing order of a step: tiles tr0 .. nt-1, then 0 .. tr0-1.
+__device__ __forceinline__ int tile_at(int n, int tr0, int nt) {
+  const int t = n + tr0;
+  return t < nt ? t : t - nt;
 }
-__device__ __forceinline__ void tmem_st_wait() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+
+// TCV slab order: tile by tile, K block by K block; position i is (tile i / nsk, K block i % nsk).
+// The first positions are the TMEM-cached slabs, then the resident ones, then the streamed ones.
+__device__ __forceinline__ void slab_at(int i, int nsk, int& t, int& sk) {
+  t = i / nsk;
+  sk = i - t * nsk;
 }
 
 // Global index of stage s of step ks in the producer's issue order: every stage on the first
@@ -441,11 +461,21 @@ struct DotF {
   }
 };
 
-template <typename WT, int NB, int NCV, int CW, bool RNN>
-__global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftParams p) {
+// TCV: the bias product on the tensor cores.  W2 is tiled as 128 vocabulary rows x 64 K (one
+// "slab", 16 KB, 128-byte swizzle, loaded by 2-D TMA); an MMA warp issues kind::f16 MMAs with
+// M = 128 vocabulary rows, N = 16 columns holding the B conditioning vectors in bf16 (RNN: a_k
+// split into bf16 hi and lo parts, rows b and 8 + b), K = r, into one TMEM accumulator per
+// tile, so each consumer thread reads the bias of one vocabulary row for every request.  The
+// first slabs of the slice move into TMEM after the first step and feed the MMA as its A
+// operand from there; the next ones stay resident in shared memory; the rest stream through
+// the ring every step.
+template <typename WT, int NB, int NCV, int CW, bool RNN, bool TCV>
+__global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
+    draft_cc_kernel(const DraftParams p, const __grid_constant__ CUtensorMap tmW2) {
   constexpr int kCWarps = CW;
   constexpr int kCThreads = CW * 32;
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = TCV ? (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023) : smem_raw;
   const CCLayout Lay = cc_layout(p, NB);
   uint8_t* ring = smem + Lay.ring;
   uint8_t* ubuf = smem + Lay.ubuf;
@@ -463,6 +493,13 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
   uint64_t* empty = full + p.nstages;
   uint64_t* ufull = empty + p.nstages;
   uint64_t* uempty = ufull + 2;
+  uint64_t* efull = uempty + 2;   // TCV: the B operand of step ks is in shared memory
+  uint64_t* mdone = efull + 1;    // TCV: every MMA the MMA warp issued has completed
+  uint64_t* accfull = mdone + 1;  // TCV: [32] tile t's accumulator holds step ks's bias
+  uint64_t* tready = accfull + 32;  // TCV: [16] slab j has been copied into TMEM
+  uint64_t* rfull = tready + 16;    // TCV: [16] resident slab i has landed
+  uint8_t* res = smem + Lay.res;
+  uint8_t* ebf = smem + Lay.ebf;
 
   constexpr int VEC = Vec<WT>::N;
   constexpr int SR = 8 / NB;  // rows per sub-group: SR rows x NB requests = 8 sums per lane
@@ -486,11 +523,24 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
   const int NS = p.nstages;
   const int nst = (SL + R - 1) / R;
   const bool ubulk = p.u_bulk && SL > 0;
+  // TCV geometry: tiles of 128 rows, r / 64 slabs each, in the order slab_at gives
+  const int nsk = r / 64;
+  const int nt = TCV ? (SL + 127) / 128 : 0;
+  const int nall = nt * nsk;
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 4);  // the four warps sharing a stage
+      mbar_init(&empty[i], TCV ? 1 : 4);  // the MMA (or a copying group) / the four warps
+    }
+    if (TCV) {
+      mbar_init(efull, 1);
+      mbar_init(mdone, 1);
+      for (int i = 0; i < 32; ++i) mbar_init(&accfull[i], 1);
+      for (int i = 0; i < 16; ++i) {
+        mbar_init(&tready[i], 1);
+        mbar_init(&rfull[i], 1);
+      }
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ufull[i], 1);
@@ -509,8 +559,11 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
     ms->valid[b] = ok;
     if (b < B && !ok) atomicMax(&hdr->status, kErrInvalid);
   }
-  const int nres = min(p.nres, nst);  // stages of the slice cached in TMEM after the first step
-  if (nres > 0 && warp == 0) {
+  // stages (CUDA cores) or slabs (tensor cores) of the slice cached in TMEM after the first step
+  const int nres = TCV ? min(p.nres, nall) : min(p.nres, nst);
+  const int nres_s = TCV ? min(p.nres_s, nall - nres) : 0;  // slabs resident in shared memory
+  const bool use_tmem = TCV || nres > 0;
+  if (use_tmem && warp == 0) {
     tc::tmem_alloc(&ms->tmem_base, 512);
     tc::tmem_relinquish();
   }
@@ -546,21 +599,50 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
           }
           u_issued = ks + 1;
         }
-        for (int s = (ks == 0 ? 0 : nres); s < nst; ++s, ++g) {
-          const int slot = g % NS;
-          if (g >= NS &&
-              !mbar_wait_or_abort(&empty[slot], (uint32_t)(((g - NS) / NS) & 1), &ms->abort)) {
-            stop = true;
-            break;
+        if constexpr (TCV) {
+          if (ks == 0)  // resident slabs: straight to their own buffers, once
+            for (int i = 0; i < nres_s; ++i) {
+              int t, sk;
+              slab_at(nres + i, nsk, t, sk);
+              mbar_expect_tx(&rfull[i], 16384u);
+              tc::tma_load_2d(res + (size_t)i * 16384, &tmW2, 64 * sk, v0 + 128 * t, &rfull[i],
+                              pol_w);
+            }
+          // ring slabs in the MMA's order: on the first step every slab but the resident ones
+          // (those bound for TMEM first), later only the streamed ones
+          for (int j = ks == 0 ? 0 : nres + nres_s; j < nall; ++j) {
+            if (ks == 0 && j >= nres && j < nres + nres_s) continue;
+            const int slot = g % NS;
+            if (g >= NS &&
+                !mbar_wait_or_abort(&empty[slot], (uint32_t)(((g - NS) / NS) & 1), &ms->abort)) {
+              stop = true;
+              break;
+            }
+            int t, sk;
+            slab_at(j, nsk, t, sk);
+            ms->stage_tag[slot] = g;
+            mbar_expect_tx(&full[slot], 16384u);
+            tc::tma_load_2d(ring + (size_t)slot * 16384, &tmW2, 64 * sk, v0 + 128 * t, &full[slot],
+                            pol_w);
+            issued = ++g;
           }
-          const int rows = min(R, SL - s * R);
-          const uint32_t bytes = (uint32_t)(rows * row_bytes);
-          ms->stage_tag[slot] = g;
-          mbar_expect_tx(&full[slot], bytes);
-          bulk_g2s(ring + (size_t)slot * p.stage_bytes,
-                   (const uint8_t*)p.W2 + (size_t)(v0 + s * R) * row_bytes, bytes, &full[slot],
-                   pol_w);
-          issued = g + 1;
+        } else {
+          for (int s = (ks == 0 ? 0 : nres); s < nst; ++s, ++g) {
+            const int slot = g % NS;
+            if (g >= NS &&
+                !mbar_wait_or_abort(&empty[slot], (uint32_t)(((g - NS) / NS) & 1), &ms->abort)) {
+              stop = true;
+              break;
+            }
+            const int rows = min(R, SL - s * R);
+            const uint32_t bytes = (uint32_t)(rows * row_bytes);
+            ms->stage_tag[slot] = g;
+            mbar_expect_tx(&full[slot], bytes);
+            bulk_g2s(ring + (size_t)slot * p.stage_bytes,
+                     (const uint8_t*)p.W2 + (size_t)(v0 + s * R) * row_bytes, bytes, &full[slot],
+                     pol_w);
+            issued = g + 1;
+          }
         }
       }
       if (stop) atomicMax(&hdr->status, kErrTimeout);
@@ -569,6 +651,93 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
         mbar_wait(&full[g % NS], (uint32_t)((g / NS) & 1));
       for (int k = max(0, u_issued - 2); k < u_issued; ++k)
         mbar_wait(&ufull[k & 1], (uint32_t)((k >> 1) & 1));
+      if (TCV)
+        for (int i = 0; i < nres_s; ++i) mbar_wait(&rfull[i], 0);
+    }
+    return;
+  }
+
+  // =========================================================== MMA warp (TCV)
+  if (TCV && warp == kCWarps + 1) {
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16_f32(128, 16);
+      const uint32_t tmem = ms->tmem_base;
+      const uint32_t acc0 = tmem + 32 * p.nres;  // accumulators follow the largest TMEM cache
+      // operand descriptors, built once: B (K block sk, K step kk) and the bases of the ring
+      // and the resident slabs
+      uint64_t bdesc[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        bdesc[q] = tc::sdesc_sw128(smem_u32(ebf) + (q >> 2) * 2048 + (q & 3) * 32);
+      const uint64_t ring_desc = tc::sdesc_sw128(smem_u32(ring));
+      const uint64_t res_desc = tc::sdesc_sw128(smem_u32(res));
+      bool stop = false;
+      int g = nres;  // ring uses 0 .. nres-1 carry the first step's TMEM-bound slabs
+      for (int ks = 0; ks < G && !stop; ++ks) {
+        if (!mbar_wait_or_abort(efull, (uint32_t)(ks & 1), &ms->abort)) {
+          stop = true;
+          break;
+        }
+        tc::fence_after_sync();
+        // after the first step the tiles that stream through the ring go first, so the ring
+        // refills while the MMAs read the resident tiles
+        const int tr0 = ks == 0 ? 0 : min(nt, (nres + nres_s) / nsk);
+        for (int n = 0; n < nt && !stop; ++n) {
+          const int t = tile_at(n, tr0, nt);
+          const uint32_t d = acc0 + 16 * t;
+#pragma unroll
+          for (int sk = 0; sk < 4; ++sk) {  // nsk <= 4 K blocks; unrolled so bdesc stays in registers
+            if (sk >= nsk) break;
+            const int i = t * nsk + sk;  // position in the slab order (tile by tile)
+            const uint64_t* bd = bdesc + 4 * sk;
+            if (i < nres) {  // A from TMEM (copied there during the first step)
+              if (ks == 0) {
+                if (!mbar_wait_or_abort(&tready[i], 0, &ms->abort)) {
+                  stop = true;
+                  break;
+                }
+                tc::fence_after_sync();
+              }
+              const uint32_t a = tmem + 32 * i;
+              if (sk == 0) tc::mma_bf16_ts_c<false>(d, a, bd[0], idesc);
+              else tc::mma_bf16_ts_c<true>(d, a, bd[0], idesc);
+              tc::mma_bf16_ts_c<true>(d, a + 8, bd[1], idesc);
+              tc::mma_bf16_ts_c<true>(d, a + 16, bd[2], idesc);
+              tc::mma_bf16_ts_c<true>(d, a + 24, bd[3], idesc);
+            } else {
+              int slot = -1;
+              uint64_t ad;
+              if (i < nres + nres_s) {  // A resident in shared memory
+                if (ks == 0 && !mbar_wait_or_abort(&rfull[i - nres], 0, &ms->abort)) {
+                  stop = true;
+                  break;
+                }
+                ad = res_desc + (uint64_t)((i - nres) * 1024);  // 16 KB per slab, in 16 B units
+              } else {  // A streamed through the ring
+                slot = g % NS;
+                if (!mbar_wait_or_abort(&full[slot], (uint32_t)((g / NS) & 1), &ms->abort)) {
+                  stop = true;
+                  break;
+                }
+                tc::fence_after_sync();
+                ad = ring_desc + (uint64_t)(slot * 1024);
+                ++g;
+              }
+              // a K step of 16 elements is 32 bytes further along the swizzled rows: +2 in the
+              // descriptor's address field
+              if (sk == 0) tc::mma_bf16_c<false>(d, ad, bd[0], idesc);
+              else tc::mma_bf16_c<true>(d, ad, bd[0], idesc);
+              tc::mma_bf16_c<true>(d, ad + 2, bd[1], idesc);
+              tc::mma_bf16_c<true>(d, ad + 4, bd[2], idesc);
+              tc::mma_bf16_c<true>(d, ad + 6, bd[3], idesc);
+              if (slot >= 0) tc::mma_commit(&empty[slot]);  // free once these MMAs have read it
+            }
+          }
+          if (!stop) tc::mma_commit(&accfull[t]);
+        }
+      }
+      if (stop) atomicMax(&hdr->status, kErrTimeout);
+      tc::mma_commit(mdone);  // lets the TMEM owner free the columns once these MMAs are done
     }
     return;
   }
@@ -580,6 +749,10 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
     for (int j = tid; j < r; j += kCThreads) sbuf[j] = p.s0 ? p.s0[(size_t)cta * r + j] : 0.f;
   if (conf && G == 1) hidden_dots<WT, kCThreads>(p, ms, tid, cta, nCTA);
   fill_noise<NB>(gbuf, SLM, SL, v0, B, 0, p.seed_lo, p.seed_hi, tid, kCThreads);
+
+  if (TCV) {  // the B operand's padding rows stay zero
+    for (int i = tid; i < nsk * 512; i += kCThreads) ((uint32_t*)ebf)[i] = 0u;
+  }
 
   bool failed = false;
   // after the 8-value reduction lane l holds value (l >> 2) = (row, request) = (idx/NB, idx%NB);
@@ -618,19 +791,50 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
       }
       csync<kCThreads>();
     }
-    // (b) this lane's K-chunks of every e_b (RNN: a_k) in registers
+    // (b) this lane's K-chunks of every e_b (RNN: a_k) in registers; TCV: the MMA's B operand
     using DT = typename std::conditional<RNN, DotF<WT>, Dot<WT>>::type;
     const float* cvec = RNN ? rbuf : ebuf;
     typename DT::E ereg[NB][NCV][DT::NE];
+    if constexpr (TCV) {
+      // row b = bf16(e_b) (exact: e_b is a bf16 row of W1); RNN: row b = bf16(a_b) and row
+      // 8 + b = bf16(a_b - that), so the two columns add up to a_b within 2^-16 relative.
+      // 16-byte chunk c of row n sits in K block c / 8 at chunk position (c % 8) ^ (n % 8).
+      const int nch = r / 8;
+      for (int i = tid; i < NB * nch; i += kCThreads) {
+        const int b = i / nch, c = i - b * nch;
+        const float* src = cvec + b * r + 8 * c;
+        uint32_t hi[4], lo[4];
 #pragma unroll
-    for (int b = 0; b < NB; ++b)
-#pragma unroll
-      for (int t = 0; t < NCV; ++t) {
-        const int cv = lane + 32 * t;
-#pragma unroll
-        for (int i = 0; i < DT::NE; ++i)
-          ereg[b][t][i] = cv < VR ? DT::load_e(cvec + b * r + cv * VEC, i) : typename DT::E(0);
+        for (int q = 0; q < 4; ++q) {
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(src[2 * q], src[2 * q + 1]);
+          hi[q] = *(const uint32_t*)&h2;
+          if (RNN) {
+            const float2 hf = __bfloat1622float2(h2);
+            const __nv_bfloat162 l2 = __floats2bfloat162_rn(src[2 * q] - hf.x, src[2 * q + 1] - hf.y);
+            lo[q] = *(const uint32_t*)&l2;
+          }
+        }
+        const int blk = (c >> 3) * 2048, cc = c & 7;
+        *(uint4*)(ebf + blk + b * 128 + ((cc ^ (b & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        if (RNN) {
+          const int n = 8 + b;
+          *(uint4*)(ebf + blk + n * 128 + ((cc ^ (n & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
       }
+      fence_proxy_async_smem();  // generic-proxy writes, read by the tensor cores
+      csync<kCThreads>();
+      if (tid == 0) mbar_arrive(efull);
+    } else {
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int t = 0; t < NCV; ++t) {
+          const int cv = lane + 32 * t;
+#pragma unroll
+          for (int i = 0; i < DT::NE; ++i)
+            ereg[b][t][i] = cv < VR ? DT::load_e(cvec + b * r + cv * VEC, i) : typename DT::E(0);
+        }
+    }
     // (c) U_k (and target) rows of the slice
     if (ubulk) {
       const bool ok = mbar_wait(&ufull[buf], (uint32_t)((ks >> 1) & 1));
@@ -677,10 +881,85 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
         ybuf[(size_t)bq * SLM + vl] = y;
       }
     };
+    // TCV: one thread per vocabulary row and all requests; slot sb[b] per request
+    Slot sb[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) slot_init(sb[b]);
+    if constexpr (TCV) {
+      const uint32_t tmem = ms->tmem_base;
+      const uint32_t lq = (uint32_t)(32 * qw) << 16;  // this warp's TMEM lane quarter
+      if (ks == 0) {
+        // slabs bound for TMEM: the group's four warps copy rows 32 qw + lane of each (one
+        // 16-byte chunk at a time out of the swizzled slab) into TMEM columns [32 j, 32 j + 32)
+        for (int j = grp; j < nres; j += kGroups) {
+          const int slot = j % NS;  // ring use j
+          const bool okw = __all_sync(0xffffffffu, wait_stage(ms->stage_tag, full, slot, j, NS));
+          if (gsync_or(grp, !okw)) {
+            wfail = true;
+            break;
+          }
+          const uint8_t* sp = ring + (size_t)slot * 16384;
+          const int m = 32 * qw + lane;
+          uint32_t wv[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *(uint4*)&wv[4 * c] = *(const uint4*)(sp + m * 128 + ((c ^ (m & 7)) << 4));
+          tc::tmem_st32(tmem + lq + 32 * j, wv);
+          tc::tmem_st_wait();
+          tc::fence_before_sync();
+          gsync_or(grp, 0);
+          if (qw == 0 && lane == 0) {
+            mbar_arrive(&tready[j]);
+            mbar_arrive(&empty[slot]);
+          }
+        }
+      }
+      const uint32_t acc0 = tmem + 32 * p.nres;
+      const int tr0 = ks == 0 ? 0 : min(nt, (nres + nres_s) / nsk);  // the MMA warp's order
+      for (int n = grp; n < nt && !wfail; n += kGroups) {
+        const int t = tile_at(n, tr0, nt);
+        const bool oka = mbar_wait_warp(&accfull[t], (uint32_t)(ks & 1));
+        if (!oka) {
+          wfail = true;
+          break;
+        }
+        tc::fence_after_sync();
+        uint32_t acc[16];
+        tc::tmem_ld16(acc0 + lq + 16 * t, acc);
+        tc::tmem_ld_wait();
+        const int vl = 128 * t + 32 * qw + lane;
+        if (vl < SL) {
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            if (b >= B) break;
+            float bias = __uint_as_float(acc[b]);
+            if (RNN) bias += __uint_as_float(acc[8 + b]);
+            const int v = v0 + vl;
+            const float uval =
+                p.u_bf16 ? __uint_as_float((uint32_t)((const uint16_t*)ubuf)[(size_t)(buf * NB + b) * SLM + vl] << 16)
+                         : ((const float*)ubuf)[(size_t)(buf * NB + b) * SLM + vl];
+            const float z = uval + bias;
+            if (p.logits) p.logits[((size_t)b * G + ks) * V + v] = z;
+            const float y = z * p.invT;
+            lse_push(sb[b].m, sb[b].l, y);
+            const float sc = y + gbuf[(size_t)b * SLM + vl];
+            if (sc > sb[b].best) {  // v grows along this thread's rows: ties keep the smaller v
+              sb[b].best = sc;
+              sb[b].tok = (uint32_t)v;
+            }
+            if (tgt) {
+              lse_push(sb[b].mt, sb[b].lt, tbuf[(size_t)(buf * NB + b) * SLM + vl] * p.invT);
+              ybuf[(size_t)b * SLM + vl] = y;
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();  // the accumulators are read: the next step may overwrite them
+    }
     // Four warps share each stage: warp q of a group takes rows [q R/4, (q+1) R/4) in
     // sub-groups of SR rows, so a slot is handed back a quarter of a stage's work after its
     // bytes land.  Stages go round-robin to the groups.
-    for (int s = grp; s < nst; s += kGroups) {
+    for (int s = grp; s < (TCV ? 0 : nst); s += kGroups) {
       const int rows = min(R, SL - s * R);
       const int rq0 = qw * (R / 4), rq1 = min(rows, rq0 + R / 4);
       if (R == 32 && NCV == 1) {
@@ -706,8 +985,8 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
           for (int j = 0; j < 8; ++j)
             *(uint4*)&wv[4 * j] = *(const uint4*)(stg + (size_t)(rq0 + j) * row_bytes + cv * 16);
           if (ks == 0 && s < nres) {
-            tmem_st32(taddr, wv);
-            tmem_st_wait();
+            tc::tmem_st32(taddr, wv);
+            tc::tmem_st_wait();
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[slot]);
@@ -776,24 +1055,50 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
     // the grid barrier's arrival too.  With a target the second pass right after the barrier
     // needs the global normalisers, so the (max, sum-exp) partials go out before the key;
     // without one only the argmax is on the critical path and the partials follow the key.
-    unsigned long long key = st.tok != 0xFFFFFFFFu ? tagged_key(st.best, st.tok, ks) : 0ull;
+    if constexpr (TCV) {
 #pragma unroll
-    for (int o = 4 * NB; o < 32; o <<= 1) {
-      const unsigned long long q = __shfl_xor_sync(0xffffffffu, key, o);
-      key = q > key ? q : key;
-      lse_merge(st.m, st.l, __shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.l, o));
-      if (tgt)
-        lse_merge(st.mt, st.lt, __shfl_xor_sync(0xffffffffu, st.mt, o),
-                  __shfl_xor_sync(0xffffffffu, st.lt, o));
-    }
-    if (lane < 4 * NB && owner) {
-      Slot& o = slots[warp * 4 + (lane >> 2)];
-      o.best = __uint_as_float((uint32_t)(key >> 32));
-      o.tok = (uint32_t)key;
-      o.m = st.m;
-      o.l = st.l;
-      o.mt = st.mt;
-      o.lt = st.lt;
+      for (int b = 0; b < NB; ++b) {
+        Slot& a = sb[b];
+        unsigned long long key = a.tok != 0xFFFFFFFFu ? tagged_key(a.best, a.tok, ks) : 0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const unsigned long long q = __shfl_xor_sync(0xffffffffu, key, o);
+          key = q > key ? q : key;
+          lse_merge(a.m, a.l, __shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.l, o));
+          if (tgt)
+            lse_merge(a.mt, a.lt, __shfl_xor_sync(0xffffffffu, a.mt, o),
+                      __shfl_xor_sync(0xffffffffu, a.lt, o));
+        }
+        if (lane == 0) {
+          Slot& o = slots[warp * 4 + b];
+          o.best = __uint_as_float((uint32_t)(key >> 32));
+          o.tok = (uint32_t)key;
+          o.m = a.m;
+          o.l = a.l;
+          o.mt = a.mt;
+          o.lt = a.lt;
+        }
+      }
+    } else {
+      unsigned long long key = st.tok != 0xFFFFFFFFu ? tagged_key(st.best, st.tok, ks) : 0ull;
+#pragma unroll
+      for (int o = 4 * NB; o < 32; o <<= 1) {
+        const unsigned long long q = __shfl_xor_sync(0xffffffffu, key, o);
+        key = q > key ? q : key;
+        lse_merge(st.m, st.l, __shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.l, o));
+        if (tgt)
+          lse_merge(st.mt, st.lt, __shfl_xor_sync(0xffffffffu, st.mt, o),
+                    __shfl_xor_sync(0xffffffffu, st.lt, o));
+      }
+      if (lane < 4 * NB && owner) {
+        Slot& o = slots[warp * 4 + (lane >> 2)];
+        o.best = __uint_as_float((uint32_t)(key >> 32));
+        o.tok = (uint32_t)key;
+        o.m = st.m;
+        o.l = st.l;
+        o.mt = st.mt;
+        o.lt = st.lt;
+      }
     }
     csync<kCThreads>();
     if (warp < B) {
@@ -904,8 +1209,11 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
     if (ubulk && tid == 0) mbar_arrive(&uempty[buf]);
   }
 
-  // TMEM is no longer read: hand it back (every consumer warp has waited for its own loads)
-  if (nres > 0) {
+  // TMEM is no longer read: hand it back (every consumer warp has waited for its own loads;
+  // with the tensor cores, the MMA warp's last commit says its MMAs are done too)
+  if (failed) ms->abort = 1;  // a waiting producer or MMA warp gives up at once
+  if (use_tmem) {
+    if (TCV && warp == 0) mbar_wait(mdone, 0);
     tc::fence_before_sync();
     csync<kCThreads>();
     if (warp == 0) {
@@ -1005,17 +1313,33 @@ __global__ void __launch_bounds__(CW * 32 + 32, 1) draft_cc_kernel(const DraftPa
   }
 }
 
-template <typename WT, int NB, int NCV>
-cudaError_t launch_t(DraftParams& p, int nblocks, cudaStream_t stream) {
+template <typename WT, int NB, int NCV, bool TCV>
+cudaError_t launch_k(DraftParams& p, const CUtensorMap& tm, int nblocks, cudaStream_t stream) {
   constexpr int CW = NB <= 2 ? 16 : 8;
-  constexpr int kThreads = CW * 32 + 32;
-  auto kern = p.head == 1 ? draft_cc_kernel<WT, NB, NCV, CW, true> : draft_cc_kernel<WT, NB, NCV, CW, false>;
+  constexpr int kThreads = CW * 32 + 32 + (TCV ? 32 : 0);
+  auto kern = p.head == 1 ? draft_cc_kernel<WT, NB, NCV, CW, true, TCV>
+                          : draft_cc_kernel<WT, NB, NCV, CW, false, TCV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)p.smem_bytes);
   if (e != cudaSuccess) return e;
-  void* args[] = {(void*)&p};
+  void* args[] = {(void*)&p, (void*)&tm};
   return cudaLaunchCooperativeKernel((const void*)kern, dim3(nblocks), dim3(kThreads), args,
                                      p.smem_bytes, stream);
+}
+
+template <typename WT, int NB, int NCV>
+cudaError_t launch_t(DraftParams& p, int nblocks, cudaStream_t stream) {
+  CUtensorMap tm;
+  std::memset(&tm, 0, sizeof tm);
+  if constexpr (std::is_same<WT, __nv_bfloat16>::value && NCV == 1) {
+    if (p.tcv) {
+      // W2 [V][r] as 128-row x 64-column tiles in the 128-byte swizzle
+      if (!encode_bf16_2d(&tm, p.W2, p.V, p.r, p.r, 128)) return cudaErrorInvalidValue;
+      return launch_k<WT, NB, NCV, true>(p, tm, nblocks, stream);
+    }
+  }
+  if (p.tcv) return cudaErrorNotSupported;
+  return launch_k<WT, NB, NCV, false>(p, tm, nblocks, stream);
 }
 
 template <typename WT, int NCV>
@@ -1034,9 +1358,41 @@ int draft_cc_supported(int B, int r, int w_bf16) {
   return B >= 1 && B <= 4 && row_bytes % 16 == 0 && row_bytes <= 1024;
 }
 
+// Tensor-core variant: bf16, B <= 4, K = r in whole 64-element blocks with one 128-row tile of A
+// in at most 128 TMEM columns, and at most 32 tiles (16 accumulator columns each) per slice.
+int draft_tcv_supported(int B, int r, int w_bf16, int slice_max) {
+  return w_bf16 && B >= 1 && B <= 4 && r % 64 == 0 && r <= 256 && slice_max >= 1 &&
+         (slice_max + 127) / 128 <= 32;
+}
+
 // Ring geometry: stages of at least 16 KB holding a multiple of 32 W2 rows, as many stages as
 // the shared memory left after the per-step buffers allows (at most 16).
 bool draft_cc_configure(DraftParams& p, size_t smem_optin) {
+  if (p.tcv) {
+    // 16 KB slabs; TMEM holds the accumulators (16 columns per tile) and as many 32-column
+    // slabs as fit beside them (at most 16); shared memory holds a ring of up to 6 slabs and,
+    // from what is left, up to 16 resident slabs
+    const int nsk = p.r / 64, ntmax = (p.slice_max + 127) / 128;
+    const int nall = ntmax * nsk;
+    p.stage_bytes = 16384;
+    int nres = (512 - 16 * ntmax) / 32;
+    nres = nres < 0 ? 0 : nres > 16 ? 16 : nres;
+    p.nres = nres < nall ? nres : nall;
+    p.nstages = 0;
+    p.nres_s = 0;
+    const size_t base = cc_layout(p, nb_of(p.B)).total;
+    const size_t avail = smem_optin > base + 64 ? smem_optin - base - 64 : 0;
+    int slabs = (int)(avail / (16384 + 16));
+    const int rest = nall - p.nres;
+    if (slabs < 2) return false;
+    p.nstages = slabs < 6 ? slabs : 6;
+    if (p.nstages > rest) p.nstages = rest < 1 ? 1 : rest;
+    int nres_s = slabs - p.nstages;
+    if (nres_s > rest - p.nstages) nres_s = rest - p.nstages;
+    p.nres_s = nres_s < 0 ? 0 : nres_s > 16 ? 16 : nres_s;
+    p.smem_bytes = cc_layout(p, nb_of(p.B)).total;
+    return p.smem_bytes <= smem_optin;
+  }
   const int row_bytes = p.r * (p.w_bf16 ? 2 : 4);
   int rows = 16384 / row_bytes;
   rows = rows < 32 ? 32 : rows / 32 * 32;

@@ -653,24 +653,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled encoder() {
-  static EncodeTiled fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (EncodeTiled)f;
-  }
-  return fn;
-}
-
 }  // namespace
 
 int draft_tc_supported(int B, int r, int w_bf16) { return w_bf16 && B >= 1 && r % 8 == 0 && r <= 512; }
@@ -692,18 +674,8 @@ bool draft_tc_configure(DraftParams& p, size_t smem_optin) {
 }
 
 cudaError_t launch_draft_tc(DraftParams& p, int nblocks, cudaStream_t stream) {
-  EncodeTiled enc = encoder();
-  if (!enc) return cudaErrorNotSupported;
   CUtensorMap tmap;
-  const cuuint64_t gdim[2] = {(cuuint64_t)p.r, (cuuint64_t)p.V};
-  const cuuint64_t gstride[1] = {(cuuint64_t)p.r * 2};
-  const cuuint32_t box[2] = {64, kNT};
-  const cuuint32_t estride[2] = {1, 1};
-  CUresult cr = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.W2), gdim,
-                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  if (!encode_bf16_2d(&tmap, p.W2, p.V, p.r, p.r, kNT)) return cudaErrorInvalidValue;
   const void* kern = p.head == 1 ? (const void*)draft_tc_kernel<true> : (const void*)draft_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)p.smem_bytes);

@@ -122,12 +122,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
   }
 }
 
+}  // namespace
+
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiled gemm_encoder() {
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link against the driver
+// library), looked up once.
+static EncodeTiled tmap_encoder() {
   static EncodeTiled fn = nullptr;
   if (!fn) {
     void* f = nullptr;
@@ -140,8 +144,9 @@ EncodeTiled gemm_encoder() {
   return fn;
 }
 
-bool make_map(EncodeTiled enc, CUtensorMap* m, const void* base, int rows, int cols, int ld,
-              int box_rows) {
+bool encode_bf16_2d(CUtensorMap* m, const void* base, int rows, int cols, int ld, int box_rows) {
+  EncodeTiled enc = tmap_encoder();
+  if (!enc) return false;
   const cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t gstride[1] = {(cuuint64_t)ld * 2};
   const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
@@ -151,8 +156,6 @@ bool make_map(EncodeTiled enc, CUtensorMap* m, const void* base, int rows, int c
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
 size_t gemm_tc_smem_bytes() { return (size_t)kGStages * kGStage + 1024 + 256; }
 
 // part[ks][M][N] = A[M][K] Bm[N][K]^T over split ks; A row stride lda, Bm row stride ldb
@@ -161,10 +164,8 @@ size_t gemm_tc_smem_bytes() { return (size_t)kGStages * kGStage + 1024 + 256; }
 cudaError_t launch_gemm_tc(const void* A, int lda, const void* Bm, int ldb, int M, int N, int K,
                            float* part, int max_split, int nsm, int* ksplit_out, unsigned* status,
                            cudaStream_t stream) {
-  EncodeTiled enc = gemm_encoder();
-  if (!enc) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
-  if (!make_map(enc, &ta, A, M, K, lda, kGM) || !make_map(enc, &tb, Bm, N, K, ldb, kGN))
+  if (!encode_bf16_2d(&ta, A, M, K, lda, kGM) || !encode_bf16_2d(&tb, Bm, N, K, ldb, kGN))
     return cudaErrorInvalidValue;
   const int nslab = (K + 63) / 64;
   const int tiles = ((M + kGM - 1) / kGM) * ((N + kGN - 1) / kGN);

@@ -59,8 +59,25 @@ def test_host_validation_without_gpu(lib):
     assert lib.dspark_tv_label(0, 10, 1.0, p, p, p, None, None) == 1
 
 
-def test_path_selection(lib):
+def test_path_override(lib, monkeypatch):
+    monkeypatch.setenv("DSPARK_DRAFT_PATH", "cuda-core")
+    assert lib.dspark_draft_path(0, 1, 151936, 256, 1) == 0
+    monkeypatch.setenv("DSPARK_DRAFT_PATH", "tensor")
+    assert lib.dspark_draft_path(0, 1, 151936, 256, 1) == 1
+    monkeypatch.setenv("DSPARK_DRAFT_PATH", "tensor-vocab")
+    assert lib.dspark_draft_path(0, 4, 151936, 72, 1) == -1      # that kernel cannot run it
+    assert lib.dspark_draft_path(0, 8, 151936, 256, 1) == -1
+    monkeypatch.setenv("DSPARK_DRAFT_PATH", "something-else")     # unknown: automatic choice
+    assert lib.dspark_draft_path(0, 1, 151936, 256, 1) == 0
+    assert lib.dspark_draft_path(0, 4, 151936, 256, 1) == 2
+
+
+def test_path_selection(lib, monkeypatch):
+    monkeypatch.delenv("DSPARK_DRAFT_PATH", raising=False)
     from semi_autoregressive_drafting_gb300 import _lib
     assert lib.dspark_draft_path(0, 1, 151936, 256, 1) == 0      # latency regime: CUDA cores
+    assert lib.dspark_draft_path(0, 2, 151936, 256, 1) == 0
+    assert lib.dspark_draft_path(0, 3, 151936, 256, 1) == 2      # tensor cores, vocabulary on M
+    assert lib.dspark_draft_path(0, 4, 151936, 72, 1) == 0       # rank not in 64-blocks: CUDA cores
     assert lib.dspark_draft_path(0, 4, 4096, 64, 0) == 0
     assert lib.dspark_draft_path(0, 1, 151936, 250, 1) == -1     # invalid rank

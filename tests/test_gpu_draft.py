@@ -23,6 +23,16 @@ def _run_case(wl, **kw):
     return parity.run_case(wl, ds=ds, **kw)
 
 
+# bf16 cases with B <= 4 run on both small-batch kernels: CUDA-core dot products (path 0) and
+# the tensor-core bias product with vocabulary rows on M (path 2)
+SMALL_PATHS = [("cuda-core", 0), ("tensor-vocab", 2)]
+
+
+def _use_path(monkeypatch, name, code, wl, head=0):
+    monkeypatch.setenv("DSPARK_DRAFT_PATH", name)
+    assert ds.draft_path(head, wl.B, wl.V, wl.r, wl.dtype == "bf16") == code
+
+
 def test_tiny_markov_workload():
     _run_case(TINY)
 
@@ -51,9 +61,34 @@ def test_vocab_smaller_than_grid():
     _run_case(TINY.with_(V=40, B=2, seed=33), target_noise=1.0)
 
 
-def test_bf16_small_with_target():
+@pytest.mark.parametrize("name,code", SMALL_PATHS)
+def test_bf16_small_with_target(monkeypatch, name, code):
     wl = inputs.WORKLOADS["qwen3_4b_markov"].with_(V=20008, d=512, B=3, seed=34)
+    _use_path(monkeypatch, name, code, wl)
     _run_case(wl, target_noise=1.0)
+
+
+@pytest.mark.parametrize("name,code", SMALL_PATHS)
+@pytest.mark.parametrize("B", [1, 2, 4])
+def test_bf16_batches_both_paths(monkeypatch, name, code, B):
+    wl = inputs.WORKLOADS["qwen3_4b_markov"].with_(V=30000, d=256, B=B, seed=50 + B)
+    _use_path(monkeypatch, name, code, wl)
+    _run_case(wl)
+
+
+@pytest.mark.parametrize("V", [1000, 130, 40])
+def test_tensor_vocab_partial_tiles(monkeypatch, V):
+    # slices of a few rows: one partial 128-row tile per block, or none at all
+    wl = inputs.WORKLOADS["qwen3_4b_markov"].with_(V=V, d=64, B=2, seed=60 + V)
+    _use_path(monkeypatch, "tensor-vocab", 2, wl)
+    _run_case(wl, target_noise=1.0)
+
+
+@pytest.mark.parametrize("r", [64, 128, 192])
+def test_tensor_vocab_ranks(monkeypatch, r):
+    wl = inputs.WORKLOADS["qwen3_4b_markov"].with_(V=50000, r=r, d=64, B=3, seed=70 + r)
+    _use_path(monkeypatch, "tensor-vocab", 2, wl)
+    _run_case(wl, target_noise=0.5)
 
 
 def test_bf16_rank_512():
@@ -61,17 +96,30 @@ def test_bf16_rank_512():
     _run_case(wl)
 
 
-def test_ring_reuse_more_stages_than_slots():
+@pytest.mark.parametrize("name,code", SMALL_PATHS)
+def test_ring_reuse_more_stages_than_slots(monkeypatch, name, code):
     # every block streams more W2 stages than the ring has slots, so slots are reused within a
     # step and warps reach a slot before its previous use completes
     wl = inputs.WORKLOADS["qwen3_4b_markov"].with_(V=80000, d=128, B=1, seed=36)
+    _use_path(monkeypatch, name, code, wl)
     _run_case(wl, want_logits=False)
     _run_case(wl.with_(B=2, seed=37), want_logits=False)
 
 
+@pytest.mark.parametrize("name,code", SMALL_PATHS)
+def test_qwen3_4b_vocab_small_hidden(monkeypatch, name, code):
+    # the full vocabulary: every slab kind of the tensor-core variant (TMEM, resident, streamed)
+    wl = inputs.WORKLOADS["qwen3_4b_markov"].with_(d=256, seed=38)
+    _use_path(monkeypatch, name, code, wl)
+    _run_case(wl, want_logits=False)
+
+
 @pytest.mark.slow
-def test_qwen3_4b_markov_full():
-    ties, _ = _run_case(inputs.WORKLOADS["qwen3_4b_markov"], want_logits=False)
+@pytest.mark.parametrize("name,code", SMALL_PATHS)
+def test_qwen3_4b_markov_full(monkeypatch, name, code):
+    wl = inputs.WORKLOADS["qwen3_4b_markov"]
+    _use_path(monkeypatch, name, code, wl)
+    ties, _ = _run_case(wl, want_logits=False)
     assert ties <= 1
 
 

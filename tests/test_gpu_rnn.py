@@ -1,8 +1,9 @@
 """GPU parity of the RNN-head draft (Eq 6) against the fp64 oracle.
 
 The sequential update runs in fp32 on the CUDA cores, the h_k columns of the joint projection
-come from the tensor-core pre-pass GEMM, and the bias product uses fp32 a_k = tanh(o_k) (small
-batches) or a bf16 high/low split of a_k on the tensor cores (larger batches).  Same rules as
+come from the tensor-core pre-pass GEMM, and the bias product uses fp32 a_k = tanh(o_k) on the
+CUDA cores, or a bf16 high/low split of a_k on the tensor cores (larger batches, and small ones
+on the vocabulary-major tensor-core variant).  Same rules as
 the Markov tests: tokens bit-exact up to counted near-ties, floats (and the final state) within
 2e-3.
 """
@@ -17,15 +18,24 @@ pytestmark = pytest.mark.gpu
 RNN = inputs.WORKLOADS["rnn_head"]
 
 
+SMALL_PATHS = [("cuda-core", 0), ("tensor-vocab", 2)]
+
+
+@pytest.mark.parametrize("name,code", SMALL_PATHS)
 @pytest.mark.parametrize("B", [1, 3])
-def test_rnn_small_batch(B):
+def test_rnn_small_batch(monkeypatch, name, code, B):
     wl = RNN.with_(B=B, V=12000, d=128, seed=100 + B)
-    assert ds.draft_path(1, B, wl.V, wl.r) == 0
+    monkeypatch.setenv("DSPARK_DRAFT_PATH", name)
+    assert ds.draft_path(1, B, wl.V, wl.r) == code
     parity.run_case(wl, ds=ds, s0_scale=0.5)
 
 
-def test_rnn_small_batch_rank64_target():
-    parity.run_case(RNN.with_(B=2, V=8008, r=64, d=64, seed=104), ds=ds, target_noise=1.0)
+@pytest.mark.parametrize("name,code", SMALL_PATHS)
+def test_rnn_small_batch_rank64_target(monkeypatch, name, code):
+    wl = RNN.with_(B=2, V=8008, r=64, d=64, seed=104)
+    monkeypatch.setenv("DSPARK_DRAFT_PATH", name)
+    assert ds.draft_path(1, wl.B, wl.V, wl.r) == code
+    parity.run_case(wl, ds=ds, target_noise=1.0)
 
 
 @pytest.mark.parametrize("B", [8, 64])
