@@ -20,6 +20,8 @@
 //     over the block's slice after the barrier from y saved in the workspace.
 #include <cuda.h>
 
+#include <cstring>
+
 #include "draft.cuh"
 #include "rnn.cuh"
 #include "tc.cuh"
@@ -51,24 +53,29 @@ struct TMisc {
 };
 
 struct TCLayout {
-  size_t a, ring, scratch, rnnbuf, misc, bars, total;
-  int nslab, na, nstage, aslabs;
+  size_t a, ring, ubuf, scratch, rnnbuf, misc, bars, total;
+  int nslab, na, nstage, aslabs, nu;
 };
+
+constexpr int kUTile = 2 * kSlab;  // U of one tile: 128 requests x 128 entries bf16, two boxes
 
 __host__ __device__ inline size_t align_up_t(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // RNN head: each A buffer holds the bf16 high halves of a_k, then the low halves.
-__host__ __device__ inline TCLayout tc_layout(int r, int na, int nstage, bool rnn) {
+__host__ __device__ inline TCLayout tc_layout(int r, int na, int nstage, bool rnn, int nu) {
   TCLayout L;
   L.nslab = (r + 63) / 64;
   L.aslabs = L.nslab * (rnn ? 2 : 1);
   L.na = na;
   L.nstage = nstage;
+  L.nu = nu;
   size_t off = 0;
   L.a = off;
   off += (size_t)na * L.aslabs * kSlab;
   L.ring = off;
   off += (size_t)nstage * kSlab;
+  L.ubuf = off;  // U tiles staged by TMA (two 16 KB swizzled boxes of 64 entries each)
+  off += (size_t)nu * kUTile;
   L.scratch = off;
   off = align_up_t(off + 3 * kM * sizeof(TSlot), 128);
   L.rnnbuf = off;  // RNN: e (r), s (r), Wj z (3r) of the request being updated
@@ -76,7 +83,7 @@ __host__ __device__ inline TCLayout tc_layout(int r, int na, int nstage, bool rn
   L.misc = off;
   off = align_up_t(off + sizeof(TMisc), 128);
   L.bars = off;
-  off += (size_t)(2 * nstage + 2 * kAcc + 2 * na + 2) * 8;
+  off += (size_t)(2 * nstage + 2 * kAcc + 2 * na + 2 + 2 * nu) * 8;
   L.total = align_up_t(off, 1024) + 1024;  // + slack to align the dynamic base to 1024
   return L;
 }
@@ -162,13 +169,13 @@ __device__ __forceinline__ int cond_token(const DraftParams& p, int b, int ks, b
   return ok ? x : 0;
 }
 
-template <bool RNN>
+template <bool RNN, bool TGT>
 __global__ void __launch_bounds__(kThreads, 1)
-    draft_tc_kernel(const DraftParams p, const __grid_constant__ CUtensorMap tmap_w2, int na,
-                    int nstage) {
+    draft_tc_kernel(const DraftParams p, const __grid_constant__ CUtensorMap tmap_w2,
+                    const __grid_constant__ CUtensorMap tmap_u, int na, int nstage, int nu) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const TCLayout Lay = tc_layout(p.r, na, nstage, RNN);
+  const TCLayout Lay = tc_layout(p.r, na, nstage, RNN, nu);
   float* r_e = (float*)(smem + Lay.rnnbuf);
   float* r_s = r_e + p.r;
   float* r_u = r_s + p.r;
@@ -184,13 +191,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* a_empty = a_full + na;
   uint64_t* tmem_done = a_empty + na;
   uint64_t* mma_done = tmem_done + 1;
+  uint64_t* u_full = mma_done + 1;   // [nu] a U tile has landed
+  uint64_t* u_empty = u_full + nu;   // [nu] every epilogue warp has read it
+  uint8_t* ubuf = smem + Lay.ubuf;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nCTA = gridDim.x, cta = blockIdx.x;
   const int B = p.B, G = p.gamma, V = p.V, r = p.r;
   const int nslab = Lay.nslab;
   const int nchunk = (B + kM - 1) / kM;
-  const bool tgt = p.target != nullptr;
+  constexpr bool tgt = TGT;  // a target is given (Eq 8): fixed per instantiation
   WsHeader* hdr = p.hdr;
 
   // vocab tiles of this block
@@ -215,6 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(tmem_done, kEpiWarps);
     mbar_init(mma_done, 1);
+    for (int i = 0; i < nu; ++i) {
+      mbar_init(&u_full[i], 1);
+      mbar_init(&u_empty[i], kEpiWarps);
+    }
     fence_mbar_init();
     ms->abort = 0;
   }
@@ -231,11 +245,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
-      int g = 0;
+      const uint64_t pol_u = policy_evict_first();  // U is read once
+      int g = 0, ui = 0;
       bool stop = false;
       for (int ks = 0; ks < G && !stop; ++ks)
         for (int c = 0; c < nchunk && !stop; ++c)
-          for (int t = 0; t < ntile && !stop; ++t)
+          for (int t = 0; t < ntile && !stop; ++t) {
+            if (nu > 0) {  // the tile's U (requests c*128.., position ks, 128 entries), ahead of use
+              const int us = ui % nu;
+              if (ui >= nu &&
+                  !wait_or_abort(&u_empty[us], (uint32_t)(((ui / nu) - 1) & 1), &ms->abort)) {
+                stop = true;
+                break;
+              }
+              mbar_expect_tx(&u_full[us], kUTile);
+              const int x = (t0 + t) * kNT;
+              tc::tma_load_3d(ubuf + (size_t)us * kUTile, &tmap_u, x, ks, c * kM, &u_full[us], pol_u);
+              tc::tma_load_3d(ubuf + (size_t)us * kUTile + kSlab, &tmap_u, x + 64, ks, c * kM,
+                              &u_full[us], pol_u);
+              ++ui;
+            }
             for (int s = 0; s < nslab; ++s, ++g) {
               const int slot = g % nstage;
               if (g >= nstage &&
@@ -247,9 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::tma_load_2d(ring + (size_t)slot * kSlab, &tmap_w2, s * 64, (t0 + t) * kNT,
                               &full[slot], pol);
             }
+          }
       if (stop) atomicMax(&hdr->status, kErrTimeout);
       for (int k = max(0, g - nstage); k < g; ++k)  // every copy must land before exit
         mbar_wait(&full[k % nstage], (uint32_t)((k / nstage) & 1));
+      for (int k = max(0, ui - nu); k < ui; ++k)
+        mbar_wait(&u_full[k % nu], (uint32_t)((k / nu) & 1));
     }
     return;
   }
@@ -327,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 16-byte vector loads of U (bf16) and the target need 16-byte aligned rows
   const bool vec_u = p.u_bf16 && (V % 8) == 0;
   const bool vec_t = (V % 4) == 0;
-  int acc_i = 0;
+  int acc_i = 0, ui = 0;
   bool failed = false;
 
   for (int ks = 0; ks < G && !failed; ++ks) {
@@ -410,87 +442,143 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < ntile; ++t, ++acc_i) {
         const int acc = acc_i % kAcc;
         const int vb = (t0 + t) * kNT + cq * 32;  // first vocab entry of this thread's 32
-        const bool whole = row_ok && vb + 32 <= V;
-        // U and target of this thread's 32 entries, in flight while the MMA finishes
-        uint4 uq[4];
-        if (whole && vec_u) {
-          const uint4* up = (const uint4*)((const __nv_bfloat16*)p.U + urow + vb);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) uq[i] = __ldcs(up + i);
+        // the tile's U: staged by TMA (row m; 16-byte chunk (cq % 2) * 4 + g of box cq / 2 sits at
+        // chunk position ^ (m % 8)), kept until the tile is done; else read from global
+        int us = -1;
+        if (nu > 0) {
+          us = ui % nu;
+          const bool oku = mbar_wait_warp(&u_full[us], (uint32_t)((ui / nu) & 1));
+          ++ui;
+          if (!oku) {
+            failed = true;
+            break;
+          }
         }
-        const bool ok = wait_or_abort(&acc_full[acc], (uint32_t)((acc_i / kAcc) & 1), &ms->abort);
-        if (!__all_sync(0xffffffffu, ok)) {
+        const uint8_t* ub = nu > 0 ? ubuf + (size_t)us * kUTile + (cq >> 1) * kSlab + m * 128 : nullptr;
+        const bool ok = mbar_wait_warp(&acc_full[acc], (uint32_t)((acc_i / kAcc) & 1));
+        if (!ok) {
           failed = true;
           break;
         }
         tc::fence_after_sync();
-        uint32_t bias[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + acc * kNT + cq * 32, bias);
-        tc::tmem_ld_wait();
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[acc]);
-        if (!row_ok || vb >= V) continue;
+        const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + acc * kNT + cq * 32;
+        // 4 groups of 8 entries, rolled to keep the code small: bias from TMEM, U, 2 Philox
+        // calls; the running max moves at most once per group
+#pragma unroll 1
+        for (int g8 = 0; g8 < 4; ++g8) {
+          uint32_t bias[8];
+          __syncwarp();
+          tc::tmem_ld8(tcol + 8 * g8, bias);  // the whole warp, every group
+          tc::tmem_ld_wait();
+          const int v = vb + 8 * g8;
+          if (!row_ok || v >= V) continue;  // (no further warp-collective work in this group)
+          const bool full = v + 8 <= V;  // all 8 entries exist (every group but the slice's last)
+          uint4 uq;
+          if (nu > 0) uq = *(const uint4*)(ub + (((((cq & 1) << 2) + g8) ^ (m & 7)) << 4));
+          else if (vec_u && full) uq = __ldcs((const uint4*)((const __nv_bfloat16*)p.U + urow + v));
+          const bool vq = nu > 0 || (vec_u && full);
+          float y[8], tv[8];
+          float gmax = -INFINITY, tmax = -INFINITY;
+          if (vq && full) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const int v = vb + j;
-          const U4 rq = philox4x32_10((uint32_t)(v >> 2), (uint32_t)ks, (uint32_t)b, kNoiseTag,
+            for (int e = 0; e < 8; ++e) {
+              const uint32_t wd = ((const uint32_t*)&uq)[e >> 1];
+              const float uval = __uint_as_float((e & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
+              y[e] = uval + __uint_as_float(bias[e]);  // z for now
+            }
+            if (TGT) {
+              if (vec_t) {
+                const float4 t0v = __ldcs((const float4*)(p.target + urow + v));
+                const float4 t1v = __ldcs((const float4*)(p.target + urow + v + 4));
+                tv[0] = t0v.x; tv[1] = t0v.y; tv[2] = t0v.z; tv[3] = t0v.w;
+                tv[4] = t1v.x; tv[5] = t1v.y; tv[6] = t1v.z; tv[7] = t1v.w;
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) tv[e] = p.target[urow + v + e];
+              }
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                tv[e] *= p.invT;
+                tmax = fmaxf(tmax, tv[e]);
+              }
+            }
+          } else {  // the slice's ragged end, or U rows without 16-byte alignment
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int vv = v + e;
+              float uval;
+              if (vq) {
+                const uint32_t wd = ((const uint32_t*)&uq)[e >> 1];
+                uval = __uint_as_float((e & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
+              } else {
+                uval = vv < V ? ld_u(p.U, urow + vv, p.u_bf16) : 0.f;
+              }
+              y[e] = vv < V ? uval + __uint_as_float(bias[e]) : -INFINITY;  // z for now
+              if (TGT) {
+                tv[e] = vv < V ? p.target[urow + vv] * p.invT : -INFINITY;
+                tmax = fmaxf(tmax, tv[e]);
+              }
+            }
+          }
+          if (p.logits)  // debug output: z
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (v + e < V) p.logits[urow + v + e] = y[e];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {  // y = z / T
+            y[e] *= p.invT;
+            gmax = fmaxf(gmax, y[e]);
+          }
+          if (gmax > st.m) {  // rescale the running sum to the new max, once per group
+            st.l *= __expf(st.m - gmax);
+            st.m = gmax;
+            C = __expf(st.m - st.best);
+          }
+          const U4 r0 = philox4x32_10((uint32_t)(v >> 2), (uint32_t)ks, (uint32_t)b, kNoiseTag,
                                       p.seed_lo, p.seed_hi);
-          const uint32_t words[4] = {rq.x, rq.y, rq.z, rq.w};
-          float yq[4];
-          float4 tq4 = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (tgt && whole && vec_t) tq4 = __ldcs((const float4*)(p.target + urow + v));
+          const U4 r1 = philox4x32_10((uint32_t)(v >> 2) + 1u, (uint32_t)ks, (uint32_t)b, kNoiseTag,
+                                      p.seed_lo, p.seed_hi);
+          const uint32_t words[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+          float ls[2] = {0.f, 0.f};  // two partial sums: a shorter dependency chain
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int vv = v + e;
-            float uval, tval = 0.f;
-            if (whole && vec_u) {
-              const uint32_t wd = ((const uint32_t*)&uq[(j + e) >> 3])[((j + e) & 7) >> 1];
-              uval = __uint_as_float(((j + e) & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
-            } else {
-              uval = vv < V ? ld_u(p.U, urow + vv, p.u_bf16) : 0.f;
-            }
-            if (tgt) {
-              if (whole && vec_t) tval = ((const float*)&tq4)[e];
-              else tval = vv < V ? p.target[urow + vv] : 0.f;
-            }
-            yq[e] = 0.f;
-            if (vv >= V) continue;
-            const float z = uval + __uint_as_float(bias[j + e]);
-            if (p.logits) p.logits[urow + vv] = z;
-            const float y = z * p.invT;
-            yq[e] = y;
-            float pe;
-            if (y > st.m) {
-              st.l = st.l * __expf(st.m - y) + 1.f;
-              st.m = y;
-              pe = 1.f;
-              C = __expf(st.m - st.best);
-            } else {
-              pe = __expf(y - st.m);
-              st.l += pe;
-            }
+          for (int e = 0; e < 8; ++e) {
+            const float pe = __expf(y[e] - st.m);
+            ls[e & 1] += pe;
             // exact skip: w = 1 - u; -ln u >= w, so w >= 1.001 exp(y - best) rules it out
             const float w = bits_to_uniform(~words[e]);
             if (!(w >= 1.001f * (pe * C))) {
-              const float sc = y + gumbel_from_uniform(bits_to_uniform(words[e]));
-              if (sc > st.best) {  // vv grows along this thread's sequence: ties keep the smaller
+              const float sc = y[e] + gumbel_from_uniform(bits_to_uniform(words[e]));
+              if (sc > st.best) {  // entries grow along this thread's sequence: ties keep the smaller
                 st.best = sc;
-                st.tok = (uint32_t)vv;
+                st.tok = (uint32_t)(v + e);
                 C = __expf(st.m - st.best);
               }
             }
-            if (tgt) lse_push(st.mt, st.lt, tval * p.invT);
           }
-          if (tgt) {
-            if (whole && vec_t) {
-              *(float4*)(p.ybuf + (size_t)b * V + v) = make_float4(yq[0], yq[1], yq[2], yq[3]);
+          st.l += ls[0] + ls[1];
+          if (TGT) {
+            if (tmax > st.mt) {
+              st.lt *= __expf(st.mt - tmax);
+              st.mt = tmax;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) st.lt += __expf(tv[e] - st.mt);
+            float* yo = p.ybuf + (size_t)b * V + v;
+            if (vec_t && v + 8 <= V) {
+              *(float4*)yo = make_float4(y[0], y[1], y[2], y[3]);
+              *(float4*)(yo + 4) = make_float4(y[4], y[5], y[6], y[7]);
             } else {
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (v + e < V) p.ybuf[(size_t)b * V + v + e] = yq[e];
+              for (int e = 0; e < 8; ++e)
+                if (v + e < V) yo[e] = y[e];
             }
           }
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&acc_empty[acc]);
+          if (nu > 0) mbar_arrive(&u_empty[us]);
         }
       }
       if (esync_or<kEpiThreads>(failed)) {
@@ -658,30 +746,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 int draft_tc_supported(int B, int r, int w_bf16) { return w_bf16 && B >= 1 && r % 8 == 0 && r <= 512; }
 
 bool draft_tc_configure(DraftParams& p, size_t smem_optin) {
-  // two A buffers when they fit next to at least 4 ring stages, else one
-  for (int na = 2; na >= 1; --na) {
-    for (int ns = 8; ns >= 3; --ns) {
-      const TCLayout L = tc_layout(p.r, na, ns, p.head == 1);
-      if (L.total <= smem_optin) {
-        p.tc_na = na;
-        p.nstages = ns;
-        p.smem_bytes = L.total;
-        return true;
+  // U tiles are staged by TMA when U is bf16 with 16-byte aligned rows; prefer two of them, then
+  // two A buffers, then the deepest W2 ring (at least 3 stages) that fits
+  const int nu_max = p.u_bf16 && p.V % 8 == 0 ? 2 : 0;
+  for (int nu = nu_max; nu >= 0; --nu)
+    for (int na = 2; na >= 1; --na)
+      for (int ns = 8; ns >= 3; --ns) {
+        const TCLayout L = tc_layout(p.r, na, ns, p.head == 1, nu);
+        if (L.total <= smem_optin) {
+          p.tc_na = na;
+          p.tc_nu = nu;
+          p.nstages = ns;
+          p.smem_bytes = L.total;
+          return true;
+        }
       }
-    }
-  }
   return false;
 }
 
 cudaError_t launch_draft_tc(DraftParams& p, int nblocks, cudaStream_t stream) {
   CUtensorMap tmap;
   if (!encode_bf16_2d(&tmap, p.W2, p.V, p.r, p.r, kNT)) return cudaErrorInvalidValue;
-  const void* kern = p.head == 1 ? (const void*)draft_tc_kernel<true> : (const void*)draft_tc_kernel<false>;
+  const bool tg = p.target != nullptr;
+  const void* kern = p.head == 1 ? (tg ? (const void*)draft_tc_kernel<true, true>
+                                       : (const void*)draft_tc_kernel<true, false>)
+                                 : (tg ? (const void*)draft_tc_kernel<false, true>
+                                       : (const void*)draft_tc_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)p.smem_bytes);
   if (e != cudaSuccess) return e;
-  int na = p.tc_na, ns = p.nstages;
-  void* args[] = {(void*)&p, (void*)&tmap, (void*)&na, (void*)&ns};
+  CUtensorMap tmap_u;
+  std::memset(&tmap_u, 0, sizeof tmap_u);
+  if (p.tc_nu > 0 && !encode_u_bf16_3d(&tmap_u, p.U, p.B, p.gamma, p.V)) return cudaErrorInvalidValue;
+  int na = p.tc_na, ns = p.nstages, nu = p.tc_nu;
+  void* args[] = {(void*)&p, (void*)&tmap, (void*)&tmap_u, (void*)&na, (void*)&ns, (void*)&nu};
   return cudaLaunchCooperativeKernel(kern, dim3(nblocks), dim3(kThreads), args, p.smem_bytes, stream);
 }
 
