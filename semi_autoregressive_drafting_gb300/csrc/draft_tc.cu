@@ -115,11 +115,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return true;
 }
 
-__device__ __forceinline__ float ld_acquire_f32(const float* p) {
-  float v;
-  asm volatile("ld.acquire.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
-  return v;
-}
 
 __device__ __forceinline__ float ld_u(const void* p, size_t i, int bf16) {
   return bf16 ? __bfloat162float(((const __nv_bfloat16*)p)[i]) : ((const float*)p)[i];
@@ -402,15 +397,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             *(uint4*)(dst + (j >> 3) * kSlab + (((j & 7) ^ (gm & 7)) << 4)) = val;
           }
         } else {
+          // the flag is read with acquire semantics by this thread, so plain loads of the a_k
+          // it publishes see the owner's stores
           if (b < B) gok = wait_flag(&p.rnn_flag[(size_t)ks * B + b], (unsigned)(ks + 1));
           const float* src = p.rnn_a + ((size_t)ks * B + b) * r;
           for (int j = gh; j < nslab * 8; j += 4) {
             uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
             if (gok && valid && j < nchk) {
+              float av[8];
+              *(float4*)&av[0] = *(const float4*)(src + 8 * j);
+              *(float4*)&av[4] = *(const float4*)(src + 8 * j + 4);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const float a0 = ld_acquire_f32(src + 8 * j + 2 * e);
-                const float a1 = ld_acquire_f32(src + 8 * j + 2 * e + 1);
+                const float a0 = av[2 * e];
+                const float a1 = av[2 * e + 1];
                 const __nv_bfloat16 h0 = __float2bfloat16_rn(a0), h1 = __float2bfloat16_rn(a1);
                 const __nv_bfloat16 l0 = __float2bfloat16_rn(a0 - __bfloat162float(h0));
                 const __nv_bfloat16 l1 = __float2bfloat16_rn(a1 - __bfloat162float(h1));
@@ -638,12 +638,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ew == (b % kEpiWarps)) {
           const float2 a = merge_ml(p.ml + ((size_t)ks * B + b) * nCTA, nCTA, lane);
           const float2 tt = merge_ml(p.mlt + ((size_t)ks * B + b) * nCTA, nCTA, lane);
-          float acc = 0.f;
           const float Ld = a.x + logf(a.y), Lt = tt.x + logf(tt.y);
-          const size_t trow = ((size_t)b * G + ks) * V;
-          for (int v = sl0 + lane; v < sl1; v += 32)
-            acc += fabsf(__expf(p.ybuf[(size_t)b * V + v] - Ld) - __expf(p.target[trow + v] * p.invT - Lt));
-          acc = warp_sum(acc);
+          const float* yr = p.ybuf + (size_t)b * V;
+          const float* tr = p.target + ((size_t)b * G + ks) * V;
+          float acc = 0.f, acc2 = 0.f;
+          int vt = sl0;  // first entry left for the scalar tail
+          if (vec_t) {   // 16-byte loads (sl0 is a multiple of 128), several in flight per lane
+            const int n4 = (sl1 - sl0) >> 2;
+#pragma unroll 4
+            for (int i = lane; i < n4; i += 32) {
+              const float4 yv = __ldcs((const float4*)(yr + sl0) + i);
+              const float4 tv = __ldcs((const float4*)(tr + sl0) + i);
+              acc += fabsf(__expf(yv.x - Ld) - __expf(tv.x * p.invT - Lt)) +
+                     fabsf(__expf(yv.y - Ld) - __expf(tv.y * p.invT - Lt));
+              acc2 += fabsf(__expf(yv.z - Ld) - __expf(tv.z * p.invT - Lt)) +
+                      fabsf(__expf(yv.w - Ld) - __expf(tv.w * p.invT - Lt));
+            }
+            vt = sl0 + 4 * n4;
+          }
+          for (int v = vt + lane; v < sl1; v += 32)
+            acc += fabsf(__expf(yr[v] - Ld) - __expf(tr[v] * p.invT - Lt));
+          acc = warp_sum(acc + acc2);
           if (lane == 0) p.l1p[((size_t)ks * B + b) * nCTA + cta] = acc;
         }
       }

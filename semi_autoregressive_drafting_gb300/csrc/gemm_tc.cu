@@ -110,8 +110,18 @@ __global__ void __launch_bounds__(kGThreads, 1)
       tc::tmem_ld_wait();
       if (m >= a.M) continue;
       const int n = n0 + g * 32;
-      for (int j = 0; j < 32; ++j)
-        if (n + j < a.N) out[n + j] = (ok && ns > 0) ? __uint_as_float(v[j]) : 0.f;
+      const bool live = ok && ns > 0;
+      if (n + 32 <= a.N && (a.N & 3) == 0) {  // 16-byte stores of this row's 32 columns
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *(float4*)(out + n + j) =
+              live ? make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                 __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        for (int j = 0; j < 32; ++j)
+          if (n + j < a.N) out[n + j] = live ? __uint_as_float(v[j]) : 0.f;
+      }
     }
     tc::fence_before_sync();
   }
