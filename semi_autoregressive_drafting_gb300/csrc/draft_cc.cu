@@ -36,7 +36,7 @@
 namespace dspark {
 namespace {
 
-constexpr int kMaxCW = 16;  // most consumer warps of any variant
+constexpr int kMaxCW = 24;  // most consumer warps of any variant
 
 struct Slot {  // running state of one (request, vocab subset)
   float best;
@@ -1315,7 +1315,9 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
 
 template <typename WT, int NB, int NCV, bool TCV>
 cudaError_t launch_k(DraftParams& p, const CUtensorMap& tm, int nblocks, cudaStream_t stream) {
-  constexpr int CW = NB <= 2 ? 16 : 8;
+  // consumer warps: 24 for one request on the CUDA cores (the stage loop is latency-bound and
+  // the variant fits 80 registers), 16 for two, 8 for four
+  constexpr int CW = (NB <= 1 && !TCV) ? 24 : NB <= 2 ? 16 : 8;
   constexpr int kThreads = CW * 32 + 32 + (TCV ? 32 : 0);
   auto kern = p.head == 1 ? draft_cc_kernel<WT, NB, NCV, CW, true, TCV>
                           : draft_cc_kernel<WT, NB, NCV, CW, false, TCV>;
