@@ -956,6 +956,8 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
       }
       tc::fence_before_sync();  // the accumulators are read: the next step may overwrite them
     }
+    float bb = 0.f;       // NB == 1: the row sum this lane holds for the batched epilogue
+    int vlb = -1, nb = 0;  // its slice entry (-1: none) and the stages batched so far
     // Four warps share each stage: warp q of a group takes rows [q R/4, (q+1) R/4) in
     // sub-groups of SR rows, so a slot is handed back a quarter of a stage's work after its
     // bytes land.  Stages go round-robin to the groups.
@@ -1003,8 +1005,24 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
             for (int b = 0; b < NB; ++b) part[j * NB + b] = DT::run(q, ereg[b][0], part[j * NB + b]);
           }
           const float bias = transpose_reduce<8>(part, lane);
-          const int row = rq0 + sg * SR + jrow;
-          if (owner && bq < B && row < rq1) epilogue(s * R + row, bias);
+          if (NB == 1) {
+            // one request: gather the 8 row sums of this stage into lanes 8 nb .. 8 nb + 7 and
+            // run the epilogue once per 4 stages, on all 32 lanes (rows still reach each lane
+            // in increasing v)
+            const float mine = __shfl_sync(0xffffffffu, bias, (lane & 7) << 2);
+            if ((lane >> 3) == nb) {
+              bb = mine;
+              vlb = rq0 + (lane & 7) < rq1 ? s * R + rq0 + (lane & 7) : -1;
+            }
+            if (++nb == 4) {
+              if (vlb >= 0) epilogue(vlb, bb);
+              vlb = -1;
+              nb = 0;
+            }
+          } else {
+            const int row = rq0 + sg * SR + jrow;
+            if (owner && bq < B && row < rq1) epilogue(s * R + row, bias);
+          }
         }
         continue;
       }
@@ -1045,6 +1063,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
         if (owner && bq < B && row < rq1) epilogue(s * R + row, bias);
       }
     }
+    if (NB == 1 && nb > 0 && vlb >= 0) epilogue(vlb, bb);  // a partial batch of stages
     if (csync_or<kCThreads>(wfail)) {
       failed = true;
       break;
@@ -1081,8 +1100,10 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
       }
     } else {
       unsigned long long key = st.tok != 0xFFFFFFFFu ? tagged_key(st.best, st.tok, ks) : 0ull;
+      // lanes of the same request: those 4 NB apart hold the owner results; with one request
+      // the batched epilogue leaves results on every lane, so all 32 are merged
 #pragma unroll
-      for (int o = 4 * NB; o < 32; o <<= 1) {
+      for (int o = NB == 1 ? 1 : 4 * NB; o < 32; o <<= 1) {
         const unsigned long long q = __shfl_xor_sync(0xffffffffu, key, o);
         key = q > key ? q : key;
         lse_merge(st.m, st.l, __shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.l, o));
