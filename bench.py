@@ -269,25 +269,46 @@ def main():
     h2d = sum(v.numel() * v.element_size() for v in hin.values())
     d2h = res_tok.numel() * 4 + sum(v.numel() * 4 for v in res.values())
     e2e_steps = min(args.steps, 200)
-    for _ in range(3):
+
+    def e2e_step(s):
         for k in names:
             din[k].copy_(hin[k], non_blocking=True)
+        staged.run(s)
+        res_tok.copy_(o.tokens, non_blocking=True)
+        for k, v in outs.items():
+            res[k].copy_(v, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step(stream)
     torch.cuda.synchronize()
+    # the step (input copies, the draft call, result copies) is captured once in a CUDA graph
+    # and replayed: one launch per step, so the host's issue time does not stretch the step
+    graph = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            e2e_step(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+    except RuntimeError:
+        graph = None
+        torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
     for i in range(e2e_steps):
         flush.zero_()
         e0.record(stream)
-        for k in names:
-            din[k].copy_(hin[k], non_blocking=True)
-        staged.run()
-        res_tok.copy_(o.tokens, non_blocking=True)
-        for k, v in outs.items():
-            res[k].copy_(v, non_blocking=True)
+        if graph is not None:
+            graph.replay()
+        else:
+            e2e_step(stream)
         e1.record(stream)
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
     e2e_ms /= e2e_steps
+    res_ok = bool((res_tok >= 0).all()) and torch.equal(res_tok.cuda(), o.tokens)
     assert ws.status() == 0, "draft kernel reported a device error (end-to-end loop)"
 
     # ---- max over ranks
@@ -324,7 +345,8 @@ def main():
                          "algorithmic_bytes_per_launch": alg,
                          "kernel": "draft_tc_kernel" if path == 1 else "draft_cc_kernel"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "cuda_graph": graph is not None, "results_copied": res_ok},
             "gpu_launches": launches * args.steps,
             "clocks": clk.summary(),
             "wall_s": wall,

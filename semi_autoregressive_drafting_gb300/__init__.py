@@ -137,8 +137,11 @@ class DraftPlan:
         self.workspace = workspace
         self.out = DraftOutput(tokens, lse, c, S, cstar, l1, logits, s_out)
 
-    def run(self) -> DraftOutput:
-        code = self._fn(*self._args)
+    def run(self, stream=None) -> DraftOutput:
+        """Enqueue the call; ``stream`` (a torch stream) overrides the one given at
+        construction, e.g. the capturing stream of a CUDA graph."""
+        args = self._args if stream is None else self._args[:-1] + (_stream(stream),)
+        code = self._fn(*args)
         if code != 0:
             _lib.check(code, self._where)
         return self.out

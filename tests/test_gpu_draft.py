@@ -150,3 +150,28 @@ def test_repeat_runs_are_bit_identical():
     for o in runs[1:]:
         for f in ("tokens", "lse", "c", "S", "cstar", "l1"):
             assert torch.equal(getattr(o, f), getattr(runs[0], f)), f
+
+
+@pytest.mark.parametrize("name,code", SMALL_PATHS)
+def test_draft_captured_in_cuda_graph(monkeypatch, name, code):
+    # the call is stream-ordered and capturable: a graph replay gives the direct call's results
+    wl = inputs.WORKLOADS["qwen3_4b_markov"].with_(V=20008, d=256, B=2, seed=90)
+    _use_path(monkeypatch, name, code, wl)
+    t = parity.to_dev(inputs.generate(wl))
+    plan = ds.DraftPlan(0, t["W1"], t["W2"], t["U"], t["x0"], T=wl.T, seed=wl.seed, h=t["h"],
+                        w=t["w"], Wj=None, target=None, forced=None, s0=None, want_logits=False,
+                        workspace=None, stream=None)
+    ref = plan.run()
+    ref = {k: getattr(ref, k).clone() for k in ("tokens", "lse", "c", "S")}
+    torch.cuda.synchronize()
+    for k in ref:
+        getattr(plan.out, k).zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        plan.run(torch.cuda.current_stream())
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert plan.workspace.status() == 0
+    for k, v in ref.items():
+        assert torch.equal(getattr(plan.out, k), v), k
