@@ -61,6 +61,7 @@ struct DraftParams {
   int u_bulk;          // 1: U/target rows are 16-byte aligned and copied with TMA bulk copies
   int tc_na;           // tensor-core path: A-operand buffers
   int tc_nu;           // tensor-core path: U tiles staged in shared memory (0 = direct loads)
+  int tc_pk;           // tensor-core path: at most 64 requests, vocabulary tiles in pairs
   size_t smem_bytes;
 };
 
@@ -76,9 +77,9 @@ int draft_tc_supported(int B, int r, int w_bf16);
 // 2-D tensor map of a row-major bf16 matrix [rows][cols] (row stride ld elements) for TMA tile
 // loads of box_rows rows x 64 columns into the 128-byte-swizzled K-major layout.
 bool encode_bf16_2d(CUtensorMap* m, const void* base, int rows, int cols, int ld, int box_rows);
-// 3-D tensor map of U [B][G][V] bf16 for TMA loads of 128 requests x one position x 64
+// 3-D tensor map of U [B][G][V] bf16 for TMA loads of box_rows requests x one position x 64
 // vocabulary entries, 128-byte swizzle (V a multiple of 8).
-bool encode_u_bf16_3d(CUtensorMap* m, const void* U, int B, int G, int V);
+bool encode_u_bf16_3d(CUtensorMap* m, const void* U, int B, int G, int V, int box_rows);
 cudaError_t launch_gemm_tc(const void* A, int lda, const void* Bm, int ldb, int M, int N, int K,
                            float* part, int max_split, int nsm, int* ksplit_out, unsigned* status,
                            cudaStream_t stream);

@@ -55,6 +55,7 @@ struct TMisc {
 struct TCLayout {
   size_t a, ring, ubuf, scratch, rnnbuf, misc, bars, total;
   int nslab, na, nstage, aslabs, nu;
+  int abytes;  // bytes of one A slab: 128 rows, or 192 when two vocabulary tiles share a tile
 };
 
 constexpr int kUTile = 2 * kSlab;  // U of one tile: 128 requests x 128 entries bf16, two boxes
@@ -62,22 +63,27 @@ constexpr int kUTile = 2 * kSlab;  // U of one tile: 128 requests x 128 entries 
 __host__ __device__ inline size_t align_up_t(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // RNN head: each A buffer holds the bf16 high halves of a_k, then the low halves.
-__host__ __device__ inline TCLayout tc_layout(int r, int na, int nstage, bool rnn, int nu) {
+// Packed mode (one chunk of at most 64 requests): each A slab holds 192 rows, [0; e; 0], so
+// that rows 64..191 ([e; 0]) and rows 0..127 ([0; e]) are the A operands of two MMAs that put
+// vocabulary tile t in TMEM lanes 0-63 and tile t + 1 in lanes 64-127 of one accumulator.
+__host__ __device__ inline TCLayout tc_layout(int r, int na, int nstage, bool rnn, int nu,
+                                              bool packed) {
   TCLayout L;
   L.nslab = (r + 63) / 64;
   L.aslabs = L.nslab * (rnn ? 2 : 1);
   L.na = na;
   L.nstage = nstage;
   L.nu = nu;
+  L.abytes = packed ? kSlab * 3 / 2 : kSlab;
   size_t off = 0;
   L.a = off;
-  off += (size_t)na * L.aslabs * kSlab;
+  off += (size_t)na * L.aslabs * L.abytes;
   L.ring = off;
   off += (size_t)nstage * kSlab;
   L.ubuf = off;  // U tiles staged by TMA (two 16 KB swizzled boxes of 64 entries each)
   off += (size_t)nu * kUTile;
   L.scratch = off;
-  off = align_up_t(off + 3 * kM * sizeof(TSlot), 128);
+  off = align_up_t(off + 4 * kM * sizeof(TSlot), 128);  // partial states of the merge
   L.rnnbuf = off;  // RNN: e (r), s (r), Wj z (3r) of the request being updated
   off = align_up_t(off + (rnn ? (size_t)5 * r * 4 : 0), 128);
   L.misc = off;
@@ -170,7 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmap_u, int na, int nstage, int nu) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const TCLayout Lay = tc_layout(p.r, na, nstage, RNN, nu);
+  const bool pk = p.tc_pk != 0;  // packed: one chunk of at most 64 requests, tiles in pairs
+  const TCLayout Lay = tc_layout(p.r, na, nstage, RNN, nu, pk);
+  const int ab_bytes = Lay.abytes;
   float* r_e = (float*)(smem + Lay.rnnbuf);
   float* r_s = r_e + p.r;
   float* r_u = r_s + p.r;
@@ -203,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t0 = (int)(((long long)ntile_all * cta) / nCTA);
   const int t1 = (int)(((long long)ntile_all * (cta + 1)) / nCTA);
   const int ntile = t1 - t0;
+  const int nround = pk ? (ntile + 1) / 2 : ntile;  // accumulator rounds per chunk
   const int sl0 = t0 * kNT, sl1 = min(V, t1 * kNT);  // vocab slice [sl0, sl1)
 
   if (tid == 0) {
@@ -246,18 +255,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = 0; ks < G && !stop; ++ks)
         for (int c = 0; c < nchunk && !stop; ++c)
           for (int t = 0; t < ntile && !stop; ++t) {
-            if (nu > 0) {  // the tile's U (requests c*128.., position ks, 128 entries), ahead of use
+            // U of the round that starts with tile t (packed: tiles t and t + 1, 64 rows each,
+            // into rows 0-63 and 64-127 of the two 64-entry boxes), ahead of use
+            if (nu > 0 && (!pk || (t & 1) == 0)) {
               const int us = ui % nu;
               if (ui >= nu &&
                   !wait_or_abort(&u_empty[us], (uint32_t)(((ui / nu) - 1) & 1), &ms->abort)) {
                 stop = true;
                 break;
               }
-              mbar_expect_tx(&u_full[us], kUTile);
+              uint8_t* dst = ubuf + (size_t)us * kUTile;
               const int x = (t0 + t) * kNT;
-              tc::tma_load_3d(ubuf + (size_t)us * kUTile, &tmap_u, x, ks, c * kM, &u_full[us], pol_u);
-              tc::tma_load_3d(ubuf + (size_t)us * kUTile + kSlab, &tmap_u, x + 64, ks, c * kM,
-                              &u_full[us], pol_u);
+              if (!pk) {
+                mbar_expect_tx(&u_full[us], kUTile);
+                tc::tma_load_3d(dst, &tmap_u, x, ks, c * kM, &u_full[us], pol_u);
+                tc::tma_load_3d(dst + kSlab, &tmap_u, x + 64, ks, c * kM, &u_full[us], pol_u);
+              } else {
+                const bool two = t + 1 < ntile;
+                mbar_expect_tx(&u_full[us], two ? kUTile : kUTile / 2);
+                tc::tma_load_3d(dst, &tmap_u, x, ks, 0, &u_full[us], pol_u);
+                tc::tma_load_3d(dst + kSlab, &tmap_u, x + 64, ks, 0, &u_full[us], pol_u);
+                if (two) {
+                  tc::tma_load_3d(dst + kSlab / 2, &tmap_u, x + kNT, ks, 0, &u_full[us], pol_u);
+                  tc::tma_load_3d(dst + kSlab + kSlab / 2, &tmap_u, x + kNT + 64, ks, 0,
+                                  &u_full[us], pol_u);
+                }
+              }
               ++ui;
             }
             for (int s = 0; s < nslab; ++s, ++g) {
@@ -295,8 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc::fence_after_sync();
-          const uint32_t a_base = smem_u32(abuf + (size_t)ab * Lay.aslabs * kSlab);
-          for (int t = 0; t < ntile && !stop; ++t, ++acc_i) {
+          const uint32_t a_base = smem_u32(abuf + (size_t)ab * Lay.aslabs * ab_bytes);
+          for (int rd = 0; rd < nround && !stop; ++rd, ++acc_i) {
             const int acc = acc_i % kAcc;
             if (acc_i >= kAcc &&
                 !wait_or_abort(&acc_empty[acc], (uint32_t)(((acc_i / kAcc) - 1) & 1), &ms->abort)) {
@@ -304,26 +327,33 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc::fence_after_sync();
-            for (int s = 0; s < nslab; ++s, ++g) {
-              const int slot = g % nstage;
-              if (!wait_or_abort(&full[slot], (uint32_t)((g / nstage) & 1), &ms->abort)) {
-                stop = true;
-                break;
-              }
-              tc::fence_after_sync();
-              const uint32_t b_base = smem_u32(ring + (size_t)slot * kSlab);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                tc::mma_bf16(tmem + acc * kNT, tc::sdesc_sw128(a_base + s * kSlab + kk * 32),
-                             tc::sdesc_sw128(b_base + kk * 32), idesc, (s | kk) != 0);
-              if (RNN) {  // a_k = hi + lo: the low halves against the same W2 slab
+            // packed: tile 2 rd against A rows 64..191 ([e; 0]), tile 2 rd + 1 against rows
+            // 0..127 ([0; e]); otherwise tile rd against the 128 rows
+            const int nt_rd = pk ? min(2, ntile - 2 * rd) : 1;
+            for (int h = 0; h < nt_rd && !stop; ++h) {
+              const uint32_t a_row = pk ? (h == 0 ? 64u * 128u : 0u) : 0u;
+              for (int s = 0; s < nslab; ++s, ++g) {
+                const int slot = g % nstage;
+                if (!wait_or_abort(&full[slot], (uint32_t)((g / nstage) & 1), &ms->abort)) {
+                  stop = true;
+                  break;
+                }
+                tc::fence_after_sync();
+                const uint32_t b_base = smem_u32(ring + (size_t)slot * kSlab);
+                const uint32_t a_s = a_base + s * ab_bytes + a_row;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                  tc::mma_bf16(tmem + acc * kNT,
-                               tc::sdesc_sw128(a_base + (nslab + s) * kSlab + kk * 32),
-                               tc::sdesc_sw128(b_base + kk * 32), idesc, 1u);
+                  tc::mma_bf16(tmem + acc * kNT, tc::sdesc_sw128(a_s + kk * 32),
+                               tc::sdesc_sw128(b_base + kk * 32), idesc, (h | s | kk) != 0);
+                if (RNN) {  // a_k = hi + lo: the low halves against the same W2 slab
+                  const uint32_t a_lo = a_s + nslab * ab_bytes;
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_bf16(tmem + acc * kNT, tc::sdesc_sw128(a_lo + kk * 32),
+                                 tc::sdesc_sw128(b_base + kk * 32), idesc, 1u);
+                }
+                tc::mma_commit(&empty[slot]);
               }
-              tc::mma_commit(&empty[slot]);
             }
             if (!stop) tc::mma_commit(&acc_full[acc]);
           }
@@ -348,14 +378,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ew = warp - 4;           // 0..15
   const int q = warp & 3;            // TMEM lane quarter
   const int cq = ew >> 2;            // 32-column quarter of each tile
-  const int m = 32 * q + lane;       // request within a chunk (TMEM lane)
-  const int gm = et & (kM - 1), gh = et >> 7;  // gather role: row, quarter of the row's chunks
+  const int lrow = 32 * q + lane;    // this thread's TMEM lane (accumulator row)
+  // request within the chunk: the lane, or in packed mode lane mod 64 (lanes 64-127 hold the
+  // same requests for the round's second vocabulary tile)
+  const int m = pk ? (lrow & 63) : lrow;
+  const int half = pk ? (q >> 1) : 0;  // packed: which tile of the round
+  // gather role: row and the share of the row's 16-byte chunks (packed: 64 rows, 8 shares)
+  const int gm = pk ? (et & 63) : (et & (kM - 1)), gh = pk ? (et >> 6) : (et >> 7);
+  const int gstep = pk ? 8 : 4;
   const int nchk = r / 8;            // 16-byte chunks of a W1 row
   // 16-byte vector loads of U (bf16) and the target need 16-byte aligned rows
   const bool vec_u = p.u_bf16 && (V % 8) == 0;
   const bool vec_t = (V % 4) == 0;
   int acc_i = 0, ui = 0;
   bool failed = false;
+  if (pk) {  // rows 0-63 and 128-191 of every A slab stay zero
+    for (size_t i = et; i < (size_t)na * Lay.aslabs * ab_bytes / 16; i += kEpiThreads) {
+      const int row = (int)((i * 16 % ab_bytes) / 128);
+      if (row < 64 || row >= 128) ((uint4*)abuf)[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
 
   for (int ks = 0; ks < G && !failed; ++ks) {
     if (RNN) {
@@ -389,19 +431,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = c * kM + gm;
         bool valid = false;
         const int x = b < B ? cond_token(p, b, ks, &valid) : 0;
-        uint8_t* dst = abuf + (size_t)ab * Lay.aslabs * kSlab + (gm >> 3) * 1024 + (gm & 7) * 128;
+        const int arow = pk ? 64 + gm : gm;  // packed: the e rows are rows 64..127
+        uint8_t* dst = abuf + (size_t)ab * Lay.aslabs * ab_bytes + (arow >> 3) * 1024 + (arow & 7) * 128;
         if (!RNN) {
           const uint4* src = (const uint4*)((const __nv_bfloat16*)p.W1 + (size_t)x * r);
-          for (int j = gh; j < nslab * 8; j += 4) {
+          for (int j = gh; j < nslab * 8; j += gstep) {
             const uint4 val = (valid && j < nchk) ? src[j] : make_uint4(0, 0, 0, 0);
-            *(uint4*)(dst + (j >> 3) * kSlab + (((j & 7) ^ (gm & 7)) << 4)) = val;
+            *(uint4*)(dst + (j >> 3) * ab_bytes + (((j & 7) ^ (arow & 7)) << 4)) = val;
           }
         } else {
           // the flag is read with acquire semantics by this thread, so plain loads of the a_k
           // it publishes see the owner's stores
           if (b < B) gok = wait_flag(&p.rnn_flag[(size_t)ks * B + b], (unsigned)(ks + 1));
           const float* src = p.rnn_a + ((size_t)ks * B + b) * r;
-          for (int j = gh; j < nslab * 8; j += 4) {
+          for (int j = gh; j < nslab * 8; j += gstep) {
             uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
             if (gok && valid && j < nchk) {
               float av[8];
@@ -418,9 +461,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lo[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
               }
             }
-            const int off = (j >> 3) * kSlab + (((j & 7) ^ (gm & 7)) << 4);
+            const int off = (j >> 3) * ab_bytes + (((j & 7) ^ (arow & 7)) << 4);
             *(uint4*)(dst + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *(uint4*)(dst + nslab * kSlab + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *(uint4*)(dst + nslab * ab_bytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
         }
       }
@@ -439,8 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       TSlot st;
       tslot_init(st);
       float C = INFINITY;  // exp(m - best) of this thread's running state
-      for (int t = 0; t < ntile; ++t, ++acc_i) {
+      for (int rd = 0; rd < nround; ++rd, ++acc_i) {
         const int acc = acc_i % kAcc;
+        const int t = pk ? 2 * rd + half : rd;  // this warp's vocabulary tile of the round
+        const bool tile_ok = t < ntile;          // (packed, odd count: the last round has one)
         const int vb = (t0 + t) * kNT + cq * 32;  // first vocab entry of this thread's 32
         // the tile's U: staged by TMA (row m; 16-byte chunk (cq % 2) * 4 + g of box cq / 2 sits at
         // chunk position ^ (m % 8)), kept until the tile is done; else read from global
@@ -454,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
         }
-        const uint8_t* ub = nu > 0 ? ubuf + (size_t)us * kUTile + (cq >> 1) * kSlab + m * 128 : nullptr;
+        const uint8_t* ub = nu > 0 ? ubuf + (size_t)us * kUTile + (cq >> 1) * kSlab + lrow * 128 : nullptr;
         const bool ok = mbar_wait_warp(&acc_full[acc], (uint32_t)((acc_i / kAcc) & 1));
         if (!ok) {
           failed = true;
@@ -462,53 +507,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_after_sync();
         const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + acc * kNT + cq * 32;
-        // 4 groups of 8 entries, rolled to keep the code small: bias from TMEM, U, 2 Philox
-        // calls; the running max moves at most once per group
+        // groups of GE entries, rolled to keep the code small: bias from TMEM, U, GE / 4
+        // independent Philox calls; the running max moves at most once per group.  (16-entry
+        // groups measured slower on GB300: 3.32 against 2.97 ms per block at B = 512.)
+        constexpr int GE = 8;
 #pragma unroll 1
-        for (int g8 = 0; g8 < 4; ++g8) {
-          uint32_t bias[8];
+        for (int gi = 0; gi < 32 / GE; ++gi) {
+          uint32_t bias[GE];
           __syncwarp();
-          tc::tmem_ld8(tcol + 8 * g8, bias);  // the whole warp, every group
+#pragma unroll
+          for (int h8 = 0; h8 < GE / 8; ++h8)  // the whole warp, every group
+            tc::tmem_ld8(tcol + GE * gi + 8 * h8, *(uint32_t(*)[8])&bias[8 * h8]);
           tc::tmem_ld_wait();
-          const int v = vb + 8 * g8;
-          if (!row_ok || v >= V) continue;  // (no further warp-collective work in this group)
-          const bool full = v + 8 <= V;  // all 8 entries exist (every group but the slice's last)
-          uint4 uq;
-          if (nu > 0) uq = *(const uint4*)(ub + (((((cq & 1) << 2) + g8) ^ (m & 7)) << 4));
-          else if (vec_u && full) uq = __ldcs((const uint4*)((const __nv_bfloat16*)p.U + urow + v));
+          const int v = vb + GE * gi;
+          if (!row_ok || !tile_ok || v >= V) continue;  // (no further warp-collective work)
+          const bool full = v + GE <= V;  // every entry exists (all groups but the slice's last)
+          uint4 uq[GE / 8];
+#pragma unroll
+          for (int h8 = 0; h8 < GE / 8; ++h8) {
+            const int c8 = GE / 8 * gi + h8;  // 16-byte chunk of this thread's 32 entries
+            if (nu > 0) uq[h8] = *(const uint4*)(ub + (((((cq & 1) << 2) + c8) ^ (lrow & 7)) << 4));
+            else if (vec_u && full)
+              uq[h8] = __ldcs((const uint4*)((const __nv_bfloat16*)p.U + urow + v + 8 * h8));
+          }
           const bool vq = nu > 0 || (vec_u && full);
-          float y[8], tv[8];
+          float y[GE], tv[GE];
           float gmax = -INFINITY, tmax = -INFINITY;
           if (vq && full) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const uint32_t wd = ((const uint32_t*)&uq)[e >> 1];
+            for (int e = 0; e < GE; ++e) {
+              const uint32_t wd = ((const uint32_t*)&uq[e >> 3])[(e & 7) >> 1];
               const float uval = __uint_as_float((e & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
               y[e] = uval + __uint_as_float(bias[e]);  // z for now
             }
             if (TGT) {
               if (vec_t) {
-                const float4 t0v = __ldcs((const float4*)(p.target + urow + v));
-                const float4 t1v = __ldcs((const float4*)(p.target + urow + v + 4));
-                tv[0] = t0v.x; tv[1] = t0v.y; tv[2] = t0v.z; tv[3] = t0v.w;
-                tv[4] = t1v.x; tv[5] = t1v.y; tv[6] = t1v.z; tv[7] = t1v.w;
+#pragma unroll
+                for (int e = 0; e < GE; e += 4) {
+                  const float4 t4 = __ldcs((const float4*)(p.target + urow + v + e));
+                  tv[e] = t4.x; tv[e + 1] = t4.y; tv[e + 2] = t4.z; tv[e + 3] = t4.w;
+                }
               } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) tv[e] = p.target[urow + v + e];
+                for (int e = 0; e < GE; ++e) tv[e] = p.target[urow + v + e];
               }
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
+              for (int e = 0; e < GE; ++e) {
                 tv[e] *= p.invT;
                 tmax = fmaxf(tmax, tv[e]);
               }
             }
           } else {  // the slice's ragged end, or U rows without 16-byte alignment
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
+            for (int e = 0; e < GE; ++e) {
               const int vv = v + e;
               float uval;
               if (vq) {
-                const uint32_t wd = ((const uint32_t*)&uq)[e >> 1];
+                const uint32_t wd = ((const uint32_t*)&uq[e >> 3])[(e & 7) >> 1];
                 uval = __uint_as_float((e & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
               } else {
                 uval = vv < V ? ld_u(p.U, urow + vv, p.u_bf16) : 0.f;
@@ -522,10 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (p.logits)  // debug output: z
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
+            for (int e = 0; e < GE; ++e)
               if (v + e < V) p.logits[urow + v + e] = y[e];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {  // y = z / T
+          for (int e = 0; e < GE; ++e) {  // y = z / T
             y[e] *= p.invT;
             gmax = fmaxf(gmax, y[e]);
           }
@@ -534,14 +589,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             st.m = gmax;
             C = __expf(st.m - st.best);
           }
-          const U4 r0 = philox4x32_10((uint32_t)(v >> 2), (uint32_t)ks, (uint32_t)b, kNoiseTag,
-                                      p.seed_lo, p.seed_hi);
-          const U4 r1 = philox4x32_10((uint32_t)(v >> 2) + 1u, (uint32_t)ks, (uint32_t)b, kNoiseTag,
-                                      p.seed_lo, p.seed_hi);
-          const uint32_t words[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+          uint32_t words[GE];
+#pragma unroll
+          for (int q4 = 0; q4 < GE / 4; ++q4) {  // independent Philox calls, one per 4 entries
+            const U4 rq = philox4x32_10((uint32_t)(v >> 2) + q4, (uint32_t)ks, (uint32_t)b,
+                                        kNoiseTag, p.seed_lo, p.seed_hi);
+            words[4 * q4] = rq.x;
+            words[4 * q4 + 1] = rq.y;
+            words[4 * q4 + 2] = rq.z;
+            words[4 * q4 + 3] = rq.w;
+          }
           float ls[2] = {0.f, 0.f};  // two partial sums: a shorter dependency chain
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
+          for (int e = 0; e < GE; ++e) {
             const float pe = __expf(y[e] - st.m);
             ls[e & 1] += pe;
             // exact skip: w = 1 - u; -ln u >= w, so w >= 1.001 exp(y - best) rules it out
@@ -562,14 +622,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               st.mt = tmax;
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) st.lt += __expf(tv[e] - st.mt);
+            for (int e = 0; e < GE; ++e) st.lt += __expf(tv[e] - st.mt);
             float* yo = p.ybuf + (size_t)b * V + v;
-            if (vec_t && v + 8 <= V) {
-              *(float4*)yo = make_float4(y[0], y[1], y[2], y[3]);
-              *(float4*)(yo + 4) = make_float4(y[4], y[5], y[6], y[7]);
+            if (vec_t && full) {
+#pragma unroll
+              for (int e = 0; e < GE; e += 4) *(float4*)(yo + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
             } else {
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
+              for (int e = 0; e < GE; ++e)
                 if (v + e < V) yo[e] = y[e];
             }
           }
@@ -585,13 +645,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         failed = true;
         break;
       }
-      // ---- merge the column quarters of each request in a fixed order, publish the candidate
-      if (cq > 0) scratch[(cq - 1) * kM + m] = st;
+      // ---- merge each request's partial states (column quarters; packed: also the two tiles
+      // of each round) in a fixed order, publish the candidate
+      const int kpart = half * 4 + cq, npart = pk ? 8 : 4, pstride = pk ? 64 : kM;
+      if (kpart > 0) scratch[(kpart - 1) * pstride + m] = st;
       esync<kEpiThreads>();
-      if (cq == 0 && row_ok) {
-#pragma unroll
-        for (int i = 0; i < 3; ++i) {
-          const TSlot& o = scratch[i * kM + m];
+      if (kpart == 0 && row_ok) {
+        for (int i = 0; i < npart - 1; ++i) {
+          const TSlot& o = scratch[i * pstride + m];
           best_merge(st.best, st.tok, o.best, o.tok);
           lse_merge(st.m, st.l, o.m, o.l);
           lse_merge(st.mt, st.lt, o.mt, o.lt);
@@ -761,21 +822,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 int draft_tc_supported(int B, int r, int w_bf16) { return w_bf16 && B >= 1 && r % 8 == 0 && r <= 512; }
 
 bool draft_tc_configure(DraftParams& p, size_t smem_optin) {
-  // U tiles are staged by TMA when U is bf16 with 16-byte aligned rows; prefer two of them, then
-  // two A buffers, then the deepest W2 ring (at least 3 stages) that fits
+  // U tiles are staged by TMA when U is bf16 with 16-byte aligned rows; prefer (at most 64
+  // requests) vocabulary tiles in pairs so that all 128 TMEM lanes and epilogue warps work, then
+  // two staged U tiles, then two A buffers, then the deepest W2 ring (at least 3 stages)
   const int nu_max = p.u_bf16 && p.V % 8 == 0 ? 2 : 0;
-  for (int nu = nu_max; nu >= 0; --nu)
-    for (int na = 2; na >= 1; --na)
-      for (int ns = 8; ns >= 3; --ns) {
-        const TCLayout L = tc_layout(p.r, na, ns, p.head == 1, nu);
-        if (L.total <= smem_optin) {
-          p.tc_na = na;
-          p.tc_nu = nu;
-          p.nstages = ns;
-          p.smem_bytes = L.total;
-          return true;
+  for (int pk = p.B <= 64 ? 1 : 0; pk >= 0; --pk)
+    for (int nu = nu_max; nu >= 0; --nu)
+      for (int na = 2; na >= 1; --na)
+        for (int ns = 8; ns >= 3; --ns) {
+          const TCLayout L = tc_layout(p.r, na, ns, p.head == 1, nu, pk != 0);
+          if (L.total <= smem_optin && (nu > 0 || nu_max == 0 || pk == 0)) {
+            p.tc_pk = pk;
+            p.tc_na = na;
+            p.tc_nu = nu;
+            p.nstages = ns;
+            p.smem_bytes = L.total;
+            return true;
+          }
         }
-      }
   return false;
 }
 
@@ -792,7 +856,8 @@ cudaError_t launch_draft_tc(DraftParams& p, int nblocks, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   CUtensorMap tmap_u;
   std::memset(&tmap_u, 0, sizeof tmap_u);
-  if (p.tc_nu > 0 && !encode_u_bf16_3d(&tmap_u, p.U, p.B, p.gamma, p.V)) return cudaErrorInvalidValue;
+  if (p.tc_nu > 0 && !encode_u_bf16_3d(&tmap_u, p.U, p.B, p.gamma, p.V, p.tc_pk ? 64 : 128))
+    return cudaErrorInvalidValue;
   int na = p.tc_na, ns = p.nstages, nu = p.tc_nu;
   void* args[] = {(void*)&p, (void*)&tmap, (void*)&tmap_u, (void*)&na, (void*)&ns, (void*)&nu};
   return cudaLaunchCooperativeKernel(kern, dim3(nblocks), dim3(kThreads), args, p.smem_bytes, stream);

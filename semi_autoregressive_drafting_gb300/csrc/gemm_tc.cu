@@ -166,12 +166,12 @@ bool encode_bf16_2d(CUtensorMap* m, const void* base, int rows, int cols, int ld
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_u_bf16_3d(CUtensorMap* m, const void* U, int B, int G, int V) {
+bool encode_u_bf16_3d(CUtensorMap* m, const void* U, int B, int G, int V, int box_rows) {
   EncodeTiled enc = tmap_encoder();
   if (!enc) return false;
   const cuuint64_t gdim[3] = {(cuuint64_t)V, (cuuint64_t)G, (cuuint64_t)B};
   const cuuint64_t gstride[2] = {(cuuint64_t)V * 2, (cuuint64_t)G * V * 2};
-  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   const cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(U), gdim, gstride, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

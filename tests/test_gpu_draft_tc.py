@@ -72,3 +72,10 @@ def test_high_concurrency_full_sampled_rows():
     wl = inputs.WORKLOADS["high_concurrency_sched"]
     ties, _ = _run(wl, rows=[0, 129, 300, 511], want_logits=False)
     assert ties <= 1
+
+
+@pytest.mark.parametrize("B,V", [(37, 40000), (64, 38537), (6, 2000)])
+def test_tc_paired_tiles(B, V):
+    # at most 64 requests: vocabulary tiles go in pairs (lanes 64-127 hold the second tile);
+    # blocks with an odd tile count end with a single-tile round
+    _run(BASE.with_(B=B, V=V, d=128, seed=100 + B), target_noise=0.5 if B == 37 else None)
