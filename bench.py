@@ -34,9 +34,13 @@ METRIC = "draft tokens/sec (B×γ per block) and achieved HBM GB/s vs roofline, 
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: every timed block starts with a cold L2
 
-# ncu DRAM traffic (read + write bytes) of one draft-kernel launch on the default workload,
-# with the sha256 prefix of the kernel source it was measured on.  A changed kernel reports null.
-TRAFFIC = {"source_sha": "477d1b6c2463407e", "bytes_per_launch": 82730496}  # 80.62 MB + 2.11 MB
+# ncu DRAM traffic (read + write bytes) of one draft-kernel launch per workload: the kernel's
+# source file, the sha256 prefix of the source it was measured on, and the bytes.  A workload
+# without a capture, or whose kernel changed since, reports null.
+TRAFFIC = {
+    "qwen3_4b_markov": ("draft_cc.cu", "477d1b6c2463407e", 82730496),          # 80.62 + 2.11 MB
+    "high_concurrency_sched": ("draft_tc.cu", "684388eea4fd34c0", 5693589248),  # 5686 + 7.5 MB
+}
 
 
 def _sha(path):
@@ -323,8 +327,9 @@ def main():
         peak, peak_kind = load_peaks()
         alg = algorithmic_bytes(wl)
         achieved = alg / (ms_step * 1e-3) / 1e9
-        src = os.path.join(ROOT, "semi_autoregressive_drafting_gb300", "csrc", "draft_cc.cu")
-        traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["source_sha"] == _sha(src) else None
+        cap = TRAFFIC.get(wl.name)
+        src = cap and os.path.join(ROOT, "semi_autoregressive_drafting_gb300", "csrc", cap[0])
+        traffic = cap[2] if cap and _sha(src) == cap[1] else None
         head = 0 if wl.head == "markov" else 1
         launches = ds.draft_launches(head, B, wl.V, wl.r, wl.dtype == "bf16")
         path = ds.draft_path(head, B, wl.V, wl.r, wl.dtype == "bf16")

@@ -12,12 +12,18 @@
 //     lane quarter, each taking 32 of a tile's 128 columns for its 32 requests, with U and the
 //     target fetched as 16-byte vectors issued before the accumulator wait;
 //   * the epilogue fuses +U_k, /T, the online (max, sum-exp), and Gumbel-max sampling with an
-//     exact skip: with w = 1 - u (exact from the Philox bits) and q = exp(y - best), an entry
-//     with w >= 1.001 q cannot beat the running best (-ln u >= w, so its score is below
-//     best - 0.0009), so the two logarithms run only for the rare entries that might;
+//     exact skip, in log2 units (y2 = y log2 e, exponentials by ex2): with w = 1 - u (exact
+//     from the Philox bits) and q = exp(y - best), an entry with w >= 1.001 q cannot beat the
+//     running best (-ln u >= w, so its score is below best - 0.0009), so the two logarithms
+//     run only for the rare entries that might; the test is one FMA and one compare per entry,
+//     and the Philox rounds that do not depend on the vocabulary index are computed once;
 //   * per step, each block publishes one candidate per request with a 64-bit atomicMax on an
 //     order-independent key, then a bounded grid barrier; the Eq 8 label runs its second pass
-//     over the block's slice after the barrier from y saved in the workspace.
+//     over the block's slice from y saved in the workspace, after the barrier and while the
+//     next step's first MMAs run;
+//   * the two spare warps compute Eq 7's w[:d] . h_k for the block's own requests up front (it
+//     does not depend on the drafted tokens); after the last step one warp per owned (request,
+//     position) finishes the token, the log-normaliser, c_k and Eq 8, then S_k.
 #include <cuda.h>
 
 #include <cstring>
@@ -89,7 +95,7 @@ __host__ __device__ inline TCLayout tc_layout(int r, int na, int nstage, bool rn
   L.misc = off;
   off = align_up_t(off + sizeof(TMisc), 128);
   L.bars = off;
-  off += (size_t)(2 * nstage + 2 * kAcc + 2 * na + 2 + 2 * nu) * 8;
+  off += (size_t)(2 * nstage + 2 * kAcc + 2 * na + 3 + 2 * nu) * 8;
   L.total = align_up_t(off, 1024) + 1024;  // + slack to align the dynamic base to 1024
   return L;
 }
@@ -135,12 +141,32 @@ __device__ __forceinline__ void tslot_init(TSlot& s) {
   s.lt = 0.f;
 }
 
-// (max, sum-exp) of all blocks' partials, merged by one warp in a fixed order
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// 2^x on the special-function unit (relative error about 2^-22; 0 for x = -inf)
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void prefetch_line(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// (max, sum-exp) of all blocks' partials, merged by one warp in a fixed order; each lane
+// issues the loads of up to 8 partials before merging them
 __device__ __forceinline__ float2 merge_ml(const float2* part, int n, int lane) {
   float m = -INFINITY, l = 0.f;
-  for (int i = lane; i < n; i += 32) {
-    const float2 q = part[i];
-    lse_merge(m, l, q.x, q.y);
+  for (int i0 = 0; i0 < n; i0 += 256) {
+    float2 q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + lane + 32 * j;
+      q[j] = i < n ? part[i] : make_float2(-INFINITY, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) lse_merge(m, l, q[j].x, q[j].y);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -149,6 +175,95 @@ __device__ __forceinline__ float2 merge_ml(const float2* part, int n, int lane) 
     lse_merge(m, l, m2, l2);
   }
   return make_float2(m, l);
+}
+
+// Sum of n floats, one warp, up to 8 loads in flight per lane (fixed order)
+__device__ __forceinline__ float warp_sum_n(const float* a, int n, int lane) {
+  float s = 0.f;
+  for (int i0 = 0; i0 < n; i0 += 256) {
+    float q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + lane + 32 * j;
+      q[j] = i < n ? a[i] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s += q[j];
+  }
+  return warp_sum(s);
+}
+
+// 8 bf16 (one 16-byte chunk) -> floats
+__device__ __forceinline__ void bf16x8(const uint4& q, float* f) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// Eq 7's two dot products for one warp (w and W1 bf16; h bf16 or fp32).  16-byte loads, four
+// chunks in flight per lane, when w is 16-byte aligned; h and W1 always are (the ABI requires
+// it, and d, r are multiples of 8).
+// w[:d] . h[o] for the (request, position) row o
+__device__ __forceinline__ float eq7_hdot(const DraftParams& p, size_t o, int lane) {
+  const __nv_bfloat16* w = (const __nv_bfloat16*)p.w;
+  float acc = 0.f;
+  if (((uintptr_t)w & 15) == 0) {
+    const int nd = p.d / 8;
+    const uint4* w4 = (const uint4*)w;
+    for (int j0 = 0; j0 < nd; j0 += 128) {
+      uint4 wq[4];
+      float hv[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + lane + 32 * u;
+        wq[u] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hv[u][i] = 0.f;
+        if (j < nd) {
+          wq[u] = w4[j];
+          if (p.u_bf16) {
+            bf16x8(((const uint4*)((const __nv_bfloat16*)p.h + o * p.d))[j], hv[u]);
+          } else {
+            const float4* hp = (const float4*)((const float*)p.h + o * p.d) + 2 * j;
+            *(float4*)&hv[u][0] = hp[0];
+            *(float4*)&hv[u][4] = hp[1];
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float wf[8];
+        bf16x8(wq[u], wf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc = fmaf(wf[i], hv[u][i], acc);
+      }
+    }
+  } else {
+    for (int j = lane; j < p.d; j += 32) acc += ld_u(p.w, j, 1) * ld_u(p.h, o * p.d + j, p.u_bf16);
+  }
+  return warp_sum(acc);
+}
+// w[d:] . W1[x]
+__device__ __forceinline__ float eq7_edot(const DraftParams& p, int x, int lane) {
+  const __nv_bfloat16* w = (const __nv_bfloat16*)p.w;
+  const __nv_bfloat16* e = (const __nv_bfloat16*)p.W1 + (size_t)x * p.r;
+  float acc = 0.f;
+  if (((uintptr_t)w & 15) == 0) {
+    const uint4* w4 = (const uint4*)w + p.d / 8;
+    for (int j = lane; j < p.r / 8; j += 32) {
+      float wf[8], ef[8];
+      bf16x8(w4[j], wf);
+      bf16x8(((const uint4*)e)[j], ef);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc = fmaf(wf[i], ef[i], acc);
+    }
+  } else {
+    for (int j = lane; j < p.r; j += 32) acc += ld_u(p.w, (size_t)p.d + j, 1) * __bfloat162float(e[j]);
+  }
+  return warp_sum(acc);
 }
 
 // Conditioning token of step ks for request b and whether the request is still valid.
@@ -194,7 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* a_empty = a_full + na;
   uint64_t* tmem_done = a_empty + na;
   uint64_t* mma_done = tmem_done + 1;
-  uint64_t* u_full = mma_done + 1;   // [nu] a U tile has landed
+  uint64_t* hdot_ready = mma_done + 1;  // the spare warps have written w[:d] . h_k (Eq 7)
+  uint64_t* u_full = hdot_ready + 1;  // [nu] a U tile has landed
   uint64_t* u_empty = u_full + nu;   // [nu] every epilogue warp has read it
   uint8_t* ubuf = smem + Lay.ubuf;
 
@@ -229,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(tmem_done, kEpiWarps);
     mbar_init(mma_done, 1);
+    mbar_init(hdot_ready, 2);
     for (int i = 0; i < nu; ++i) {
       mbar_init(&u_full[i], 1);
       mbar_init(&u_empty[i], kEpiWarps);
@@ -371,7 +488,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_dealloc(tmem, kTmemCols);
     return;
   }
-  if (warp < 4) return;
+  // owned requests: b = cta + i nCTA (Eq 7 / S_k, tokens and normalisers are finished by them)
+  const int nown = cta < B ? (B - 1 - cta) / nCTA + 1 : 0;
+
+  // =========================================================== spare warps: w[:d] . h_k (Eq 7)
+  // for every owned (request, position); these do not depend on the drafted tokens
+  if (warp == 2 || warp == 3) {
+    if (p.h && p.w)
+      for (int pi = warp - 2; pi < nown * G; pi += 2) {
+        const size_t o = (size_t)(cta + (pi / G) * nCTA) * G + pi % G;
+        const float hd = eq7_hdot(p, o, lane);
+        if (lane == 0) p.hdot[o] = hd;
+      }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(hdot_ready);
+    return;
+  }
 
   // =========================================================== epilogue warps
   const int et = tid - 128;          // 0..511
@@ -398,6 +530,196 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row < 64 || row >= 128) ((uint4*)abuf)[i] = make_uint4(0, 0, 0, 0);
     }
   }
+
+  // y and the target in log2 units: y2 = z log2(e) / T, so that 2^(y2 - m2) = exp(y - m)
+  const float s2 = p.invT * kLog2e;
+  const void* const Up = p.U;
+  const float* const tgp = p.target;
+  float* const lgp = p.logits;
+  float* const ybp = p.ybuf;
+  const uint32_t sd0 = p.seed_lo, sd1 = p.seed_hi;
+
+  // One group of 8 consecutive vocabulary entries v..v+7 of this thread's row: logits (Eq 4),
+  // the online normaliser, Philox Gumbel-max with the exact skip; with a target, its
+  // normaliser, and y saved for the Eq 8 second pass.  st.m, st.mt and st.best are in log2
+  // units here.  Skip test: with w = 1 - u (exact) and q = exp(y - best), an entry with
+  // w >= 1.001 q cannot win (-ln u >= w, so its score is below best - 0.0009 in natural units).
+  // f = 1 + w - 2^-24 is read straight from the bits, and f >= fl(1 + 1.002 q') (q' = the
+  // computed q, within 1e-5 of q) implies w >= 1.002 q' >= 1.001 q, so a skipped entry is one
+  // the exact fp32 comparison would also reject.  Cp = 1.002 exp(m - best), q' = pe Cp / 1.002.
+  auto group = [&](int gi, int vb, const uint32_t* bs, const uint8_t* ub, size_t urow, int b,
+                   TSlot& st, float& Cp, const PhiloxFixed& pfx) {
+    const int v = vb + 8 * gi;
+    if (v >= V) return;
+    const bool full = v + 8 <= V;
+    float y[8], tv[8];
+    uint4 uq = make_uint4(0, 0, 0, 0);
+    bool vq = false;
+    if (nu > 0) {  // staged: 16-byte chunk (cq % 2) * 4 + gi of the row sits at chunk ^ (row % 8)
+      uq = *(const uint4*)(ub + (((((cq & 1) << 2) + gi) ^ (lrow & 7)) << 4));
+      vq = true;
+    } else if (vec_u && full) {
+      uq = __ldcs((const uint4*)((const __nv_bfloat16*)Up + urow + v));
+      vq = true;
+    }
+    if (vq && full) {
+      float uf[8];
+      bf16x8(uq, uf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = uf[e] + __uint_as_float(bs[e]);  // z for now
+      if (TGT) {
+        if (vec_t) {
+          const float4 a = *(const float4*)(tgp + urow + v);
+          const float4 c4 = *(const float4*)(tgp + urow + v + 4);
+          tv[0] = a.x; tv[1] = a.y; tv[2] = a.z; tv[3] = a.w;
+          tv[4] = c4.x; tv[5] = c4.y; tv[6] = c4.z; tv[7] = c4.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) tv[e] = tgp[urow + v + e];
+        }
+      }
+    } else {  // the slice's ragged end, or U rows without 16-byte alignment
+      float uf[8];
+      bf16x8(uq, uf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int vv = v + e;
+        const float uval = vq ? uf[e] : (vv < V ? ld_u(Up, urow + vv, p.u_bf16) : 0.f);
+        y[e] = vv < V ? uval + __uint_as_float(bs[e]) : -INFINITY;
+        if (TGT) tv[e] = vv < V ? tgp[urow + vv] : -INFINITY;
+      }
+    }
+    if (lgp)  // debug output: z
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (v + e < V) lgp[urow + v + e] = y[e];
+    float gmax = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      y[e] *= s2;
+      gmax = fmaxf(gmax, y[e]);
+    }
+    if (gmax > st.m) {  // rescale the running sum to the new max, once per group
+      st.l *= ex2f(st.m - gmax);
+      st.m = gmax;
+      Cp = 1.002f * ex2f(st.m - st.best);
+    }
+    uint32_t wd[8];
+    {
+      const U4 r0 = philox_var((uint32_t)(v >> 2), pfx, sd0, sd1);
+      const U4 r1 = philox_var((uint32_t)(v >> 2) + 1u, pfx, sd0, sd1);
+      wd[0] = r0.x; wd[1] = r0.y; wd[2] = r0.z; wd[3] = r0.w;
+      wd[4] = r1.x; wd[5] = r1.y; wd[6] = r1.z; wd[7] = r1.w;
+    }
+    float ls0 = 0.f, ls1 = 0.f;
+    bool any = false;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float pe = ex2f(y[e] - st.m);
+      if (e & 1) ls1 += pe; else ls0 += pe;
+      const float f = __uint_as_float(0x3F800000u | (~wd[e] >> 9));
+      any |= f < fmaf(pe, Cp, 1.f);
+    }
+    st.l += ls0 + ls1;
+    if (any) {  // rare: the candidates in order (ties keep the smaller entry), one copy of
+                // the logarithms for all of them to keep the loop's code small
+      uint32_t mask = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float pe = ex2f(y[e] - st.m);
+        const float f = __uint_as_float(0x3F800000u | (~wd[e] >> 9));
+        mask |= (f < fmaf(pe, Cp, 1.f)) ? (1u << e) : 0u;
+      }
+      while (mask) {
+        const int e = __ffs(mask) - 1;
+        mask &= mask - 1;
+        float ye = y[0];
+        uint32_t we = wd[0];
+#pragma unroll
+        for (int j = 1; j < 8; ++j)
+          if (e == j) {
+            ye = y[j];
+            we = wd[j];
+          }
+        // u = (2 (bits >> 9) + 1) 2^-24, exactly; Gumbel noise in log2 units: -log2(-ln u)
+        const float u = __uint_as_float(0x3F800000u | (we >> 9)) - 0.99999994f;
+        const float sc = ye - log2f(-logf(u));
+        if (sc > st.best) {
+          st.best = sc;
+          st.tok = (uint32_t)(v + e);
+        }
+      }
+      Cp = 1.002f * ex2f(st.m - st.best);
+    }
+    if (TGT) {
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        tv[e] *= s2;
+        tmax = fmaxf(tmax, tv[e]);
+      }
+      if (tmax > st.mt) {
+        st.lt *= ex2f(st.mt - tmax);
+        st.mt = tmax;
+      }
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (e & 1) a1 += ex2f(tv[e] - st.mt); else a0 += ex2f(tv[e] - st.mt);
+      }
+      st.lt += a0 + a1;
+      float* yo = ybp + (size_t)b * V + v;  // y2, read back by the second pass
+      if (vec_t && full) {
+        *(float4*)yo = make_float4(y[0], y[1], y[2], y[3]);
+        *(float4*)(yo + 4) = make_float4(y[4], y[5], y[6], y[7]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (v + e < V) yo[e] = y[e];
+      }
+    }
+  };
+
+  // Eq 8 of step kp over this block's slice, once every block has published step kp: the global
+  // normalisers of p^d and p^t, then the slice's sum of |p^d - p^t| for each request (y2 from
+  // the workspace, the target re-read; eight 16-byte loads of each in flight per lane)
+  auto second_pass = [&](int kp) {
+    for (int b = ew; b < B; b += kEpiWarps) {
+      const float2 a = merge_ml(p.ml + ((size_t)kp * B + b) * nCTA, nCTA, lane);
+      const float2 tt = merge_ml(p.mlt + ((size_t)kp * B + b) * nCTA, nCTA, lane);
+      const float Ld2 = (a.x + logf(a.y)) * kLog2e, Lt2 = (tt.x + logf(tt.y)) * kLog2e;
+      const float* yr = ybp + (size_t)b * V;
+      const float* tr = tgp + ((size_t)b * G + kp) * V;
+      float acc = 0.f;
+      int vt = sl0;  // first entry left for the scalar tail
+      if (vec_t) {   // sl0 is a multiple of 128
+        const int n4 = (sl1 - sl0) >> 2;
+        const float4* y4 = (const float4*)(yr + sl0);
+        const float4* t4 = (const float4*)(tr + sl0);
+        for (int i0 = 0; i0 < n4; i0 += 256) {
+          float4 yv[8], tq[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int i = i0 + lane + 32 * j;
+            yv[j] = i < n4 ? __ldcs(y4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            tq[j] = i < n4 ? __ldcs(t4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (i0 + lane + 32 * j < n4)
+              acc += fabsf(ex2f(yv[j].x - Ld2) - ex2f(tq[j].x * s2 - Lt2)) +
+                     fabsf(ex2f(yv[j].y - Ld2) - ex2f(tq[j].y * s2 - Lt2)) +
+                     fabsf(ex2f(yv[j].z - Ld2) - ex2f(tq[j].z * s2 - Lt2)) +
+                     fabsf(ex2f(yv[j].w - Ld2) - ex2f(tq[j].w * s2 - Lt2));
+        }
+        vt = sl0 + 4 * n4;
+      }
+      for (int v = vt + lane; v < sl1; v += 32)
+        acc += fabsf(ex2f(yr[v] - Ld2) - ex2f(tr[v] * s2 - Lt2));
+      acc = warp_sum(acc);
+      if (lane == 0) p.l1p[((size_t)kp * B + b) * nCTA + cta] = acc;
+    }
+  };
 
   for (int ks = 0; ks < G && !failed; ++ks) {
     if (RNN) {
@@ -475,20 +797,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       esync<kEpiThreads>();
       if (et == 0) mbar_arrive(&a_full[ab]);
 
+      // Eq 8 of the previous step, while the MMAs of this step's first rounds run
+      if (tgt && c == 0 && ks > 0) {
+        second_pass(ks - 1);
+        esync<kEpiThreads>();
+      }
+
       // ---- tiles: bias from TMEM, logits, sampling, normalisers
       const int b = c * kM + m;
       const bool row_ok = b < B;
       const size_t urow = ((size_t)b * G + ks) * V;
+      const PhiloxFixed pfx = philox_fix((uint32_t)ks, (uint32_t)b, kNoiseTag, sd0, sd1);
       TSlot st;
       tslot_init(st);
-      float C = INFINITY;  // exp(m - best) of this thread's running state
+      float Cp = INFINITY;           // 1.002 exp(m - best) of this thread's running state
+      const int tstep = pk ? 2 : 1;  // this warp's tile advances by tstep per round
       for (int rd = 0; rd < nround; ++rd, ++acc_i) {
         const int acc = acc_i % kAcc;
         const int t = pk ? 2 * rd + half : rd;  // this warp's vocabulary tile of the round
         const bool tile_ok = t < ntile;          // (packed, odd count: the last round has one)
         const int vb = (t0 + t) * kNT + cq * 32;  // first vocab entry of this thread's 32
-        // the tile's U: staged by TMA (row m; 16-byte chunk (cq % 2) * 4 + g of box cq / 2 sits at
-        // chunk position ^ (m % 8)), kept until the tile is done; else read from global
+        if (row_ok && t + 3 * tstep < ntile) {  // this thread's U and target lines, 3 rounds ahead
+          const size_t vp = urow + (size_t)(t0 + t + 3 * tstep) * kNT + cq * 32;
+          if (nu > 0) prefetch_line((const __nv_bfloat16*)Up + vp);
+          if (TGT) prefetch_line(tgp + vp);
+        }
+        // the tile's U: staged by TMA, kept until the tile is done; else read from global
         int us = -1;
         if (nu > 0) {
           us = ui % nu;
@@ -507,132 +841,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_after_sync();
         const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + acc * kNT + cq * 32;
-        // groups of GE entries, rolled to keep the code small: bias from TMEM, U, GE / 4
-        // independent Philox calls; the running max moves at most once per group.  (16-entry
-        // groups measured slower on GB300: 3.32 against 2.97 ms per block at B = 512.)
-        constexpr int GE = 8;
+        const bool act = row_ok && tile_ok;
+        // one 8-column TMEM load (the whole warp) per 8-entry group; the loop stays rolled to
+        // keep the code small
 #pragma unroll 1
-        for (int gi = 0; gi < 32 / GE; ++gi) {
-          uint32_t bias[GE];
+        for (int gi = 0; gi < 4; ++gi) {
+          uint32_t bias[8];
           __syncwarp();
-#pragma unroll
-          for (int h8 = 0; h8 < GE / 8; ++h8)  // the whole warp, every group
-            tc::tmem_ld8(tcol + GE * gi + 8 * h8, *(uint32_t(*)[8])&bias[8 * h8]);
-          tc::tmem_ld_wait();
-          const int v = vb + GE * gi;
-          if (!row_ok || !tile_ok || v >= V) continue;  // (no further warp-collective work)
-          const bool full = v + GE <= V;  // every entry exists (all groups but the slice's last)
-          uint4 uq[GE / 8];
-#pragma unroll
-          for (int h8 = 0; h8 < GE / 8; ++h8) {
-            const int c8 = GE / 8 * gi + h8;  // 16-byte chunk of this thread's 32 entries
-            if (nu > 0) uq[h8] = *(const uint4*)(ub + (((((cq & 1) << 2) + c8) ^ (lrow & 7)) << 4));
-            else if (vec_u && full)
-              uq[h8] = __ldcs((const uint4*)((const __nv_bfloat16*)p.U + urow + v + 8 * h8));
-          }
-          const bool vq = nu > 0 || (vec_u && full);
-          float y[GE], tv[GE];
-          float gmax = -INFINITY, tmax = -INFINITY;
-          if (vq && full) {
-#pragma unroll
-            for (int e = 0; e < GE; ++e) {
-              const uint32_t wd = ((const uint32_t*)&uq[e >> 3])[(e & 7) >> 1];
-              const float uval = __uint_as_float((e & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
-              y[e] = uval + __uint_as_float(bias[e]);  // z for now
-            }
-            if (TGT) {
-              if (vec_t) {
-#pragma unroll
-                for (int e = 0; e < GE; e += 4) {
-                  const float4 t4 = __ldcs((const float4*)(p.target + urow + v + e));
-                  tv[e] = t4.x; tv[e + 1] = t4.y; tv[e + 2] = t4.z; tv[e + 3] = t4.w;
-                }
-              } else {
-#pragma unroll
-                for (int e = 0; e < GE; ++e) tv[e] = p.target[urow + v + e];
-              }
-#pragma unroll
-              for (int e = 0; e < GE; ++e) {
-                tv[e] *= p.invT;
-                tmax = fmaxf(tmax, tv[e]);
-              }
-            }
-          } else {  // the slice's ragged end, or U rows without 16-byte alignment
-#pragma unroll
-            for (int e = 0; e < GE; ++e) {
-              const int vv = v + e;
-              float uval;
-              if (vq) {
-                const uint32_t wd = ((const uint32_t*)&uq[e >> 3])[(e & 7) >> 1];
-                uval = __uint_as_float((e & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
-              } else {
-                uval = vv < V ? ld_u(p.U, urow + vv, p.u_bf16) : 0.f;
-              }
-              y[e] = vv < V ? uval + __uint_as_float(bias[e]) : -INFINITY;  // z for now
-              if (TGT) {
-                tv[e] = vv < V ? p.target[urow + vv] * p.invT : -INFINITY;
-                tmax = fmaxf(tmax, tv[e]);
-              }
-            }
-          }
-          if (p.logits)  // debug output: z
-#pragma unroll
-            for (int e = 0; e < GE; ++e)
-              if (v + e < V) p.logits[urow + v + e] = y[e];
-#pragma unroll
-          for (int e = 0; e < GE; ++e) {  // y = z / T
-            y[e] *= p.invT;
-            gmax = fmaxf(gmax, y[e]);
-          }
-          if (gmax > st.m) {  // rescale the running sum to the new max, once per group
-            st.l *= __expf(st.m - gmax);
-            st.m = gmax;
-            C = __expf(st.m - st.best);
-          }
-          uint32_t words[GE];
-#pragma unroll
-          for (int q4 = 0; q4 < GE / 4; ++q4) {  // independent Philox calls, one per 4 entries
-            const U4 rq = philox4x32_10((uint32_t)(v >> 2) + q4, (uint32_t)ks, (uint32_t)b,
-                                        kNoiseTag, p.seed_lo, p.seed_hi);
-            words[4 * q4] = rq.x;
-            words[4 * q4 + 1] = rq.y;
-            words[4 * q4 + 2] = rq.z;
-            words[4 * q4 + 3] = rq.w;
-          }
-          float ls[2] = {0.f, 0.f};  // two partial sums: a shorter dependency chain
-#pragma unroll
-          for (int e = 0; e < GE; ++e) {
-            const float pe = __expf(y[e] - st.m);
-            ls[e & 1] += pe;
-            // exact skip: w = 1 - u; -ln u >= w, so w >= 1.001 exp(y - best) rules it out
-            const float w = bits_to_uniform(~words[e]);
-            if (!(w >= 1.001f * (pe * C))) {
-              const float sc = y[e] + gumbel_from_uniform(bits_to_uniform(words[e]));
-              if (sc > st.best) {  // entries grow along this thread's sequence: ties keep the smaller
-                st.best = sc;
-                st.tok = (uint32_t)(v + e);
-                C = __expf(st.m - st.best);
-              }
-            }
-          }
-          st.l += ls[0] + ls[1];
-          if (TGT) {
-            if (tmax > st.mt) {
-              st.lt *= __expf(st.mt - tmax);
-              st.mt = tmax;
-            }
-#pragma unroll
-            for (int e = 0; e < GE; ++e) st.lt += __expf(tv[e] - st.mt);
-            float* yo = p.ybuf + (size_t)b * V + v;
-            if (vec_t && full) {
-#pragma unroll
-              for (int e = 0; e < GE; e += 4) *(float4*)(yo + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < GE; ++e)
-                if (v + e < V) yo[e] = y[e];
-            }
-          }
+          tc::tmem_ld8_wait(tcol + 8 * gi, bias);
+          if (act) group(gi, vb, bias, ub, urow, b, st, Cp, pfx);
         }
         tc::fence_before_sync();
         __syncwarp();
@@ -645,6 +862,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         failed = true;
         break;
       }
+      // back to natural units for the normalisers (the published best stays in log2 units: it
+      // is only compared with other blocks' log2 scores)
+      st.m *= kLn2;
+      st.mt *= kLn2;
       // ---- merge each request's partial states (column quarters; packed: also the two tiles
       // of each round) in a fixed order, publish the candidate
       const int kpart = half * 4 + cq, npart = pk ? 8 : 4, pstride = pk ? 64 : kM;
@@ -692,39 +913,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       failed = true;
       break;
     }
-
-    if (tgt) {
-      // ---- Eq 8 second pass over this block's slice, all requests: normalisers of p^d, p^t
-      for (int b = 0; b < B; ++b) {
-        if (ew == (b % kEpiWarps)) {
-          const float2 a = merge_ml(p.ml + ((size_t)ks * B + b) * nCTA, nCTA, lane);
-          const float2 tt = merge_ml(p.mlt + ((size_t)ks * B + b) * nCTA, nCTA, lane);
-          const float Ld = a.x + logf(a.y), Lt = tt.x + logf(tt.y);
-          const float* yr = p.ybuf + (size_t)b * V;
-          const float* tr = p.target + ((size_t)b * G + ks) * V;
-          float acc = 0.f, acc2 = 0.f;
-          int vt = sl0;  // first entry left for the scalar tail
-          if (vec_t) {   // 16-byte loads (sl0 is a multiple of 128), several in flight per lane
-            const int n4 = (sl1 - sl0) >> 2;
-#pragma unroll 4
-            for (int i = lane; i < n4; i += 32) {
-              const float4 yv = __ldcs((const float4*)(yr + sl0) + i);
-              const float4 tv = __ldcs((const float4*)(tr + sl0) + i);
-              acc += fabsf(__expf(yv.x - Ld) - __expf(tv.x * p.invT - Lt)) +
-                     fabsf(__expf(yv.y - Ld) - __expf(tv.y * p.invT - Lt));
-              acc2 += fabsf(__expf(yv.z - Ld) - __expf(tv.z * p.invT - Lt)) +
-                      fabsf(__expf(yv.w - Ld) - __expf(tv.w * p.invT - Lt));
-            }
-            vt = sl0 + 4 * n4;
-          }
-          for (int v = vt + lane; v < sl1; v += 32)
-            acc += fabsf(__expf(yr[v] - Ld) - __expf(tr[v] * p.invT - Lt));
-          acc = warp_sum(acc + acc2);
-          if (lane == 0) p.l1p[((size_t)ks * B + b) * nCTA + cta] = acc;
-        }
-      }
-      esync<kEpiThreads>();
-    }
   }
 
   // release TMEM to its owner (also on the failure path)
@@ -736,45 +924,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (et == 0) atomicMax(&hdr->status, kErrTimeout);
     return;
   }
+  if (tgt) {  // Eq 8 of the last step
+    second_pass(G - 1);
+    esync<kEpiThreads>();
+  }
 
-  // ---- owned requests (b % nCTA == cta): tokens, log-normalisers, Eq 7 / S_k, Eq 8
-  for (int b = cta + ew * nCTA; b < B; b += kEpiWarps * nCTA) {
-    float surv = 1.f;
-    bool alive = true;
-    for (int k = 0; k < G; ++k) {
-      const size_t o = (size_t)b * G + k;
-      bool valid = false;
-      const int x = cond_token(p, b, k, &valid);
-      if (alive && !valid && lane == 0) atomicMax(&hdr->status, kErrInvalid);
-      alive = alive && valid;
-      const int tok = alive ? (int)key_token(ld_acquire64(&p.keys[(size_t)k * B + b])) : -1;
-      const float2 ml = merge_ml(p.ml + ((size_t)k * B + b) * nCTA, nCTA, lane);
-      if (p.h && p.w) {
-        float acc = 0.f;
-        for (int j = lane; j < p.d; j += 32)
-          acc += ld_u(p.w, j, 1) * ld_u(p.h, o * p.d + j, p.u_bf16);
-        for (int j = lane; j < r; j += 32)
-          acc += ld_u(p.w, (size_t)p.d + j, 1) * ld_u(p.W1, (size_t)x * r + j, 1);
-        acc = warp_sum(acc);
-        const float cv = alive ? sigmoidf_acc(acc) : NAN;
-        surv = alive ? surv * cv : NAN;
-        if (lane == 0) {
-          p.c[o] = cv;
-          p.S[o] = surv;
-        }
-      }
+  // ---- owned requests, one warp per (request, position): token, log-normaliser, Eq 7, and
+  // Eq 8 for all but the last position (the last block out finishes that one)
+  const bool conf = p.h && p.w;
+  if (conf && !mbar_wait_warp(hdot_ready, 0) && lane == 0) atomicMax(&hdr->status, kErrTimeout);
+  for (int pi = ew; pi < nown * G; pi += kEpiWarps) {
+    const int b = cta + (pi / G) * nCTA, k = pi % G;
+    const size_t o = (size_t)b * G + k;
+    bool valid = false;  // once false, false for every later position of the request
+    const int x = cond_token(p, b, k, &valid);
+    if (!valid && lane == 0) atomicMax(&hdr->status, kErrInvalid);
+    const int tok = valid ? (int)key_token(ld_acquire64(&p.keys[(size_t)k * B + b])) : -1;
+    const float2 ml = merge_ml(p.ml + ((size_t)k * B + b) * nCTA, nCTA, lane);
+    if (conf) {
+      const float z7 = ((volatile float*)p.hdot)[o] + eq7_edot(p, x, lane);
+      if (lane == 0) p.c[o] = valid ? sigmoidf_acc(z7) : NAN;
+    }
+    if (lane == 0) {
+      p.tokens[o] = tok;
+      p.lse[o] = valid ? ml.x + logf(ml.y) : NAN;
+    }
+    if (tgt && k + 1 < G) {
+      const float s = warp_sum_n(p.l1p + ((size_t)k * B + b) * nCTA, nCTA, lane);
       if (lane == 0) {
-        p.tokens[o] = tok;
-        p.lse[o] = alive ? ml.x + logf(ml.y) : NAN;
+        p.l1[o] = valid ? s : NAN;
+        p.cstar[o] = valid ? fminf(1.f, fmaxf(0.f, 1.f - 0.5f * s)) : NAN;
       }
-      if (tgt && k + 1 < G) {
-        float s = 0.f;
-        for (int i = lane; i < nCTA; i += 32) s += p.l1p[((size_t)k * B + b) * nCTA + i];
-        s = warp_sum(s);
-        if (lane == 0) {
-          p.l1[o] = alive ? s : NAN;
-          p.cstar[o] = alive ? fminf(1.f, fmaxf(0.f, 1.f - 0.5f * s)) : NAN;
-        }
+    }
+  }
+  if (conf) {  // S_k = prod_{i <= k} c_i, from the c this block's warps just wrote
+    esync<kEpiThreads>();
+    for (int i = et; i < nown; i += kEpiThreads) {
+      const size_t o = (size_t)(cta + i * nCTA) * G;
+      float surv = 1.f;
+      for (int k = 0; k < G; ++k) {
+        surv *= ((volatile float*)p.c)[o + k];
+        p.S[o + k] = surv;
       }
     }
   }
@@ -795,9 +985,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __threadfence();
     if (tgt)
       for (int b = ew; b < B; b += kEpiWarps) {
-        float s = 0.f;
-        for (int i = lane; i < nCTA; i += 32) s += p.l1p[((size_t)(G - 1) * B + b) * nCTA + i];
-        s = warp_sum(s);
+        const float s = warp_sum_n(p.l1p + ((size_t)(G - 1) * B + b) * nCTA, nCTA, lane);
         if (lane == 0) {
           const size_t o = (size_t)b * G + G - 1;
           const bool vb = ((volatile int32_t*)p.tokens)[o] >= 0;
