@@ -38,8 +38,8 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: every timed block starts with a cold
 # source file, the sha256 prefix of the source it was measured on, and the bytes.  A workload
 # without a capture, or whose kernel changed since, reports null.
 TRAFFIC = {
-    "qwen3_4b_markov": ("draft_cc.cu", "477d1b6c2463407e", 82730496),          # 80.62 + 2.11 MB
-    "high_concurrency_sched": ("draft_tc.cu", "684388eea4fd34c0", 5693589248),  # 5686 + 7.5 MB
+    "qwen3_4b_markov": ("draft_cc.cu", "e35cee97189b27e2", 82493184),          # 80.62 + 1.87 MB
+    "high_concurrency_sched": ("draft_tc.cu", "4d737546be5bf48d", 5722781952),  # 5715 + 7.4 MB
 }
 
 

@@ -189,6 +189,10 @@ dspark_status run_draft(const DraftArgs& a) {
   p.invT = 1.f / a.T;
   p.seed_lo = (uint32_t)(a.seed & 0xFFFFFFFFu);
   p.seed_hi = (uint32_t)(a.seed >> 32);
+  for (int i = 0; i < 10; ++i) {
+    p.rk0[i] = p.seed_lo + (uint32_t)i * 0x9E3779B9u;
+    p.rk1[i] = p.seed_hi + (uint32_t)i * 0xBB67AE85u;
+  }
   p.w_bf16 = w_bf16;
   p.u_bf16 = u_bf16;
   p.W1 = a.W1;

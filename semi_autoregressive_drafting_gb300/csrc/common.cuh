@@ -17,6 +17,10 @@ constexpr unsigned kOk = 0, kErrInvalid = 1, kErrTimeout = 4;
 
 constexpr uint32_t kNoiseTag = 0x44535052u;  // "DSPR": 4th counter word of the sampling noise
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // one second per wait
+// Longest a thread stays suspended inside one mbarrier try_wait before it re-checks its abort
+// flag and time bound; it resumes as soon as the phase completes, so waiting threads take no
+// issue slots from the warps doing the work.
+constexpr uint32_t kSuspendHintNs = 20000;
 
 // Workspace header (first 256 bytes of every draft workspace).
 struct WsHeader {
@@ -73,8 +77,11 @@ __host__ __device__ __forceinline__ PhiloxFixed philox_fix(uint32_t c1, uint32_t
   f.l2 = (uint32_t)p0;
   return f;
 }
-__host__ __device__ __forceinline__ U4 philox_var(uint32_t c0, const PhiloxFixed& f, uint32_t k0,
-                                                  uint32_t k1) {
+// The varying part, with the round keys given (rk0[i] = k0 + i * 0x9E3779B9, rk1[i] = k1 +
+// i * 0xBB67AE85; e.g. from kernel parameters, so that no key arithmetic runs per call).
+__host__ __device__ __forceinline__ U4 philox_var(uint32_t c0, const PhiloxFixed& f,
+                                                     const uint32_t (&rk0)[10],
+                                                     const uint32_t (&rk1)[10]) {
   const uint64_t p0 = (uint64_t)0xD2511F53u * c0;  // round 1
   const uint32_t w2 = (uint32_t)(p0 >> 32) ^ f.x2;
   const uint64_t p1 = (uint64_t)0xCD9E8D57u * w2;  // round 2
@@ -82,12 +89,11 @@ __host__ __device__ __forceinline__ U4 philox_var(uint32_t c0, const PhiloxFixed
   uint32_t x2 = (uint32_t)p0 ^ f.y2, x3 = f.l2;
 #pragma unroll
   for (int round = 2; round < 10; ++round) {
-    const uint32_t kr0 = k0 + (uint32_t)round * 0x9E3779B9u, kr1 = k1 + (uint32_t)round * 0xBB67AE85u;
     const uint64_t q0 = (uint64_t)0xD2511F53u * x0;
     const uint64_t q1 = (uint64_t)0xCD9E8D57u * x2;
-    x0 = (uint32_t)(q1 >> 32) ^ x1 ^ kr0;
+    x0 = (uint32_t)(q1 >> 32) ^ x1 ^ rk0[round];
     x1 = (uint32_t)q1;
-    x2 = (uint32_t)(q0 >> 32) ^ x3 ^ kr1;
+    x2 = (uint32_t)(q0 >> 32) ^ x3 ^ rk1[round];
     x3 = (uint32_t)q0;
   }
   return U4{x0, x1, x2, x3};
@@ -315,7 +321,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
   bool ok = true;
   if ((threadIdx.x & 31) == 0 && !mbar_try_wait(bar, parity)) {
     const unsigned long long t0 = globaltimer();
-    while (!mbar_try_wait_sleep(bar, parity, 1000)) {
+    while (!mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) {
       if (globaltimer() - t0 > kWaitLimitNs) {
         ok = false;
         break;
@@ -328,7 +334,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) {
     if (globaltimer() - t0 > kWaitLimitNs) return false;
   }
   return true;

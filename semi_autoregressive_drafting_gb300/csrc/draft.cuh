@@ -16,6 +16,7 @@ struct DraftParams {
   int B, gamma, V, r, d;
   float invT;
   uint32_t seed_lo, seed_hi;
+  uint32_t rk0[10], rk1[10];  // Philox round keys: seed_lo + i * 0x9E3779B9, seed_hi + i * 0xBB67AE85
   int w_bf16, u_bf16;  // dtype flags (weights / activations)
   // inputs
   const void* W1;

@@ -27,6 +27,7 @@
 #include <cuda.h>
 
 #include <cstring>
+#include <type_traits>
 
 #include "draft.cuh"
 #include "rnn.cuh"
@@ -59,7 +60,7 @@ struct TMisc {
 };
 
 struct TCLayout {
-  size_t a, ring, ubuf, scratch, rnnbuf, misc, bars, total;
+  size_t a, ring, ubuf, scratch, sbest, rnnbuf, misc, bars, total;
   int nslab, na, nstage, aslabs, nu;
   int abytes;  // bytes of one A slab: 128 rows, or 192 when two vocabulary tiles share a tile
 };
@@ -90,6 +91,8 @@ __host__ __device__ inline TCLayout tc_layout(int r, int na, int nstage, bool rn
   off += (size_t)nu * kUTile;
   L.scratch = off;
   off = align_up_t(off + 4 * kM * sizeof(TSlot), 128);  // partial states of the merge
+  L.sbest = off;  // running best of every (part, request row) during the tiles, [8][kM] floats
+  off = align_up_t(off + 8 * kM * sizeof(float), 128);
   L.rnnbuf = off;  // RNN: e (r), s (r), Wj z (3r) of the request being updated
   off = align_up_t(off + (rnn ? (size_t)5 * r * 4 : 0), 128);
   L.misc = off;
@@ -121,7 +124,7 @@ __device__ __forceinline__ int esync_or(int pred) {
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) {
     if (*abort || globaltimer() - t0 > kWaitLimitNs) return false;
   }
   return true;
@@ -144,6 +147,23 @@ __device__ __forceinline__ void tslot_init(TSlot& s) {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// log2(-ln u) for the Philox word `bits`, u = (2 (bits >> 9) + 1) 2^-24: the Gumbel noise in
+// log2 units is minus this.  t = -ln u = -ln(1 - w) with w = 1 - u (exact) is the series
+// w + w^2/2 + ... + w^5/5 for w <= 1/16 (truncation below w^5/6 = 1.6e-7 relative), else logf;
+// the outer logarithm is lg2.approx (absolute error about 2^-22, below one ulp of a score).
+__device__ __forceinline__ float gumbel_log2(uint32_t bits) {
+  const float u = __uint_as_float(0x3F800000u | (bits >> 9)) - 0.99999994f;  // exact
+  const float w = 1.f - u;                                                    // exact
+  float t;
+  if (w <= 0.0625f)
+    t = w * fmaf(w, fmaf(w, fmaf(w, fmaf(w, 0.2f, 0.25f), 0.33333334f), 0.5f), 1.f);
+  else
+    t = -logf(u);
+  float l2;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(t));
+  return l2;
+}
+
 // 2^x on the special-function unit (relative error about 2^-22; 0 for x = -inf)
 __device__ __forceinline__ float ex2f(float x) {
   float y;
@@ -154,10 +174,11 @@ __device__ __forceinline__ void prefetch_line(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// (max, sum-exp) of all blocks' partials, merged by one warp in a fixed order; each lane
-// issues the loads of up to 8 partials before merging them
+// (max, sum-exp) of all blocks' partials, merged by one warp in a fixed order: each lane issues
+// the loads of up to 8 partials, the warp takes their maximum M, then sums l_i exp(m_i - M)
+// (empty partials are (-inf, 0) and add nothing)
 __device__ __forceinline__ float2 merge_ml(const float2* part, int n, int lane) {
-  float m = -INFINITY, l = 0.f;
+  float M = -INFINITY, L = 0.f;
   for (int i0 = 0; i0 < n; i0 += 256) {
     float2 q[8];
 #pragma unroll
@@ -165,16 +186,19 @@ __device__ __forceinline__ float2 merge_ml(const float2* part, int n, int lane) 
       const int i = i0 + lane + 32 * j;
       q[j] = i < n ? part[i] : make_float2(-INFINITY, 0.f);
     }
+    float mb = fmaxf(fmaxf(fmaxf(q[0].x, q[1].x), fmaxf(q[2].x, q[3].x)),
+                     fmaxf(fmaxf(q[4].x, q[5].x), fmaxf(q[6].x, q[7].x)));
 #pragma unroll
-    for (int j = 0; j < 8; ++j) lse_merge(m, l, q[j].x, q[j].y);
-  }
+    for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    const float Mn = fmaxf(M, mb);  // the same in every lane
+    if (Mn == -INFINITY) continue;
+    float sum = 0.f;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
-    lse_merge(m, l, m2, l2);
+    for (int j = 0; j < 8; ++j) sum += q[j].y * __expf(q[j].x - Mn);
+    L = L * __expf(M - Mn) + sum;
+    M = Mn;
   }
-  return make_float2(m, l);
+  return make_float2(M, warp_sum(L));
 }
 
 // Sum of n floats, one warp, up to 8 loads in flight per lane (fixed order)
@@ -300,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* abuf = smem + Lay.a;
   uint8_t* ring = smem + Lay.ring;
   TSlot* scratch = (TSlot*)(smem + Lay.scratch);
+  volatile float* sbest = (volatile float*)(smem + Lay.sbest);
   TMisc* ms = (TMisc*)(smem + Lay.misc);
   uint64_t* full = (uint64_t*)(smem + Lay.bars);
   uint64_t* empty = full + nstage;
@@ -515,6 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // same requests for the round's second vocabulary tile)
   const int m = pk ? (lrow & 63) : lrow;
   const int half = pk ? (q >> 1) : 0;  // packed: which tile of the round
+  // part of the request's row this thread holds: column quarter, and in packed mode the tile
+  const int kpart = half * 4 + cq, npart = pk ? 8 : 4;
   // gather role: row and the share of the row's 16-byte chunks (packed: 64 rows, 8 shares)
   const int gm = pk ? (et & 63) : (et & (kM - 1)), gh = pk ? (et >> 6) : (et >> 7);
   const int gstep = pk ? 8 : 4;
@@ -537,38 +564,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float* const tgp = p.target;
   float* const lgp = p.logits;
   float* const ybp = p.ybuf;
-  const uint32_t sd0 = p.seed_lo, sd1 = p.seed_hi;
 
   // One group of 8 consecutive vocabulary entries v..v+7 of this thread's row: logits (Eq 4),
   // the online normaliser, Philox Gumbel-max with the exact skip; with a target, its
   // normaliser, and y saved for the Eq 8 second pass.  st.m, st.mt and st.best are in log2
-  // units here.  Skip test: with w = 1 - u (exact) and q = exp(y - best), an entry with
+  // units here; the group's max is taken on z (the scale is positive, and rounding is
+  // monotone, so fl(max z * s2) is the max of fl(z * s2)), and each exponential is one FMA and
+  // one ex2.  Skip test: with w = 1 - u (exact) and q = exp(y - best), an entry with
   // w >= 1.001 q cannot win (-ln u >= w, so its score is below best - 0.0009 in natural units).
   // f = 1 + w - 2^-24 is read straight from the bits, and f >= fl(1 + 1.002 q') (q' = the
   // computed q, within 1e-5 of q) implies w >= 1.002 q' >= 1.001 q, so a skipped entry is one
   // the exact fp32 comparison would also reject.  Cp = 1.002 exp(m - best), q' = pe Cp / 1.002.
-  auto group = [&](int gi, int vb, const uint32_t* bs, const uint8_t* ub, size_t urow, int b,
-                   TSlot& st, float& Cp, const PhiloxFixed& pfx) {
+  // FAST (a compile-time constant at each call): all 8 entries exist, U is staged, no debug
+  // output, and the target (if any) has 16-byte aligned rows.
+  auto group = [&](auto fast_tag, int gi, int vb, const uint32_t* bs, const uint8_t* ub,
+                   size_t urow, int b, TSlot& st, float& tb, float& Cp, const PhiloxFixed& pfx,
+                   volatile float* sb_own) {
+    constexpr bool FAST = decltype(fast_tag)::value;
     const int v = vb + 8 * gi;
-    if (v >= V) return;
-    const bool full = v + 8 <= V;
-    float y[8], tv[8];
+    if (!FAST && v >= V) return;
+    const bool full = FAST || v + 8 <= V;
+    float z[8], tv[8];
     uint4 uq = make_uint4(0, 0, 0, 0);
     bool vq = false;
-    if (nu > 0) {  // staged: 16-byte chunk (cq % 2) * 4 + gi of the row sits at chunk ^ (row % 8)
+    if (FAST || nu > 0) {  // staged: 16-byte chunk (cq % 2) * 4 + gi of the row sits at chunk ^ (row % 8)
       uq = *(const uint4*)(ub + (((((cq & 1) << 2) + gi) ^ (lrow & 7)) << 4));
       vq = true;
     } else if (vec_u && full) {
       uq = __ldcs((const uint4*)((const __nv_bfloat16*)Up + urow + v));
       vq = true;
     }
-    if (vq && full) {
+    if (FAST || (vq && full)) {
       float uf[8];
       bf16x8(uq, uf);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = uf[e] + __uint_as_float(bs[e]);  // z for now
+      for (int e = 0; e < 8; ++e) z[e] = uf[e] + __uint_as_float(bs[e]);
       if (TGT) {
-        if (vec_t) {
+        if (FAST || vec_t) {
           const float4 a = *(const float4*)(tgp + urow + v);
           const float4 c4 = *(const float4*)(tgp + urow + v + 4);
           tv[0] = a.x; tv[1] = a.y; tv[2] = a.z; tv[3] = a.w;
@@ -585,71 +617,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 8; ++e) {
         const int vv = v + e;
         const float uval = vq ? uf[e] : (vv < V ? ld_u(Up, urow + vv, p.u_bf16) : 0.f);
-        y[e] = vv < V ? uval + __uint_as_float(bs[e]) : -INFINITY;
+        z[e] = vv < V ? uval + __uint_as_float(bs[e]) : -INFINITY;
         if (TGT) tv[e] = vv < V ? tgp[urow + vv] : -INFINITY;
       }
     }
-    if (lgp)  // debug output: z
+    if (!FAST && lgp)  // debug output: z
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        if (v + e < V) lgp[urow + v + e] = y[e];
-    float gmax = -INFINITY;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      y[e] *= s2;
-      gmax = fmaxf(gmax, y[e]);
-    }
+        if (v + e < V) lgp[urow + v + e] = z[e];
+    const float gmax = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])),
+                             fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7]))) * s2;
     if (gmax > st.m) {  // rescale the running sum to the new max, once per group
       st.l *= ex2f(st.m - gmax);
       st.m = gmax;
-      Cp = 1.002f * ex2f(st.m - st.best);
+      Cp = 1.002f * ex2f(st.m - tb);
     }
+    const float nm = -st.m;
     uint32_t wd[8];
     {
-      const U4 r0 = philox_var((uint32_t)(v >> 2), pfx, sd0, sd1);
-      const U4 r1 = philox_var((uint32_t)(v >> 2) + 1u, pfx, sd0, sd1);
+      const U4 r0 = philox_var((uint32_t)(v >> 2), pfx, p.rk0, p.rk1);
+      const U4 r1 = philox_var((uint32_t)(v >> 2) + 1u, pfx, p.rk0, p.rk1);
       wd[0] = r0.x; wd[1] = r0.y; wd[2] = r0.z; wd[3] = r0.w;
       wd[4] = r1.x; wd[5] = r1.y; wd[6] = r1.z; wd[7] = r1.w;
     }
     float ls0 = 0.f, ls1 = 0.f;
-    bool any = false;
+    uint32_t mask = 0;  // entries that might beat the running best
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const float pe = ex2f(y[e] - st.m);
+      const float pe = ex2f(fmaf(z[e], s2, nm));
       if (e & 1) ls1 += pe; else ls0 += pe;
       const float f = __uint_as_float(0x3F800000u | (~wd[e] >> 9));
-      any |= f < fmaf(pe, Cp, 1.f);
+      if (f < fmaf(pe, Cp, 1.f)) mask |= 1u << e;
     }
     st.l += ls0 + ls1;
-    if (any) {  // rare: the candidates in order (ties keep the smaller entry), one copy of
-                // the logarithms for all of them to keep the loop's code small
-      uint32_t mask = 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float pe = ex2f(y[e] - st.m);
-        const float f = __uint_as_float(0x3F800000u | (~wd[e] >> 9));
-        mask |= (f < fmaf(pe, Cp, 1.f)) ? (1u << e) : 0u;
-      }
+    if (mask) {  // the candidates in order (ties keep the smaller entry); the lanes of a warp
+                 // hold different requests, so this runs whenever any lane has one
       while (mask) {
         const int e = __ffs(mask) - 1;
         mask &= mask - 1;
-        float ye = y[0];
+        float ze = z[0];
         uint32_t we = wd[0];
 #pragma unroll
         for (int j = 1; j < 8; ++j)
           if (e == j) {
-            ye = y[j];
+            ze = z[j];
             we = wd[j];
           }
-        // u = (2 (bits >> 9) + 1) 2^-24, exactly; Gumbel noise in log2 units: -log2(-ln u)
-        const float u = __uint_as_float(0x3F800000u | (we >> 9)) - 0.99999994f;
-        const float sc = ye - log2f(-logf(u));
+        const float sc = ze * s2 - gumbel_log2(we);
         if (sc > st.best) {
           st.best = sc;
           st.tok = (uint32_t)(v + e);
         }
       }
-      Cp = 1.002f * ex2f(st.m - st.best);
+      *sb_own = st.best;
+      tb = fmaxf(tb, st.best);
+      Cp = 1.002f * ex2f(st.m - tb);
     }
     if (TGT) {
       float tmax = -INFINITY;
@@ -668,14 +690,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (e & 1) a1 += ex2f(tv[e] - st.mt); else a0 += ex2f(tv[e] - st.mt);
       }
       st.lt += a0 + a1;
-      float* yo = ybp + (size_t)b * V + v;  // y2, read back by the second pass
-      if (vec_t && full) {
-        *(float4*)yo = make_float4(y[0], y[1], y[2], y[3]);
-        *(float4*)(yo + 4) = make_float4(y[4], y[5], y[6], y[7]);
+      float* yo = ybp + (size_t)b * V + v;  // y2 = z s2, read back by the second pass
+      if (FAST || (vec_t && full)) {
+        *(float4*)yo = make_float4(z[0] * s2, z[1] * s2, z[2] * s2, z[3] * s2);
+        *(float4*)(yo + 4) = make_float4(z[4] * s2, z[5] * s2, z[6] * s2, z[7] * s2);
       } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          if (v + e < V) yo[e] = y[e];
+          if (v + e < V) yo[e] = z[e] * s2;
       }
     }
   };
@@ -793,6 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         failed = true;
         break;
       }
+      sbest[kpart * kM + m] = -INFINITY;  // no best known yet for this chunk and step
       fence_proxy_async_smem();
       esync<kEpiThreads>();
       if (et == 0) mbar_arrive(&a_full[ab]);
@@ -807,10 +830,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = c * kM + m;
       const bool row_ok = b < B;
       const size_t urow = ((size_t)b * G + ks) * V;
-      const PhiloxFixed pfx = philox_fix((uint32_t)ks, (uint32_t)b, kNoiseTag, sd0, sd1);
+      const PhiloxFixed pfx = philox_fix((uint32_t)ks, (uint32_t)b, kNoiseTag, p.seed_lo, p.seed_hi);
       TSlot st;
       tslot_init(st);
-      float Cp = INFINITY;           // 1.002 exp(m - best) of this thread's running state
+      // The skip threshold uses tb, the best score known for this request in the block: this
+      // thread's own and the other parts' (the 4 column quarters, and in packed mode the two
+      // tiles of a round, hold the same requests), published in shared memory.  An entry
+      // skipped against another part's score is below a score that part has evaluated, so it
+      // cannot win; a stale (smaller) value only skips less.
+      float tb = -INFINITY;
+      float Cp = INFINITY;           // 1.002 exp(m - tb)
+      volatile float* const sb_own = sbest + kpart * kM + m;
       const int tstep = pk ? 2 : 1;  // this warp's tile advances by tstep per round
       for (int rd = 0; rd < nround; ++rd, ++acc_i) {
         const int acc = acc_i % kAcc;
@@ -841,15 +871,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_after_sync();
         const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + acc * kNT + cq * 32;
-        const bool act = row_ok && tile_ok;
-        // one 8-column TMEM load (the whole warp) per 8-entry group; the loop stays rolled to
-        // keep the code small
+        if (row_ok) {  // the other parts' bests for this request
+          float ob = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i < npart && i != kpart) ob = fmaxf(ob, sbest[i * kM + m]);
+          if (ob > tb) {
+            tb = ob;
+            Cp = 1.002f * ex2f(st.m - tb);
+          }
+        }
+        // one 8-column TMEM load (the whole warp) per 8-entry group; the loops stay rolled to
+        // keep the code small.  Whole staged tiles without debug output take the fast group
+        // (the condition is the same for every lane of the warp).
+        if (tile_ok && nu > 0 && lgp == nullptr && vb + 32 <= V && (!TGT || vec_t)) {
 #pragma unroll 1
-        for (int gi = 0; gi < 4; ++gi) {
-          uint32_t bias[8];
-          __syncwarp();
-          tc::tmem_ld8_wait(tcol + 8 * gi, bias);
-          if (act) group(gi, vb, bias, ub, urow, b, st, Cp, pfx);
+          for (int gi = 0; gi < 4; ++gi) {
+            uint32_t bias[8];
+            __syncwarp();
+            tc::tmem_ld8_wait(tcol + 8 * gi, bias);
+            if (row_ok) group(std::true_type{}, gi, vb, bias, ub, urow, b, st, tb, Cp, pfx, sb_own);
+          }
+        } else {
+#pragma unroll 1
+          for (int gi = 0; gi < 4; ++gi) {
+            uint32_t bias[8];
+            __syncwarp();
+            tc::tmem_ld8_wait(tcol + 8 * gi, bias);
+            if (row_ok && tile_ok) group(std::false_type{}, gi, vb, bias, ub, urow, b, st, tb, Cp, pfx, sb_own);
+          }
         }
         tc::fence_before_sync();
         __syncwarp();
@@ -868,7 +918,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       st.mt *= kLn2;
       // ---- merge each request's partial states (column quarters; packed: also the two tiles
       // of each round) in a fixed order, publish the candidate
-      const int kpart = half * 4 + cq, npart = pk ? 8 : 4, pstride = pk ? 64 : kM;
+      const int pstride = pk ? 64 : kM;
       if (kpart > 0) scratch[(kpart - 1) * pstride + m] = st;
       esync<kEpiThreads>();
       if (kpart == 0 && row_ok) {
