@@ -11,7 +11,8 @@
 //   [P2] "DSpark: 既要猜得连贯，也要把验证算力花在刀刃上", "设计" (scheduler prose), "Results".
 //   [P3] "DSpark: Wait It's All Autoregressive?", "A parallel backbone with autoregressive
 //        sampling" and "How the Markov sampler works".
-//   [P4] "Phase-Conditioned Speculative Decoding", sections 3 and 6 (Eq 7, Eq 8, Theta = tau*SPS).
+//   [P4] "Phase-Conditioned Speculative Decoding", sections 3 and 6 (Eq 7, Eq 8, Theta = tau*SPS),
+//        and its reference to Leviathan, Kalman, Matias (ICML 2023) for the accept/reject rule.
 //
 // Readings taken where the pages are silent (each is listed in the design notes):
 //   * Temperature: p_k = softmax((U_k + B_k) / T); Eq 4 itself has no temperature.
@@ -27,6 +28,14 @@
 //   * Eq 7 has no bias; w[0:d] multiplies h_k and w[d:d+r] multiplies W1[x_{k-1}], also for
 //     the RNN head.
 //   * Eq 8 is clamped to [0, 1] (delta table D7); the target distribution uses the same T.
+//   * Verify (the standard speculative accept/reject rule that [P4 s3] equates with Eq 8, and the
+//     round [P2 "Why DSpark?"] describes: accept the matching prefix, stop at the first
+//     rejection; accepted length counts the target's bonus token [P2 "Results"]): position j
+//     (0-based) accepts x_j iff ln a_j < ln q_j(x_j) - ln p_j(x_j), with a_j = word 0 of Philox
+//     counter (0, j, b, 0x41434350) as above; at the first rejection j the correction is a
+//     Gumbel-max sample of max(0, q_j - p_j) (of q_j if that is zero everywhere), and after
+//     gamma acceptances the bonus is a Gumbel-max sample of q_gamma; both draw u_v from Philox
+//     counter (floor(v/4), j, b, 0x52455344).
 //   * Scheduler (Algorithm 1 is named, not printed): choose per-request verify lengths l_b in
 //     0..gamma maximising Theta = SPS(n) * sum_b (1 + sum_{k<=l_b} S_{b,k}) with
 //     n = sum_b (l_b + 1); only contiguous prefixes are legal; ties go to fewer tokens.
@@ -101,6 +110,18 @@ double uniform(uint64_t seed, int b, int k, int64_t v) {
 
 double gumbel(uint64_t seed, int b, int k, int64_t v) {
   return -std::log(-std::log(uniform(seed, b, k, v)));
+}
+
+const uint32_t kAcceptTag = 0x41434350u;    // "ACCP": acceptance uniforms of the verify rule
+const uint32_t kResidualTag = 0x52455344u;  // "RESD": noise of the correction / bonus sample
+
+// (2 * (bits >> 9) + 1) * 2^-24 for word `lane` of Philox(counter, key(seed)).
+double uniform_ctr(uint64_t seed, uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, int lane) {
+  const uint32_t ctr[4] = {c0, c1, c2, c3};
+  const uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  philox4x32_10(ctr, key, out);
+  return (2.0 * (double)(out[lane] >> 9) + 1.0) * std::ldexp(1.0, -24);
 }
 
 double sigmoid(double x) { return 1.0 / (1.0 + std::exp(-x)); }
@@ -291,6 +312,99 @@ void orc_tv_label(int N, int V, double T, const float* draft, const float* targe
     }
     tv_label_row(y, tau, &cstar[i], &l1[i]);
   }
+}
+
+// Speculative verification of one draft block per request: the standard accept/reject rule
+// [P4 s3: c* = 1 - TV is its single-step acceptance probability; P2 "Why DSpark?": the
+// matching prefix is accepted and the round stops at the first rejection; P2 "Results": the
+// target contributes a bonus token].  For request b, with p_j = softmax(zd[b][j] / T) (draft,
+// j = 0..gamma-1) and q_j = softmax(zt[b][j] / T) (target, j = 0..gamma):
+//   for j = 0, 1, ...: accept x_j = tok[b][j] iff ln a_j < ln q_j(x_j) - ln p_j(x_j)
+//   (a_j uniform, i.e. with probability min(1, q_j(x_j) / p_j(x_j)));
+//   at the first rejection j: n = j, and the correction is drawn from max(0, q_j - p_j)
+//   (normalised; from q_j when that is zero everywhere);
+//   if all gamma are accepted: n = gamma, and the bonus is drawn from q_gamma.
+// Both draws are Gumbel-max: argmax_v (ln w_v + g_v) over the entries with w_v > 0, ties to the
+// smaller v.  Outputs: n_acc[b] = n; out[b][0..n-1] = the accepted tokens, out[b][n] = the
+// correction or bonus, out[b][n+1..gamma] = -1.  margin[b][j] = (ln q - ln p)(x_j) - ln a_j for
+// the positions tested (NaN after n); best/best2/tok2 are the winning and runner-up perturbed
+// scores of the draw and the runner-up's id.  Returns 1 (and n_acc = -1) for a request with a
+// drafted token outside [0, V).
+int orc_verify(int B, int gamma, int V, double T, uint64_t seed, const float* zd,
+               const float* zt, const int32_t* tok, int32_t* n_acc, int32_t* out,
+               double* margin, double* best, double* best2, int32_t* tok2, int nthreads) {
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
+  for (int b = 0; b < B; ++b) {
+    std::vector<double> y(V), tau(V), w(V);
+    for (int j = 0; j <= gamma; ++j) out[(size_t)b * (gamma + 1) + j] = -1;
+    for (int j = 0; j < gamma; ++j) margin[(size_t)b * gamma + j] = NAN;
+    bool ok = true;
+    for (int j = 0; j < gamma; ++j) ok = ok && tok[(size_t)b * gamma + j] >= 0 && tok[(size_t)b * gamma + j] < V;
+    if (!ok) {
+      bad = 1;
+      n_acc[b] = -1;
+      best[b] = best2[b] = NAN;
+      tok2[b] = -1;
+      continue;
+    }
+    int n = gamma;
+    for (int j = 0; j < gamma; ++j) {
+      const size_t dj = ((size_t)b * gamma + j) * V, tj = ((size_t)b * (gamma + 1) + j) * V;
+      for (int v = 0; v < V; ++v) {
+        y[v] = (double)zd[dj + v] / T;
+        tau[v] = (double)zt[tj + v] / T;
+      }
+      const double Ld = logsumexp(y), Lt = logsumexp(tau);
+      const int x = tok[(size_t)b * gamma + j];
+      const double log_ratio = (tau[x] - Lt) - (y[x] - Ld);  // ln q_j(x) - ln p_j(x)
+      const double a = uniform_ctr(seed, 0u, (uint32_t)j, (uint32_t)b, kAcceptTag, 0);
+      margin[(size_t)b * gamma + j] = log_ratio - std::log(a);
+      out[(size_t)b * (gamma + 1) + j] = x;
+      if (!(std::log(a) < log_ratio)) {  // rejected: the correction replaces x_j
+        n = j;
+        bool any = false;
+        for (int v = 0; v < V; ++v) {
+          w[v] = std::max(0.0, std::exp(tau[v] - Lt) - std::exp(y[v] - Ld));
+          any = any || w[v] > 0.0;
+        }
+        if (!any)
+          for (int v = 0; v < V; ++v) w[v] = std::exp(tau[v] - Lt);
+        break;
+      }
+    }
+    if (n == gamma) {  // every drafted token accepted: the bonus from q_gamma
+      const size_t tj = ((size_t)b * (gamma + 1) + gamma) * V;
+      for (int v = 0; v < V; ++v) tau[v] = (double)zt[tj + v] / T;
+      const double Lt = logsumexp(tau);
+      for (int v = 0; v < V; ++v) w[v] = std::exp(tau[v] - Lt);
+    }
+    int t1 = -1, t2 = -1;
+    double s1 = -INFINITY, s2 = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+      if (!(w[v] > 0.0)) continue;
+      const double u = uniform_ctr(seed, (uint32_t)(v >> 2), (uint32_t)n, (uint32_t)b, kResidualTag, v & 3);
+      const double sc = std::log(w[v]) - std::log(-std::log(u));
+      if (sc > s1) {
+        t2 = t1;
+        s2 = s1;
+        t1 = v;
+        s1 = sc;
+      } else if (sc > s2) {
+        t2 = v;
+        s2 = sc;
+      }
+    }
+    n_acc[b] = n;
+    out[(size_t)b * (gamma + 1) + n] = t1;
+    best[b] = s1;
+    best2[b] = s2;
+    tok2[b] = t2;
+  }
+  return bad;
 }
 
 // Hardware-aware prefix scheduler [P2 "设计"; P4 s3 Theta = tau * SPS(B)].  Choose l_b in

@@ -60,6 +60,8 @@ def _load():
         lib.orc_confidence.restype = I
         lib.orc_tv_label.argtypes = [I, I, ctypes.c_double, P, P, P, P, I]
         lib.orc_tv_label.restype = None
+        lib.orc_verify.argtypes = [I, I, I, ctypes.c_double, ctypes.c_uint64] + [P] * 9 + [I]
+        lib.orc_verify.restype = I
         lib.orc_prefix_schedule.argtypes = [I, I, P, P, P, P]
         lib.orc_prefix_schedule.restype = I
         _lib = lib
@@ -189,3 +191,38 @@ def prefix_schedule(S, sps):
     theta = np.zeros(1, dtype=np.float64)
     st = _load().orc_prefix_schedule(B, gamma, _ptr(S), _ptr(sps), _ptr(ln), _ptr(theta))
     return ln, float(theta[0]), st
+
+
+@dataclass
+class VerifyResult:
+    n_accepted: np.ndarray  # [B] int32, -1 for a request with an invalid drafted token
+    tokens: np.ndarray      # [B, gamma + 1] accepted prefix, then the correction or bonus; -1 after
+    margin: np.ndarray      # [B, gamma] (ln q - ln p)(x_j) - ln a_j where tested, NaN after
+    best: np.ndarray        # [B] winning perturbed score of the correction / bonus draw
+    best2: np.ndarray       # [B] runner-up score
+    tokens2: np.ndarray     # [B] runner-up id
+    status: int
+
+
+def verify(*, gamma: int, T: float, seed: int, draft_logits, target_logits, draft_tokens,
+           nthreads: int = 0) -> VerifyResult:
+    """The speculative accept/reject rule on one draft block per request.
+
+    ``draft_logits`` is float32 [B, gamma, V], ``target_logits`` float32 [B, gamma + 1, V],
+    ``draft_tokens`` int32 [B, gamma].
+    """
+    zd = _c(draft_logits, np.float32)
+    zt = _c(target_logits, np.float32)
+    x = _c(draft_tokens, np.int32)
+    B, g, V = zd.shape
+    if g != gamma or zt.shape != (B, gamma + 1, V) or x.shape != (B, gamma):
+        raise ValueError("shapes: draft [B, gamma, V], target [B, gamma + 1, V], tokens [B, gamma]")
+    n = np.zeros(B, dtype=np.int32)
+    out = np.zeros((B, gamma + 1), dtype=np.int32)
+    margin = np.zeros((B, gamma), dtype=np.float64)
+    best = np.zeros(B, dtype=np.float64)
+    best2 = np.zeros(B, dtype=np.float64)
+    tok2 = np.zeros(B, dtype=np.int32)
+    st = _load().orc_verify(B, gamma, V, float(T), seed, _ptr(zd), _ptr(zt), _ptr(x), _ptr(n),
+                            _ptr(out), _ptr(margin), _ptr(best), _ptr(best2), _ptr(tok2), nthreads)
+    return VerifyResult(n, out, margin, best, best2, tok2, st)
