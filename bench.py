@@ -40,6 +40,8 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: every timed block starts with a cold
 TRAFFIC = {
     "qwen3_4b_markov": ("draft_cc.cu", "e35cee97189b27e2", 82493184),          # 80.62 + 1.87 MB
     "high_concurrency_sched": ("draft_tc.cu", "4d737546be5bf48d", 5722781952),  # 5715 + 7.4 MB
+    # the three verify kernels of one call (bench.py --op verify)
+    "verify qwen3_8b_labels": ("verify.cu", "256b8f8a4f1f9538", 659341312),
 }
 
 
@@ -186,6 +188,122 @@ def cpu_baseline(wl, seconds: float = 15.0):
     return {"value": wl.B * n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{n} draft positions x B={wl.B} over the full vocabulary ({dt:.1f} s)"}
 
+VERIFY_METRIC = "verified draft blocks/sec (B per call) and achieved HBM GB/s vs roofline, 1 GB300"
+
+
+def run_verify(args, wl, rank, world, local_rank):
+    """The speculative verify step on fp32 draft and target logits of the workload's shape."""
+    import torch
+
+    import semi_autoregressive_drafting_gb300 as ds
+    from semi_autoregressive_drafting_gb300 import inputs
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    B, G, V = wl.B, wl.gamma, wl.V
+    host = inputs.verify_inputs(B, G, V, seed=wl.seed + 100 * rank, tokens="argmax")
+    dev = {k: v.cuda() for k, v in host.items()}
+    ws = ds.VerifyWorkspace(B, G, V)
+    n = torch.empty(B, dtype=torch.int32, device="cuda")
+    toks = torch.empty(B, G + 1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def call(d):
+        ds.verify(d["draft_logits"], d["target_logits"], d["draft_tokens"], T=wl.T, seed=wl.seed,
+                  workspace=ws, stream=stream, out=(n, toks))
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call(dev)
+    torch.cuda.synchronize()
+    assert ws.status() == 0, "verify reported a device error during warm-up"
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            call(dev)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    times = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(times) / len(times)
+    assert ws.status() == 0, "verify reported a device error"
+    # end to end: the logits and tokens copied in from pinned host memory, results copied out
+    hin = {k: v.pin_memory() for k, v in host.items()}
+    din = {k: torch.empty_like(v) for k, v in dev.items()}
+    hn = torch.empty(B, dtype=torch.int32).pin_memory()
+    ht = torch.empty(B, G + 1, dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    d2h = hn.numel() * 4 + ht.numel() * 4
+
+    def e2e_step():
+        for k in din:
+            din[k].copy_(hin[k], non_blocking=True)
+        call(din)
+        hn.copy_(n, non_blocking=True)
+        ht.copy_(toks, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = min(args.steps, 50)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for _ in range(e2e_steps):
+        flush.zero_()
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_ms /= e2e_steps
+    if dist:
+        tt = torch.tensor([ms, e2e_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = tt.tolist()
+    if rank == 0:
+        peak, peak_kind = load_peaks()
+        # what the step must move: every draft row and every target row once (the
+        # normalisers), and the one drawn row per request (draft and target) again
+        alg = (B * G * V + B * (G + 1) * V) * 4 + B * 2 * V * 4 + B * G * 4
+        achieved = alg / (ms * 1e-3) / 1e9
+        cap = TRAFFIC.get("verify " + wl.name)
+        src = cap and os.path.join(ROOT, "semi_autoregressive_drafting_gb300", "csrc", cap[0])
+        traffic = cap[2] if cap and _sha(src) == cap[1] else None
+        line = {
+            "metric": VERIFY_METRIC, "value": world * B / (ms * 1e-3), "unit": "blocks/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": f"verify {wl.name}", "B": B, "gamma": G, "V": V, "T": wl.T,
+                       "tokens": "largest draft logit per position",
+                       "l2": "flushed between timed calls (512 MB write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_kind": f"{peak_kind} copy bandwidth",
+                         "algorithmic_bytes_per_launch": alg,
+                         "kernel": "verify_part_kernel + verify_decide_kernel + verify_draw_kernel"},
+            "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": "blocks/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk.summary(),
+            "ms_per_step_min": min(times), "ms_per_step_median": statistics.median(times),
+            "accepted_mean": float(n.float().mean()),
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -195,6 +313,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_4b_markov")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["draft", "verify"], default="draft",
+                    help="draft: the draft block (default); verify: the speculative accept/reject "
+                         "step on the workload's B, gamma, V")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -208,6 +329,9 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args, wl)
+        return
+    if args.op == "verify":
+        run_verify(args, wl, rank, world, local_rank)
         return
 
     import torch

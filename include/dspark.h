@@ -167,6 +167,38 @@ dspark_status dspark_prefix_schedule(int B, int gamma, const float* S, const dou
                                      int32_t* len, double* theta, void* stream);
 
 /*
+ * Speculative verification of one draft block per request: the standard accept/reject rule,
+ * whose single-step acceptance probability is Eq 8's c* [P4 s3; Leviathan, Kalman, Matias,
+ * ICML 2023], with the round [P2 "Why DSpark?"] stopping at the first rejection and the target
+ * adding a bonus token [P2 "Results"].  For request b, p_j = softmax(draft_logits[b][j] / T),
+ * q_j = softmax(target_logits[b][j] / T):
+ *   position j = 0, 1, ... accepts draft_tokens[b][j] iff ln a_j < ln q_j(x_j) - ln p_j(x_j)
+ *   (probability min(1, q_j(x_j) / p_j(x_j))); at the first rejection j the correction is a
+ *   Gumbel-max draw from max(0, q_j - p_j) (from q_j if that is zero everywhere); after gamma
+ *   acceptances the bonus is a draw from q_gamma.
+ *   a_j: word 0 of Philox4x32-10 at counter (0, j, b, 0x41434350) with the sampler's key and
+ *   uniform; the draw's noise for entry v: word v mod 4 at counter (v / 4, j, b, 0x52455344).
+ *   Draws are Gumbel-max in fp32 (ties to the smaller entry), like the draft sampler.
+ * Arguments (device pointers, row-major, caller-owned):
+ *   draft_logits   [B][gamma][V] fp32 draft logits z (the draft call's `logits` output)
+ *   target_logits  [B][gamma+1][V] fp32 target logits; row gamma feeds the bonus
+ *   draft_tokens   [B][gamma] int32
+ *   n_accepted     [B] int32 out: accepted drafted tokens, 0..gamma (-1 for an invalid request)
+ *   out_tokens     [B][gamma+1] int32 out: the accepted prefix, then the correction or bonus,
+ *                  then -1
+ *   workspace      dspark_verify_workspace_bytes(B, gamma, V) bytes, 256-byte aligned, zeroed
+ *                  once before the first call; every call leaves it ready for the next
+ * Limits: 1 <= gamma <= 16, 2 <= V <= 2^24, T finite and > 0.  Three launches on `stream`.
+ * A drafted token outside [0, V) gives that request n_accepted = -1 and out_tokens -1, and sets
+ * DSPARK_ERR_INVALID in the workspace status (read with dspark_get_status).
+ */
+size_t dspark_verify_workspace_bytes(int B, int gamma, int V);
+dspark_status dspark_verify(int B, int gamma, int V, float T, uint64_t seed,
+                            const float* draft_logits, const float* target_logits,
+                            const int32_t* draft_tokens, int32_t* n_accepted, int32_t* out_tokens,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * The Markov draft of dspark_markov_draft for callers that cannot allocate device memory.  The
  * paper has no counterpart: this is a deployment variant of the same computation.  Callers such
  * as plugins inside another framework's memory pool, serving engines that forbid allocation on

@@ -19,7 +19,8 @@ import torch
 from . import _lib
 
 __all__ = ["Workspace", "markov_draft", "rnn_draft", "confidence", "tv_label",
-           "prefix_schedule", "draft_path", "draft_launches", "DraftOutput", "DraftPlan"]
+           "prefix_schedule", "draft_path", "draft_launches", "DraftOutput", "DraftPlan",
+           "VerifyWorkspace", "verify"]
 
 _F32, _BF16 = 0, 1
 
@@ -204,6 +205,43 @@ def prefix_schedule(S, sps, *, stream=None):
                                       _stream(stream))
     _lib.check(code, "dspark_prefix_schedule")
     return ln, theta
+
+
+class VerifyWorkspace(Workspace):
+    """Zero-initialised device scratch for ``verify`` (shapes up to B, gamma, V)."""
+
+    def __init__(self, B: int, gamma: int, V: int, device=None):
+        n = _lib.load().dspark_verify_workspace_bytes(B, gamma, V)
+        if n == 0:
+            raise ValueError("invalid verify shape for a workspace")
+        self.nbytes = int(n)
+        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def verify(draft_logits, target_logits, draft_tokens, *, T=1.0, seed=0, workspace=None,
+           stream=None, out=None):
+    """Speculative accept/reject of one draft block per request.  See ``dspark_verify``.
+
+    draft_logits [B, gamma, V] fp32, target_logits [B, gamma + 1, V] fp32, draft_tokens
+    [B, gamma] int32.  Returns (n_accepted [B] int32, out_tokens [B, gamma + 1] int32).
+    """
+    lib = _lib.load()
+    B, gamma, V = draft_logits.shape
+    if draft_logits.dtype != torch.float32 or target_logits.dtype != torch.float32:
+        raise TypeError("verify takes fp32 logits")
+    if tuple(target_logits.shape) != (B, gamma + 1, V) or tuple(draft_tokens.shape) != (B, gamma):
+        raise ValueError("target_logits must be [B, gamma + 1, V] and draft_tokens [B, gamma]")
+    ws = workspace or VerifyWorkspace(B, gamma, V, device=draft_logits.device)
+    if out is None:
+        n = torch.empty(B, dtype=torch.int32, device=draft_logits.device)
+        toks = torch.empty(B, gamma + 1, dtype=torch.int32, device=draft_logits.device)
+    else:
+        n, toks = out
+    code = lib.dspark_verify(B, gamma, V, float(T), int(seed) & (2**64 - 1), _ptr(draft_logits),
+                             _ptr(target_logits), _ptr(draft_tokens), _ptr(n), _ptr(toks),
+                             ws.buf.data_ptr(), ws.nbytes, _stream(stream))
+    _lib.check(code, "dspark_verify")
+    return n, toks
 
 
 def draft_path(head: int, B: int, V: int, r: int, bf16: bool = True) -> int:

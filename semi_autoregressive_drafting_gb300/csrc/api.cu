@@ -340,6 +340,31 @@ dspark_status dspark_prefix_schedule(int B, int gamma, const float* S, const dou
   return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "prefix_schedule launch");
 }
 
+size_t dspark_verify_workspace_bytes(int B, int gamma, int V) {
+  if (B < 1 || gamma < 1 || gamma > 16 || V < 2 || V > (1 << 24)) return 0;
+  return verify_workspace_bytes(B, gamma, V);
+}
+
+dspark_status dspark_verify(int B, int gamma, int V, float T, uint64_t seed,
+                            const float* draft_logits, const float* target_logits,
+                            const int32_t* draft_tokens, int32_t* n_accepted, int32_t* out_tokens,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  g_err.clear();
+  if (B < 1 || B > (1 << 20) || gamma < 1 || gamma > 16 || V < 2 || V > (1 << 24))
+    return fail(DSPARK_ERR_INVALID, "bad shape B=%d gamma=%d V=%d", B, gamma, V);
+  if (!(T > 0.f) || !std::isfinite(T)) return fail(DSPARK_ERR_INVALID, "T must be finite and > 0");
+  if (!draft_logits || !target_logits || !draft_tokens || !n_accepted || !out_tokens)
+    return fail(DSPARK_ERR_INVALID, "all arrays are required");
+  if (!aligned(draft_logits, 16) || !aligned(target_logits, 16))
+    return fail(DSPARK_ERR_INVALID, "draft_logits and target_logits must be 16-byte aligned");
+  const size_t need = verify_workspace_bytes(B, gamma, V);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    return fail(DSPARK_ERR_WORKSPACE, "workspace must be 256-byte aligned and >= %zu bytes", need);
+  cudaError_t e = launch_verify(B, gamma, V, T, seed, draft_logits, target_logits, draft_tokens,
+                                n_accepted, out_tokens, workspace, (cudaStream_t)stream);
+  return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "verify launch");
+}
+
 dspark_status dspark_get_status(void* workspace, size_t workspace_bytes, void* stream) {
   g_err.clear();
   if (!workspace || workspace_bytes < sizeof(WsHeader))

@@ -11,6 +11,10 @@ cudaError_t launch_confidence(int B, int G, int V, int r, int d, int w_bf16, con
                               const int32_t* tokens, float* c, float* S, cudaStream_t stream);
 cudaError_t launch_tv_label(int N, int V, float T, const float* d, const float* t, float* cstar,
                             float* l1, cudaStream_t stream);
+size_t verify_workspace_bytes(int B, int G, int V);
+cudaError_t launch_verify(int B, int G, int V, float T, uint64_t seed, const float* zd,
+                          const float* zt, const int32_t* tok, int32_t* n_acc, int32_t* out,
+                          void* workspace, cudaStream_t stream);
 cudaError_t launch_prefix_schedule(int B, int G, const float* S, const double* sps, int32_t* len,
                                    double* theta, cudaStream_t stream);
 

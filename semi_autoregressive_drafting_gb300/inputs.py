@@ -112,3 +112,24 @@ def to_oracle(x: torch.Tensor | None):
     if x.dtype == torch.bfloat16:
         return x.view(torch.int16).numpy().view(np.uint16)
     return x.numpy()
+
+
+def verify_inputs(B: int, gamma: int, V: int, *, seed: int, logit_std: float = 3.0,
+                  target_noise: float = 1.0, tokens: str = "uniform") -> dict:
+    """Host tensors for the verify step: draft logits [B, gamma, V] ~ N(0, logit_std^2) fp32,
+    target logits [B, gamma + 1, V] fp32 (the first gamma rows = draft + N(0, target_noise^2),
+    the bonus row ~ N(0, logit_std^2)), and drafted tokens [B, gamma] int32: uniform in [0, V)
+    ("uniform") or each row's largest draft logit ("argmax", a high-acceptance stand-in)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    zd = _randn(g, (B, gamma, V), logit_std, torch.float32)
+    zt = torch.empty(B, gamma + 1, V, dtype=torch.float32)
+    zt[:, :gamma] = zd + _randn(g, (B, gamma, V), target_noise, torch.float32)
+    zt[:, gamma] = _randn(g, (B, V), logit_std, torch.float32)
+    if tokens == "uniform":
+        x = torch.randint(0, V, (B, gamma), generator=g, dtype=torch.int32)
+    elif tokens == "argmax":
+        x = zd.argmax(dim=2).to(torch.int32)
+    else:
+        raise ValueError(tokens)
+    return {"draft_logits": zd, "target_logits": zt.contiguous(), "draft_tokens": x}
