@@ -36,6 +36,10 @@
 //     Gumbel-max sample of max(0, q_j - p_j) (of q_j if that is zero everywhere), and after
 //     gamma acceptances the bonus is a Gumbel-max sample of q_gamma; both draw u_v from Philox
 //     counter (floor(v/4), j, b, 0x52455344).
+//   * Training losses (Eqs 9-12 [P1 s1]): p_k = softmax(zd_k / T), q_k = softmax(zt_k / T),
+//     w_k = exp(-(k-1)/gamma); c*_k (Eq 8) is a label in L_conf: no gradient flows through it,
+//     and the target logits are frozen [P1 s1, "the target is frozen throughout"].  The losses
+//     are sums over positions (no division by sum w_k).
 //   * Scheduler (Algorithm 1 is named, not printed): choose per-request verify lengths l_b in
 //     0..gamma maximising Theta = SPS(n) * sum_b (1 + sum_{k<=l_b} S_{b,k}) with
 //     n = sum_b (l_b + 1); only contiguous prefixes are legal; ties go to fewer tokens.
@@ -403,6 +407,86 @@ int orc_verify(int B, int gamma, int V, double T, uint64_t seed, const float* zd
     best[b] = s1;
     best2[b] = s2;
     tok2[b] = t2;
+  }
+  return bad;
+}
+
+// Training losses of one draft block per request [P1 s1 Eqs 9-12; delta table D3-D7].  For
+// request b and k = 1..gamma (row j = k - 1), p_k = softmax(zd[b][j] / T) (draft),
+// q_k = softmax(zt[b][j] / T) (frozen target), x*_k = labels[b][j], c_k = sigmoid(conf[b][j]):
+//   w_k    = exp(-(k - 1) / gamma)
+//   L_ce   = -sum_k w_k ln p_k(x*_k)                                             (Eq 9)
+//   L_tv   =  sum_k w_k ||p_k - q_k||_1                                           (Eq 10)
+//   c*_k   =  clamp(1 - 1/2 ||p_k - q_k||_1, 0, 1)                                (Eq 8)
+//   L_conf = -sum_k w_k [c*_k ln c_k + (1 - c*_k) ln(1 - c_k)]                    (Eq 11)
+//   L      =  a_ce L_ce + a_tv L_tv + a_conf L_conf                               (Eq 12)
+// and the gradients with c* held as a label:
+//   dL/dzd[b][j][v] = (w_k / T) (a_ce (p_v - [v == x*]) + a_tv p_v (s_v - sum_u s_u p_u)),
+//                     s_u = sign(p_u - q_u) (0 where they are equal)
+//   dL/dconf[b][j]  = a_conf w_k (c_k - c*_k).
+// loss[b] = L; parts[b] = (L_ce, L_tv, L_conf); grad_z [B][gamma][V] and grad_c [B][gamma] may
+// be NULL.  Returns 1 (and NaN outputs for that request) when a label lies outside [0, V).
+int orc_draft_loss(int B, int gamma, int V, double T, const float* zd, const float* zt,
+                   const int32_t* labels, const float* conf, double a_ce, double a_tv,
+                   double a_conf, double* loss, double* parts, double* grad_z, double* grad_c,
+                   int nthreads) {
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int b = 0; b < B; ++b) {
+    std::vector<double> y(V), tau(V), p(V), q(V);
+    double Lce = 0.0, Ltv = 0.0, Lconf = 0.0;
+    bool ok = true;
+    for (int j = 0; j < gamma; ++j) {
+      const int x = labels[(size_t)b * gamma + j];
+      if (x < 0 || x >= V) {
+        ok = false;
+        break;
+      }
+      const double wk = std::exp(-(double)j / (double)gamma);  // k = j + 1
+      const size_t row = ((size_t)b * gamma + j) * V;
+      for (int v = 0; v < V; ++v) {
+        y[v] = (double)zd[row + v] / T;
+        tau[v] = (double)zt[row + v] / T;
+      }
+      const double Ld = logsumexp(y), Lt = logsumexp(tau);
+      double l1 = 0.0, sp = 0.0;
+      for (int v = 0; v < V; ++v) {
+        p[v] = std::exp(y[v] - Ld);
+        q[v] = std::exp(tau[v] - Lt);
+        l1 += std::fabs(p[v] - q[v]);
+        sp += (p[v] > q[v] ? 1.0 : p[v] < q[v] ? -1.0 : 0.0) * p[v];
+      }
+      const double cstar = std::min(1.0, std::max(0.0, 1.0 - 0.5 * l1));
+      const double cl = (double)conf[(size_t)b * gamma + j];
+      const double c = sigmoid(cl);
+      // ln c = -softplus(-l), ln(1 - c) = -softplus(l)
+      const double log_c = -(std::max(-cl, 0.0) + std::log1p(std::exp(-std::fabs(cl))));
+      const double log_1mc = -(std::max(cl, 0.0) + std::log1p(std::exp(-std::fabs(cl))));
+      Lce += -wk * (y[x] - Ld);
+      Ltv += wk * l1;
+      Lconf += -wk * (cstar * log_c + (1.0 - cstar) * log_1mc);
+      if (grad_z)
+        for (int v = 0; v < V; ++v) {
+          const double s_v = p[v] > q[v] ? 1.0 : p[v] < q[v] ? -1.0 : 0.0;
+          grad_z[row + v] = wk / T * (a_ce * (p[v] - (v == x ? 1.0 : 0.0)) + a_tv * p[v] * (s_v - sp));
+        }
+      if (grad_c) grad_c[(size_t)b * gamma + j] = a_conf * wk * (c - cstar);
+    }
+    if (!ok) {
+      bad = 1;
+      loss[b] = NAN;
+      if (parts) parts[3 * (size_t)b] = parts[3 * (size_t)b + 1] = parts[3 * (size_t)b + 2] = NAN;
+      continue;
+    }
+    loss[b] = a_ce * Lce + a_tv * Ltv + a_conf * Lconf;
+    if (parts) {
+      parts[3 * (size_t)b] = Lce;
+      parts[3 * (size_t)b + 1] = Ltv;
+      parts[3 * (size_t)b + 2] = Lconf;
+    }
   }
   return bad;
 }

@@ -62,6 +62,9 @@ def _load():
         lib.orc_tv_label.restype = None
         lib.orc_verify.argtypes = [I, I, I, ctypes.c_double, ctypes.c_uint64] + [P] * 9 + [I]
         lib.orc_verify.restype = I
+        lib.orc_draft_loss.argtypes = ([I, I, I, ctypes.c_double, P, P, P, P] + [ctypes.c_double] * 3
+                                       + [P] * 4 + [I])
+        lib.orc_draft_loss.restype = I
         lib.orc_prefix_schedule.argtypes = [I, I, P, P, P, P]
         lib.orc_prefix_schedule.restype = I
         _lib = lib
@@ -226,3 +229,31 @@ def verify(*, gamma: int, T: float, seed: int, draft_logits, target_logits, draf
     st = _load().orc_verify(B, gamma, V, float(T), seed, _ptr(zd), _ptr(zt), _ptr(x), _ptr(n),
                             _ptr(out), _ptr(margin), _ptr(best), _ptr(best2), _ptr(tok2), nthreads)
     return VerifyResult(n, out, margin, best, best2, tok2, st)
+
+
+@dataclass
+class LossResult:
+    loss: np.ndarray         # [B] L = a_ce L_ce + a_tv L_tv + a_conf L_conf
+    parts: np.ndarray        # [B, 3] (L_ce, L_tv, L_conf)
+    grad_logits: np.ndarray  # [B, gamma, V] dL / d draft logits
+    grad_conf: np.ndarray    # [B, gamma] dL / d confidence logits
+    status: int
+
+
+def draft_loss(*, T: float, draft_logits, target_logits, labels, conf_logits,
+               alpha=(0.1, 0.9, 1.0), nthreads: int = 0) -> LossResult:
+    """Eqs 9-12 and their gradients for draft logits [B, gamma, V] fp32, frozen target logits
+    [B, gamma, V] fp32, labels [B, gamma] int32 and confidence logits [B, gamma] fp32."""
+    zd = _c(draft_logits, np.float32)
+    zt = _c(target_logits, np.float32)
+    lab = _c(labels, np.int32)
+    cf = _c(conf_logits, np.float32)
+    B, gamma, V = zd.shape
+    loss = np.zeros(B)
+    parts = np.zeros((B, 3))
+    gz = np.zeros((B, gamma, V))
+    gc = np.zeros((B, gamma))
+    st = _load().orc_draft_loss(B, gamma, V, float(T), _ptr(zd), _ptr(zt), _ptr(lab), _ptr(cf),
+                                float(alpha[0]), float(alpha[1]), float(alpha[2]), _ptr(loss),
+                                _ptr(parts), _ptr(gz), _ptr(gc), nthreads)
+    return LossResult(loss, parts, gz, gc, st)

@@ -55,7 +55,7 @@ def test_tv_label(N, V, T):
     assert abs(cs[0].item() - 1.0) < 1e-6
 
 
-@pytest.mark.parametrize("B,G", [(1, 1), (3, 7), (64, 7), (512, 7), (1000, 16)])
+@pytest.mark.parametrize("B,G", [(1, 1), (3, 7), (64, 7), (512, 7), (128, 15), (1000, 16)])
 def test_prefix_schedule_bit_exact(B, G):
     rng = np.random.default_rng(B * 31 + G)
     c = rng.uniform(0.02, 0.999, (B, G))

@@ -42,7 +42,7 @@ def test_tiny_batches(B):
     _run_case(TINY.with_(B=B, seed=10 + B))
 
 
-@pytest.mark.parametrize("gamma", [1, 16])
+@pytest.mark.parametrize("gamma", [1, 15, 16])
 def test_block_sizes(gamma):
     _run_case(TINY.with_(gamma=gamma, seed=20 + gamma))
 

@@ -74,6 +74,13 @@ def test_high_concurrency_full_sampled_rows():
     assert ties <= 1
 
 
+@pytest.mark.parametrize("B,G", [(64, 15), (130, 15)])
+def test_tc_gamma15(B, G):
+    # the longer draft length the pages also evaluate ("DSpark：既要猜得连贯…", Results: gamma 15)
+    _run(BASE.with_(B=B, gamma=G, V=12000, d=128, seed=110 + B), want_logits=False,
+         target_noise=1.0 if B == 64 else None)
+
+
 @pytest.mark.parametrize("B,V", [(37, 40000), (64, 38537), (6, 2000)])
 def test_tc_paired_tiles(B, V):
     # at most 64 requests: vocabulary tiles go in pairs (lanes 64-127 hold the second tile);

@@ -69,6 +69,7 @@ def run_case(B, G, V, *, seed, T=1.0, tokens="uniform", noise=1.0, vseed=7, iden
 
 @pytest.mark.parametrize("B,G,V,tokens", [(5, 3, 5000, "uniform"), (64, 7, 40000, "argmax"),
                                           (37, 16, 20001, "uniform"), (1, 1, 2, "uniform"),
+                                          (128, 15, 8192, "argmax"),
                                           (130, 4, 16384 * 2 + 4, "argmax")])
 def test_verify_matches_oracle(B, G, V, tokens):
     o, ties = run_case(B, G, V, seed=200 + B, tokens=tokens)
