@@ -305,6 +305,127 @@ def run_verify(args, wl, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+LOSS_METRIC = "loss+gradient draft blocks/sec (B per call) and achieved HBM GB/s vs roofline, 1 GB300"
+
+
+def run_loss(args, wl, rank, world, local_rank):
+    """Eqs 9-12 and their gradients on fp32 draft and target logits of the workload's shape."""
+    import torch
+
+    import semi_autoregressive_drafting_gb300 as ds
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    B, G, V = wl.B, wl.gamma, wl.V
+    g = torch.Generator().manual_seed(wl.seed + 100 * rank)
+    host = {"zd": torch.randn(B, G, V, generator=g) * wl.U_std}
+    host["zt"] = host["zd"] + torch.randn(B, G, V, generator=g)
+    host["lab"] = torch.randint(0, V, (B, G), generator=g, dtype=torch.int32)
+    host["cf"] = torch.randn(B, G, generator=g)
+    dev = {k: v.cuda() for k, v in host.items()}
+    lib = ds._lib.load()
+    ws = ds.LossWorkspace(B, G, V)
+    loss = torch.empty(B, device="cuda")
+    parts = torch.empty(B, 3, device="cuda")
+    gz = torch.empty(B, G, V, device="cuda")
+    gc = torch.empty(B, G, device="cuda")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def call(d):
+        code = lib.dspark_draft_loss(B, G, V, float(wl.T), d["zd"].data_ptr(), d["zt"].data_ptr(),
+                                     d["lab"].data_ptr(), d["cf"].data_ptr(), 0.1, 0.9, 1.0,
+                                     loss.data_ptr(), parts.data_ptr(), gz.data_ptr(),
+                                     gc.data_ptr(), ws.buf.data_ptr(), ws.nbytes, stream.cuda_stream)
+        assert code == 0, ds._lib.load().dspark_last_error()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call(dev)
+    torch.cuda.synchronize()
+    assert ws.status() == 0, "loss reported a device error during warm-up"
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            call(dev)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    times = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(times) / len(times)
+    assert ws.status() == 0, "loss reported a device error"
+    # end to end: logits, labels and confidence logits in from pinned host memory; the losses,
+    # their parts and both gradients out
+    hin = {k: v.pin_memory() for k, v in host.items()}
+    din = {k: torch.empty_like(v) for k, v in dev.items()}
+    hout = [torch.empty_like(t, device="cpu").pin_memory() for t in (loss, parts, gz, gc)]
+    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    d2h = sum(t.numel() * 4 for t in hout)
+
+    def e2e_step():
+        for k in din:
+            din[k].copy_(hin[k], non_blocking=True)
+        call(din)
+        for h, t in zip(hout, (loss, parts, gz, gc)):
+            h.copy_(t, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = min(args.steps, 30)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for _ in range(e2e_steps):
+        flush.zero_()
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_ms /= e2e_steps
+    if dist:
+        tt = torch.tensor([ms, e2e_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = tt.tolist()
+    if rank == 0:
+        peak, peak_kind = load_peaks()
+        # the least the step must move: both logit arrays read once, the logit gradient written once
+        alg = 3 * B * G * V * 4 + B * G * 4 * 3
+        achieved = alg / (ms * 1e-3) / 1e9
+        line = {
+            "metric": LOSS_METRIC, "value": world * B / (ms * 1e-3), "unit": "blocks/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": f"loss {wl.name}", "B": B, "gamma": G, "V": V, "T": wl.T,
+                       "alpha": [0.1, 0.9, 1.0],
+                       "l2": "flushed between timed calls (512 MB write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_kind": f"{peak_kind} copy bandwidth",
+                         "algorithmic_bytes_per_launch": alg,
+                         "kernel": "loss_part + loss_stat + loss_grad + loss_final"},
+            "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": "blocks/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clk.summary(),
+            "ms_per_step_min": min(times), "ms_per_step_median": statistics.median(times),
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -313,9 +434,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_4b_markov")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["draft", "verify"], default="draft",
+    ap.add_argument("--op", choices=["draft", "verify", "loss"], default="draft",
                     help="draft: the draft block (default); verify: the speculative accept/reject "
-                         "step on the workload's B, gamma, V")
+                         "step on the workload's B, gamma, V; loss: the training losses (Eqs 9-12) "
+                         "and their gradients on that shape")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -332,6 +454,9 @@ def main():
         return
     if args.op == "verify":
         run_verify(args, wl, rank, world, local_rank)
+        return
+    if args.op == "loss":
+        run_loss(args, wl, rank, world, local_rank)
         return
 
     import torch

@@ -199,6 +199,35 @@ dspark_status dspark_verify(int B, int gamma, int V, float T, uint64_t seed,
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The drafter's training losses and their gradients [P1 s1 Eqs 9-12; delta table D3-D7], for
+ * teacher-forced draft logits.  For request b and position k = 1..gamma (row j = k - 1):
+ *   p_k = softmax(draft_logits[b][j] / T), q_k = softmax(target_logits[b][j] / T) (frozen),
+ *   x*_k = labels[b][j], c_k = sigmoid(conf_logits[b][j]), w_k = exp(-(k - 1) / gamma);
+ *   L_ce = -sum_k w_k ln p_k(x*_k)  (Eq 9);  L_tv = sum_k w_k ||p_k - q_k||_1  (Eq 10);
+ *   c*_k = clamp(1 - 1/2 ||p_k - q_k||_1, 0, 1)  (Eq 8);
+ *   L_conf = -sum_k w_k [c*_k ln c_k + (1 - c*_k) ln(1 - c_k)]  (Eq 11);
+ *   L = alpha_ce L_ce + alpha_tv L_tv + alpha_conf L_conf  (Eq 12; defaults 0.1, 0.9, 1.0).
+ * c* is a label (no gradient through it):
+ *   grad_logits[b][j][v] = (w_k / T) (alpha_ce (p_v - [v == x*]) + alpha_tv p_v (s_v - sum_u s_u p_u)),
+ *   s_u = sign(p_u - q_u);  grad_conf[b][j] = alpha_conf w_k (c_k - c*_k).
+ * Arguments (device pointers, row-major, caller-owned): draft_logits, target_logits
+ * [B][gamma][V] fp32 (16-byte aligned); labels [B][gamma] int32; conf_logits [B][gamma] fp32.
+ * Outputs, each optional (NULL skips it, at least one given): loss [B], parts [B][3]
+ * (L_ce, L_tv, L_conf), grad_logits [B][gamma][V] (16-byte aligned), grad_conf [B][gamma], all
+ * fp32.  workspace: dspark_draft_loss_workspace_bytes(B, gamma, V) bytes, 256-byte aligned
+ * (contents need not be zero).  Limits: 1 <= gamma <= 16, 2 <= V <= 2^24, T finite and > 0.
+ * A label outside [0, V) makes every output of its request NaN and sets DSPARK_ERR_INVALID in
+ * the workspace status.  Three or four launches on `stream`.
+ */
+size_t dspark_draft_loss_workspace_bytes(int B, int gamma, int V);
+dspark_status dspark_draft_loss(int B, int gamma, int V, float T, const float* draft_logits,
+                                const float* target_logits, const int32_t* labels,
+                                const float* conf_logits, float alpha_ce, float alpha_tv,
+                                float alpha_conf, float* loss, float* parts, float* grad_logits,
+                                float* grad_conf, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/*
  * The Markov draft of dspark_markov_draft for callers that cannot allocate device memory.  The
  * paper has no counterpart: this is a deployment variant of the same computation.  Callers such
  * as plugins inside another framework's memory pool, serving engines that forbid allocation on

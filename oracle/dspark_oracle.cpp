@@ -425,7 +425,7 @@ int orc_verify(int B, int gamma, int V, double T, uint64_t seed, const float* zd
 //                     s_u = sign(p_u - q_u) (0 where they are equal)
 //   dL/dconf[b][j]  = a_conf w_k (c_k - c*_k).
 // loss[b] = L; parts[b] = (L_ce, L_tv, L_conf); grad_z [B][gamma][V] and grad_c [B][gamma] may
-// be NULL.  Returns 1 (and NaN outputs for that request) when a label lies outside [0, V).
+// be NULL.  Returns 1 when a label lies outside [0, V); every output of that request is NaN.
 int orc_draft_loss(int B, int gamma, int V, double T, const float* zd, const float* zt,
                    const int32_t* labels, const float* conf, double a_ce, double a_tv,
                    double a_conf, double* loss, double* parts, double* grad_z, double* grad_c,
@@ -441,10 +441,21 @@ int orc_draft_loss(int B, int gamma, int V, double T, const float* zd, const flo
     bool ok = true;
     for (int j = 0; j < gamma; ++j) {
       const int x = labels[(size_t)b * gamma + j];
-      if (x < 0 || x >= V) {
-        ok = false;
-        break;
+      ok = ok && x >= 0 && x < V;
+    }
+    if (!ok) {  // every output of the request is NaN
+      bad = 1;
+      loss[b] = NAN;
+      if (parts) parts[3 * (size_t)b] = parts[3 * (size_t)b + 1] = parts[3 * (size_t)b + 2] = NAN;
+      for (int j = 0; j < gamma; ++j) {
+        if (grad_c) grad_c[(size_t)b * gamma + j] = NAN;
+        if (grad_z)
+          for (int v = 0; v < V; ++v) grad_z[((size_t)b * gamma + j) * V + v] = NAN;
       }
+      continue;
+    }
+    for (int j = 0; j < gamma; ++j) {
+      const int x = labels[(size_t)b * gamma + j];
       const double wk = std::exp(-(double)j / (double)gamma);  // k = j + 1
       const size_t row = ((size_t)b * gamma + j) * V;
       for (int v = 0; v < V; ++v) {
@@ -474,12 +485,6 @@ int orc_draft_loss(int B, int gamma, int V, double T, const float* zd, const flo
           grad_z[row + v] = wk / T * (a_ce * (p[v] - (v == x ? 1.0 : 0.0)) + a_tv * p[v] * (s_v - sp));
         }
       if (grad_c) grad_c[(size_t)b * gamma + j] = a_conf * wk * (c - cstar);
-    }
-    if (!ok) {
-      bad = 1;
-      loss[b] = NAN;
-      if (parts) parts[3 * (size_t)b] = parts[3 * (size_t)b + 1] = parts[3 * (size_t)b + 2] = NAN;
-      continue;
     }
     loss[b] = a_ce * Lce + a_tv * Ltv + a_conf * Lconf;
     if (parts) {

@@ -20,7 +20,7 @@ from . import _lib
 
 __all__ = ["Workspace", "markov_draft", "rnn_draft", "confidence", "tv_label",
            "prefix_schedule", "draft_path", "draft_launches", "DraftOutput", "DraftPlan",
-           "VerifyWorkspace", "verify"]
+           "VerifyWorkspace", "verify", "LossWorkspace", "draft_loss"]
 
 _F32, _BF16 = 0, 1
 
@@ -242,6 +242,42 @@ def verify(draft_logits, target_logits, draft_tokens, *, T=1.0, seed=0, workspac
                              ws.buf.data_ptr(), ws.nbytes, _stream(stream))
     _lib.check(code, "dspark_verify")
     return n, toks
+
+
+class LossWorkspace(Workspace):
+    """Device scratch for ``draft_loss`` (shapes up to B, gamma, V)."""
+
+    def __init__(self, B: int, gamma: int, V: int, device=None):
+        n = _lib.load().dspark_draft_loss_workspace_bytes(B, gamma, V)
+        if n == 0:
+            raise ValueError("invalid loss shape for a workspace")
+        self.nbytes = int(n)
+        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def draft_loss(draft_logits, target_logits, labels, conf_logits, *, T=1.0,
+               alpha=(0.1, 0.9, 1.0), want_grads=True, workspace=None, stream=None):
+    """Eqs 9-12 and their gradients (c* held as a label).  See ``dspark_draft_loss``.
+
+    Returns (loss [B], parts [B, 3], grad_logits [B, gamma, V] or None, grad_conf [B, gamma]
+    or None), all fp32.
+    """
+    lib = _lib.load()
+    B, gamma, V = draft_logits.shape
+    if draft_logits.dtype != torch.float32 or target_logits.dtype != torch.float32:
+        raise TypeError("draft_loss takes fp32 logits")
+    dev = draft_logits.device
+    ws = workspace or LossWorkspace(B, gamma, V, device=dev)
+    loss = torch.empty(B, dtype=torch.float32, device=dev)
+    parts = torch.empty(B, 3, dtype=torch.float32, device=dev)
+    gz = torch.empty_like(draft_logits) if want_grads else None
+    gc = torch.empty(B, gamma, dtype=torch.float32, device=dev) if want_grads else None
+    code = lib.dspark_draft_loss(B, gamma, V, float(T), _ptr(draft_logits), _ptr(target_logits),
+                                 _ptr(labels), _ptr(conf_logits), float(alpha[0]),
+                                 float(alpha[1]), float(alpha[2]), _ptr(loss), _ptr(parts),
+                                 _ptr(gz), _ptr(gc), ws.buf.data_ptr(), ws.nbytes, _stream(stream))
+    _lib.check(code, "dspark_draft_loss")
+    return loss, parts, gz, gc
 
 
 def draft_path(head: int, B: int, V: int, r: int, bf16: bool = True) -> int:

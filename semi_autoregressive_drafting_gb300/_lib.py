@@ -33,6 +33,8 @@ SIGNATURES = {
     "dspark_prefix_schedule": (I, [I, I, P, P, P, P, P]),
     "dspark_verify_workspace_bytes": (SZ, [I, I, I]),
     "dspark_verify": (I, [I, I, I, F, U64, P, P, P, P, P, P, SZ, P]),
+    "dspark_draft_loss_workspace_bytes": (SZ, [I, I, I]),
+    "dspark_draft_loss": (I, [I, I, I, F, P, P, P, P, F, F, F, P, P, P, P, P, SZ, P]),
     "dspark_get_status": (I, [P, SZ, P]),
     "dspark_last_error": (ctypes.c_char_p, []),
     "dspark_draft_path": (I, [I, I, I, I, I]),

@@ -365,6 +365,38 @@ dspark_status dspark_verify(int B, int gamma, int V, float T, uint64_t seed,
   return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "verify launch");
 }
 
+size_t dspark_draft_loss_workspace_bytes(int B, int gamma, int V) {
+  if (B < 1 || gamma < 1 || gamma > 16 || V < 2 || V > (1 << 24)) return 0;
+  return loss_workspace_bytes(B, gamma, V);
+}
+
+dspark_status dspark_draft_loss(int B, int gamma, int V, float T, const float* draft_logits,
+                                const float* target_logits, const int32_t* labels,
+                                const float* conf_logits, float alpha_ce, float alpha_tv,
+                                float alpha_conf, float* loss, float* parts, float* grad_logits,
+                                float* grad_conf, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  g_err.clear();
+  if (B < 1 || B > (1 << 20) || gamma < 1 || gamma > 16 || V < 2 || V > (1 << 24))
+    return fail(DSPARK_ERR_INVALID, "bad shape B=%d gamma=%d V=%d", B, gamma, V);
+  if (!(T > 0.f) || !std::isfinite(T)) return fail(DSPARK_ERR_INVALID, "T must be finite and > 0");
+  if (!std::isfinite(alpha_ce) || !std::isfinite(alpha_tv) || !std::isfinite(alpha_conf))
+    return fail(DSPARK_ERR_INVALID, "the loss weights must be finite");
+  if (!draft_logits || !target_logits || !labels || !conf_logits)
+    return fail(DSPARK_ERR_INVALID, "draft_logits, target_logits, labels and conf_logits are required");
+  if (!loss && !parts && !grad_logits && !grad_conf)
+    return fail(DSPARK_ERR_INVALID, "no output requested");
+  if (!aligned(draft_logits, 16) || !aligned(target_logits, 16) || (grad_logits && !aligned(grad_logits, 16)))
+    return fail(DSPARK_ERR_INVALID, "draft_logits, target_logits and grad_logits must be 16-byte aligned");
+  const size_t need = loss_workspace_bytes(B, gamma, V);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    return fail(DSPARK_ERR_WORKSPACE, "workspace must be 256-byte aligned and >= %zu bytes", need);
+  cudaError_t e = launch_loss(B, gamma, V, T, draft_logits, target_logits, labels, conf_logits,
+                              alpha_ce, alpha_tv, alpha_conf, loss, parts, grad_logits, grad_conf,
+                              workspace, (cudaStream_t)stream);
+  return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "draft loss launch");
+}
+
 dspark_status dspark_get_status(void* workspace, size_t workspace_bytes, void* stream) {
   g_err.clear();
   if (!workspace || workspace_bytes < sizeof(WsHeader))

@@ -15,6 +15,11 @@ size_t verify_workspace_bytes(int B, int G, int V);
 cudaError_t launch_verify(int B, int G, int V, float T, uint64_t seed, const float* zd,
                           const float* zt, const int32_t* tok, int32_t* n_acc, int32_t* out,
                           void* workspace, cudaStream_t stream);
+size_t loss_workspace_bytes(int B, int G, int V);
+cudaError_t launch_loss(int B, int G, int V, float T, const float* zd, const float* zt,
+                        const int32_t* lab, const float* conf, float a_ce, float a_tv, float a_conf,
+                        float* loss, float* parts, float* grad_z, float* grad_c, void* workspace,
+                        cudaStream_t stream);
 cudaError_t launch_prefix_schedule(int B, int G, const float* S, const double* sps, int32_t* len,
                                    double* theta, cudaStream_t stream);
 
