@@ -40,6 +40,13 @@
 //     w_k = exp(-(k-1)/gamma); c*_k (Eq 8) is a label in L_conf: no gradient flows through it,
 //     and the target logits are frozen [P1 s1, "the target is frozen throughout"].  The losses
 //     are sums over positions (no division by sum w_k).
+//   * STS calibration ([P4 s3] "sequential temperature scaling that minimises expected
+//     calibration error of the cumulative product, one position at a time"; [P1 delta table
+//     D13] "left-to-right 1-D grid search on the cumulative product, prefix held fixed"; the
+//     ECE formula there is garbled): the standard equal-width-bin ECE with M bins,
+//     ECE = sum_m |sum_{n in bin m} (S_n - y_n)| / N, bin = min(M - 1, floor(S M)); the
+//     survival label of position k is y = [accepted length >= k]; the temperature grid is
+//     given by the caller and ties go to the first grid entry.
 //   * Scheduler (Algorithm 1 is named, not printed): choose per-request verify lengths l_b in
 //     0..gamma maximising Theta = SPS(n) * sum_b (1 + sum_{k<=l_b} S_{b,k}) with
 //     n = sum_b (l_b + 1); only contiguous prefixes are legal; ties go to fewer tokens.
@@ -494,6 +501,47 @@ int orc_draft_loss(int B, int gamma, int V, double T, const float* zd, const flo
     }
   }
   return bad;
+}
+
+// Sequential temperature scaling of the confidence head [P4 s3; P1 delta table D13].  N
+// calibration blocks, confidence logits conf [N][gamma], accepted lengths acc [N] (0..gamma),
+// a temperature grid [ng].  For k = 1..gamma in order, with tau_1..tau_{k-1} already chosen:
+//   S_k[n](t) = prod_{i<k} sigmoid(conf[n][i-1] / tau_i) * sigmoid(conf[n][k-1] / t)
+//   y_k[n]    = [acc[n] >= k]
+//   ECE_k(t)  = sum_m |sum_{n : bin(S_k[n](t)) = m} (S_k[n](t) - y_k[n])| / N,
+//               bin(s) = min(M - 1, floor(s M))
+//   tau_k     = the first grid entry with the smallest ECE_k
+// Outputs tau [gamma], ece [gamma] (ECE_k at tau_k) and ece_grid [gamma][ng] (every ECE_k(t)).
+// Returns 1 if an accepted length lies outside [0, gamma] or a grid entry is not > 0.
+int orc_sts(int N, int gamma, const float* conf, const int32_t* acc, int ng, const float* grid,
+            int M, double* tau, double* ece, double* ece_grid) {
+  for (int n = 0; n < N; ++n)
+    if (acc[n] < 0 || acc[n] > gamma) return 1;
+  for (int g = 0; g < ng; ++g)
+    if (!(grid[g] > 0.0f)) return 1;
+  std::vector<double> prefix(N, 1.0), sums(M);
+  for (int k = 1; k <= gamma; ++k) {
+    int best_g = 0;
+    for (int g = 0; g < ng; ++g) {
+      const double t = (double)grid[g];
+      std::fill(sums.begin(), sums.end(), 0.0);
+      for (int n = 0; n < N; ++n) {
+        const double S = prefix[n] * sigmoid((double)conf[(size_t)n * gamma + k - 1] / t);
+        const double y = acc[n] >= k ? 1.0 : 0.0;
+        const int m = std::min(M - 1, (int)std::floor(S * M));
+        sums[m] += S - y;
+      }
+      double e = 0.0;
+      for (int m = 0; m < M; ++m) e += std::fabs(sums[m]);
+      e /= (double)N;
+      ece_grid[(size_t)(k - 1) * ng + g] = e;
+      if (e < ece_grid[(size_t)(k - 1) * ng + best_g]) best_g = g;
+    }
+    tau[k - 1] = (double)grid[best_g];
+    ece[k - 1] = ece_grid[(size_t)(k - 1) * ng + best_g];
+    for (int n = 0; n < N; ++n) prefix[n] *= sigmoid((double)conf[(size_t)n * gamma + k - 1] / tau[k - 1]);
+  }
+  return 0;
 }
 
 // Hardware-aware prefix scheduler [P2 "设计"; P4 s3 Theta = tau * SPS(B)].  Choose l_b in

@@ -65,6 +65,8 @@ def _load():
         lib.orc_draft_loss.argtypes = ([I, I, I, ctypes.c_double, P, P, P, P] + [ctypes.c_double] * 3
                                        + [P] * 4 + [I])
         lib.orc_draft_loss.restype = I
+        lib.orc_sts.argtypes = [I, I, P, P, I, P, I, P, P, P]
+        lib.orc_sts.restype = I
         lib.orc_prefix_schedule.argtypes = [I, I, P, P, P, P]
         lib.orc_prefix_schedule.restype = I
         _lib = lib
@@ -257,3 +259,19 @@ def draft_loss(*, T: float, draft_logits, target_logits, labels, conf_logits,
                                 float(alpha[0]), float(alpha[1]), float(alpha[2]), _ptr(loss),
                                 _ptr(parts), _ptr(gz), _ptr(gc), nthreads)
     return LossResult(loss, parts, gz, gc, st)
+
+
+def sts(conf_logits, accepted, grid, bins: int = 15):
+    """Sequential temperature scaling: per-position temperatures from the grid minimising the
+    ECE of the cumulative product, left to right.  Returns (tau [gamma], ece [gamma],
+    ece_grid [gamma, len(grid)], status)."""
+    cf = _c(conf_logits, np.float32)
+    acc = _c(accepted, np.int32)
+    gr = _c(grid, np.float32)
+    N, gamma = cf.shape
+    tau = np.zeros(gamma)
+    ece = np.zeros(gamma)
+    eg = np.zeros((gamma, len(gr)))
+    st = _load().orc_sts(N, gamma, _ptr(cf), _ptr(acc), len(gr), _ptr(gr), bins, _ptr(tau),
+                         _ptr(ece), _ptr(eg))
+    return tau, ece, eg, st
