@@ -228,6 +228,29 @@ dspark_status dspark_draft_loss(int B, int gamma, int V, float T, const float* d
                                 void* stream);
 
 /*
+ * Sequential temperature scaling of the confidence head [P4 s3: calibration that minimises the
+ * expected calibration error of the cumulative product, one position at a time; P1 delta
+ * table D13: a left-to-right 1-D grid search with the prefix held fixed].  N calibration blocks
+ * with confidence logits conf_logits [N][gamma] fp32 and accepted lengths accepted [N] int32
+ * (0..gamma, e.g. dspark_verify's n_accepted); a temperature grid [ngrid] fp32 (> 0).  For
+ * k = 1..gamma, with tau_1..tau_{k-1} already chosen:
+ *   S_k[n](t) = prod_{i<k} sigmoid(conf[n][i-1] / tau_i) * sigmoid(conf[n][k-1] / t),
+ *   y_k[n] = [accepted[n] >= k],
+ *   ECE_k(t) = sum_m |sum_{n in bin m} (S_k[n](t) - y_k[n])| / N,  bin(s) = min(bins-1, floor(s bins))
+ *   (the standard equal-width-bin ECE; the page's own formula is garbled),
+ *   tau_k = the first grid entry with the smallest ECE_k.
+ * Outputs: tau [gamma], ece [gamma] (ECE_k at tau_k), ece_grid [gamma][ngrid] (every ECE_k(t))
+ * or NULL; fp32.  Limits: 1 <= gamma <= 16, 1 <= ngrid <= 4096, 1 <= bins <= 64.  workspace:
+ * dspark_sts_workspace_bytes(N, gamma, ngrid, bins) bytes, 256-byte aligned.  An accepted
+ * length outside [0, gamma] or a grid entry <= 0 sets DSPARK_ERR_INVALID in the workspace
+ * status.  Deterministic (fixed reduction order).  2 * gamma launches on `stream`.
+ */
+size_t dspark_sts_workspace_bytes(int N, int gamma, int ngrid, int bins);
+dspark_status dspark_sts(int N, int gamma, const float* conf_logits, const int32_t* accepted,
+                         int ngrid, const float* grid, int bins, float* tau, float* ece,
+                         float* ece_grid, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * The Markov draft of dspark_markov_draft for callers that cannot allocate device memory.  The
  * paper has no counterpart: this is a deployment variant of the same computation.  Callers such
  * as plugins inside another framework's memory pool, serving engines that forbid allocation on

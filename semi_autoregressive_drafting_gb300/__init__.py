@@ -20,7 +20,7 @@ from . import _lib
 
 __all__ = ["Workspace", "markov_draft", "rnn_draft", "confidence", "tv_label",
            "prefix_schedule", "draft_path", "draft_launches", "DraftOutput", "DraftPlan",
-           "VerifyWorkspace", "verify", "LossWorkspace", "draft_loss"]
+           "VerifyWorkspace", "verify", "LossWorkspace", "draft_loss", "sts"]
 
 _F32, _BF16 = 0, 1
 
@@ -278,6 +278,31 @@ def draft_loss(draft_logits, target_logits, labels, conf_logits, *, T=1.0,
                                  _ptr(gz), _ptr(gc), ws.buf.data_ptr(), ws.nbytes, _stream(stream))
     _lib.check(code, "dspark_draft_loss")
     return loss, parts, gz, gc
+
+
+def sts(conf_logits, accepted, grid, *, bins=15, stream=None):
+    """Sequential temperature scaling of the confidence head.  See ``dspark_sts``.
+
+    conf_logits [N, gamma] fp32, accepted [N] int32, grid [ngrid] fp32.  Returns (tau [gamma],
+    ece [gamma], ece_grid [gamma, ngrid]) fp32 and the device status.
+    """
+    lib = _lib.load()
+    N, gamma = conf_logits.shape
+    ng = grid.shape[0]
+    n = lib.dspark_sts_workspace_bytes(N, gamma, ng, bins)
+    if n == 0:
+        raise ValueError("invalid sts shape")
+    ws = Workspace.__new__(Workspace)
+    ws.nbytes = int(n)
+    ws.buf = torch.zeros(ws.nbytes, dtype=torch.uint8, device=conf_logits.device)
+    tau = torch.empty(gamma, dtype=torch.float32, device=conf_logits.device)
+    ece = torch.empty_like(tau)
+    eg = torch.empty(gamma, ng, dtype=torch.float32, device=conf_logits.device)
+    code = lib.dspark_sts(N, gamma, _ptr(conf_logits), _ptr(accepted), ng, _ptr(grid), bins,
+                          _ptr(tau), _ptr(ece), _ptr(eg), ws.buf.data_ptr(), ws.nbytes,
+                          _stream(stream))
+    _lib.check(code, "dspark_sts")
+    return tau, ece, eg, ws.status(stream)
 
 
 def draft_path(head: int, B: int, V: int, r: int, bf16: bool = True) -> int:

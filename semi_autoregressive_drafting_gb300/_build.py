@@ -18,7 +18,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdspark.so")
 
 SOURCES = ["api.cu", "draft_cc.cu", "draft_tc.cu", "gemm_tc.cu", "aux_kernels.cu", "noalloc.cu",
-           "verify.cu", "loss.cu"]
+           "verify.cu", "loss.cu", "sts.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
          "--expt-relaxed-constexpr"]

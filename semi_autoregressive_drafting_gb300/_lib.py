@@ -34,6 +34,8 @@ SIGNATURES = {
     "dspark_verify_workspace_bytes": (SZ, [I, I, I]),
     "dspark_verify": (I, [I, I, I, F, U64, P, P, P, P, P, P, SZ, P]),
     "dspark_draft_loss_workspace_bytes": (SZ, [I, I, I]),
+    "dspark_sts_workspace_bytes": (SZ, [I, I, I, I]),
+    "dspark_sts": (I, [I, I, P, P, I, P, I, P, P, P, P, SZ, P]),
     "dspark_draft_loss": (I, [I, I, I, F, P, P, P, P, F, F, F, P, P, P, P, P, SZ, P]),
     "dspark_get_status": (I, [P, SZ, P]),
     "dspark_last_error": (ctypes.c_char_p, []),

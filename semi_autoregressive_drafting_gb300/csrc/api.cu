@@ -397,6 +397,28 @@ dspark_status dspark_draft_loss(int B, int gamma, int V, float T, const float* d
   return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "draft loss launch");
 }
 
+size_t dspark_sts_workspace_bytes(int N, int gamma, int ngrid, int bins) {
+  if (N < 1 || gamma < 1 || gamma > 16 || ngrid < 1 || ngrid > 4096 || bins < 1 || bins > 64) return 0;
+  return sts_workspace_bytes(N, gamma, ngrid, bins);
+}
+
+dspark_status dspark_sts(int N, int gamma, const float* conf_logits, const int32_t* accepted,
+                         int ngrid, const float* grid, int bins, float* tau, float* ece,
+                         float* ece_grid, void* workspace, size_t workspace_bytes, void* stream) {
+  g_err.clear();
+  if (N < 1 || N > (1 << 26) || gamma < 1 || gamma > 16 || ngrid < 1 || ngrid > 4096 || bins < 1 ||
+      bins > 64)
+    return fail(DSPARK_ERR_INVALID, "bad shape N=%d gamma=%d ngrid=%d bins=%d", N, gamma, ngrid, bins);
+  if (!conf_logits || !accepted || !grid || !tau || !ece)
+    return fail(DSPARK_ERR_INVALID, "conf_logits, accepted, grid, tau and ece are required");
+  const size_t need = sts_workspace_bytes(N, gamma, ngrid, bins);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    return fail(DSPARK_ERR_WORKSPACE, "workspace must be 256-byte aligned and >= %zu bytes", need);
+  cudaError_t e = launch_sts(N, gamma, conf_logits, accepted, ngrid, grid, bins, tau, ece, ece_grid,
+                             workspace, (cudaStream_t)stream);
+  return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "sts launch");
+}
+
 dspark_status dspark_get_status(void* workspace, size_t workspace_bytes, void* stream) {
   g_err.clear();
   if (!workspace || workspace_bytes < sizeof(WsHeader))

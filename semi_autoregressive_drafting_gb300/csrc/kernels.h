@@ -20,6 +20,10 @@ cudaError_t launch_loss(int B, int G, int V, float T, const float* zd, const flo
                         const int32_t* lab, const float* conf, float a_ce, float a_tv, float a_conf,
                         float* loss, float* parts, float* grad_z, float* grad_c, void* workspace,
                         cudaStream_t stream);
+size_t sts_workspace_bytes(int N, int G, int ng, int bins);
+cudaError_t launch_sts(int N, int G, const float* conf, const int32_t* acc, int ng, const float* grid,
+                       int bins, float* tau, float* ece, float* ece_grid, void* workspace,
+                       cudaStream_t stream);
 cudaError_t launch_prefix_schedule(int B, int G, const float* S, const double* sps, int32_t* len,
                                    double* theta, cudaStream_t stream);
 
