@@ -62,6 +62,23 @@ def algorithmic_bytes(wl) -> int:
     return wl.gamma * per_step + (wl.d + wl.r) * es_w
 
 
+def packed(specs, device):
+    """One buffer holding the arrays (name, shape, dtype) at 256-byte aligned offsets, pinned
+    when on the host; returns the flat uint8 buffer and the named views."""
+    import torch
+
+    offs, o = {}, 0
+    for name, shape, dt in specs:
+        n = int(torch.Size(shape).numel()) * torch.empty((), dtype=dt).element_size()
+        offs[name] = (o, n)
+        o = (o + n + 255) // 256 * 256
+    buf = (torch.empty(o, dtype=torch.uint8, pin_memory=True) if device == "cpu"
+           else torch.empty(o, dtype=torch.uint8, device=device))
+    views = {name: buf[a:a + n].view(dt).view(shape)
+             for (name, shape, dt), (a, n) in zip(specs, offs.values())}
+    return buf, views
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -509,33 +526,41 @@ def main():
     ms_step = sum(times) / len(times)
     assert ws.status() == 0, "draft kernel reported a device error"
 
-    # ---- end to end through the public API: pinned host inputs in, results out, every step
-    # per-step inputs come from pinned host memory; the weights stay resident on the device
+    # ---- end to end through the public API: pinned host inputs in, results out, every step.
+    # The step's inputs (U, h, x0 and the target) sit in one pinned host buffer and the results
+    # (tokens, lse, c, S, c*, l1) in one device buffer, each array at a 256-byte aligned offset
+    # (the draft call takes any aligned device pointers), so a step is one copy in, the draft
+    # call and one copy out.  The weights stay resident on the device.
     names = ["U", "h", "x0"] + (["target"] if host.get("target") is not None else [])
-    hin = {k: host[k].pin_memory() for k in names}
-    din = {k: torch.empty_like(dev[k]) for k in names}
-    staged = plan(din["U"], din["h"], din["x0"], din.get("target"))
+    in_specs = [(k, tuple(host[k].shape), host[k].dtype) for k in names]
+    hin_buf, hin = packed(in_specs, "cpu")
+    din_buf, din = packed(in_specs, "cuda")
+    for k in names:
+        hin[k].copy_(host[k])
+    conf = dev["h"] is not None and dev["w"] is not None
+    out_specs = [("tokens", (B, G), torch.int32), ("lse", (B, G), torch.float32)]
+    if conf:
+        out_specs += [("c", (B, G), torch.float32), ("S", (B, G), torch.float32)]
+    if host.get("target") is not None:
+        out_specs += [("cstar", (B, G), torch.float32), ("l1", (B, G), torch.float32)]
+    dout_buf, dout = packed(out_specs, "cuda")
+    hout_buf, hout = packed(out_specs, "cpu")
+    staged = plan(din["U"], din["h"], din["x0"], din.get("target"), out=dout)
     o = staged.out
-    outs = {k: getattr(o, k) for k in ("lse", "c", "S", "cstar", "l1") if getattr(o, k) is not None}
-    res = {k: torch.empty(B, G, dtype=torch.float32).pin_memory() for k in outs}
-    res_tok = torch.empty(B, G, dtype=torch.int32).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in hin.values())
-    d2h = res_tok.numel() * 4 + sum(v.numel() * 4 for v in res.values())
+    h2d = hin_buf.numel()
+    d2h = hout_buf.numel()
     e2e_steps = min(args.steps, 200)
 
     def e2e_step(s):
-        for k in names:
-            din[k].copy_(hin[k], non_blocking=True)
+        din_buf.copy_(hin_buf, non_blocking=True)
         staged.run(s)
-        res_tok.copy_(o.tokens, non_blocking=True)
-        for k, v in outs.items():
-            res[k].copy_(v, non_blocking=True)
+        hout_buf.copy_(dout_buf, non_blocking=True)
 
     for _ in range(3):
         e2e_step(stream)
     torch.cuda.synchronize()
-    # the step (input copies, the draft call, result copies) is captured once in a CUDA graph
-    # and replayed: one launch per step, so the host's issue time does not stretch the step
+    # the step (input copy, the draft call, result copy) is captured once in a CUDA graph and
+    # replayed: one launch per step, so the host's issue time does not stretch the step
     graph = None
     try:
         graph = torch.cuda.CUDAGraph()
@@ -561,7 +586,7 @@ def main():
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
     e2e_ms /= e2e_steps
-    res_ok = bool((res_tok >= 0).all()) and torch.equal(res_tok.cuda(), o.tokens)
+    res_ok = bool((hout["tokens"] >= 0).all()) and torch.equal(hout["tokens"].cuda(), o.tokens)
     assert ws.status() == 0, "draft kernel reported a device error (end-to-end loop)"
 
     # ---- max over ranks

@@ -20,7 +20,7 @@ from . import _lib
 
 __all__ = ["Workspace", "markov_draft", "rnn_draft", "confidence", "tv_label",
            "prefix_schedule", "draft_path", "draft_launches", "DraftOutput", "DraftPlan",
-           "VerifyWorkspace", "verify", "LossWorkspace", "draft_loss", "sts"]
+           "VerifyWorkspace", "verify", "LossWorkspace", "draft_loss", "sts", "CapacityRing"]
 
 _F32, _BF16 = 0, 1
 
@@ -303,6 +303,34 @@ def sts(conf_logits, accepted, grid, *, bins=15, stream=None):
                           _stream(stream))
     _lib.check(code, "dspark_sts")
     return tau, ece, eg, ws.status(stream)
+
+
+class CapacityRing:
+    """The steps/s table the prefix scheduler reads, delayed by ``delay`` steps.
+
+    "DSpark：既要猜得连贯…" ("设计") notes that the production scheduler uses a capacity
+    estimate delayed by two steps, to fit asynchronous scheduling and CUDA Graphs.  ``table`` is
+    one fixed device buffer that ``prefix_schedule`` can read (also from a captured graph);
+    ``advance(sps)`` records this step's measured table and copies the one recorded ``delay``
+    steps earlier into ``table``, stream-ordered (until ``delay`` steps have been recorded,
+    ``table`` keeps the initial table).  Only tensor copies: no arithmetic of the method here.
+    """
+
+    def __init__(self, initial, delay: int = 2):
+        if delay < 0:
+            raise ValueError("delay must be >= 0")
+        self.delay = delay
+        self.table = initial.clone()
+        self._ring = [torch.empty_like(initial) for _ in range(delay + 1)]
+        self._step = 0
+
+    def advance(self, sps) -> "torch.Tensor":
+        slot = self._step % (self.delay + 1)
+        self._ring[slot].copy_(sps, non_blocking=True)
+        if self._step >= self.delay:
+            self.table.copy_(self._ring[(self._step - self.delay) % (self.delay + 1)], non_blocking=True)
+        self._step += 1
+        return self.table
 
 
 def draft_path(head: int, B: int, V: int, r: int, bf16: bool = True) -> int:
