@@ -355,24 +355,46 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
 
 // (max, sum-exp) of all blocks' partials for one (step, request), merged by one warp in a
 // fixed order (deterministic): lane-strided merge, then a butterfly.
+// (max, sum-exp) of all blocks' partials, merged by one warp in a fixed order: each lane issues
+// the loads of up to 8 partials, the warp takes their maximum M, then sums l_i exp(m_i - M)
+// (empty partials are (-inf, 0) and add nothing)
 __device__ __forceinline__ float2 warp_merge_ml(const float2* part, int n, int lane) {
-  float m = -INFINITY, l = 0.f;
-  for (int i = lane; i < n; i += 32) {
-    const float2 q = part[i];
-    lse_merge(m, l, q.x, q.y);
-  }
+  float M = -INFINITY, L = 0.f;
+  for (int i0 = 0; i0 < n; i0 += 256) {
+    float2 q[8];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
-    lse_merge(m, l, m2, l2);
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + lane + 32 * j;
+      q[j] = i < n ? part[i] : make_float2(-INFINITY, 0.f);
+    }
+    float mb = fmaxf(fmaxf(fmaxf(q[0].x, q[1].x), fmaxf(q[2].x, q[3].x)),
+                     fmaxf(fmaxf(q[4].x, q[5].x), fmaxf(q[6].x, q[7].x)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    const float Mn = fmaxf(M, mb);  // the same in every lane
+    if (Mn == -INFINITY) continue;
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sum += q[j].y * __expf(q[j].x - Mn);
+    L = L * __expf(M - Mn) + sum;
+    M = Mn;
   }
-  return make_float2(m, l);
+  return make_float2(M, warp_sum(L));
 }
 
+// sum of n floats by one warp, up to 8 loads in flight per lane (fixed order)
 __device__ __forceinline__ float warp_sum_strided(const float* part, int n, int lane) {
   float s = 0.f;
-  for (int i = lane; i < n; i += 32) s += part[i];
+  for (int i0 = 0; i0 < n; i0 += 256) {
+    float q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + lane + 32 * j;
+      q[j] = i < n ? part[i] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s += q[j];
+  }
   return warp_sum(s);
 }
 
