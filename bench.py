@@ -176,7 +176,7 @@ def run_reference(args, wl):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": wl.name, "B": wl.B, "gamma": wl.gamma,
-                                        "V": wl.V, "r": wl.r, "d": wl.d},
+                                        "V": wl.V, "r": wl.r, "d": wl.d, "T": wl.T},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "one draft position over the full vocabulary per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
