@@ -40,7 +40,7 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: every timed block starts with a cold
 TRAFFIC = {
     "qwen3_4b_markov": ("draft_cc.cu", "a654b711be85aa4d", 83114240),          # 80.62 + 2.49 MB
     "high_concurrency_sched": ("draft_tc.cu", "4d737546be5bf48d", 5722781952),  # 5715 + 7.4 MB
-    "qwen3_8b_labels": ("draft_tc.cu", "4d737546be5bf48d", 1430964736),         # 1224 + 207 MB
+    # (qwen3_8b_labels: two launches per call since the target pre-pass; no single-kernel record)
     "rnn_head": ("draft_tc.cu", "4d737546be5bf48d", 546869248),                 # 541.2 + 5.7 MB
     # the three verify kernels of one call (bench.py --op verify)
     "verify qwen3_8b_labels": ("verify.cu", "256b8f8a4f1f9538", 659341312),
@@ -609,6 +609,8 @@ def main():
         head = 0 if wl.head == "markov" else 1
         launches = ds.draft_launches(head, B, wl.V, wl.r, wl.dtype == "bf16")
         path = ds.draft_path(head, B, wl.V, wl.r, wl.dtype == "bf16")
+        if path == 1 and wl.target_noise is not None:
+            launches += 1  # the target's normalisers, before the draft
         path_name = {0: "cuda-core", 1: "tcgen05, requests on M",
                      2: "tcgen05, vocabulary on M"}.get(path, "none")
         line = {

@@ -303,7 +303,9 @@ const char* dspark_last_error(void);
  */
 int dspark_draft_path(int head, int B, int V, int r, dspark_dtype wdt);
 
-/* Number of kernel launches one draft call with these arguments makes on its stream. */
+/* Number of kernel launches one draft call with these arguments makes on its stream, without a
+ * target (on path 1 a target adds one: its normalisers are formed by a streaming launch before
+ * the draft). */
 int dspark_draft_launches(int head, int B, int V, int r, dspark_dtype wdt);
 
 #ifdef __cplusplus

@@ -2,6 +2,7 @@
 // workspace layout, kernel-path selection and stream-ordered launches.  No torch types, no
 // allocation; the only process-wide state is a per-device cache of SM count and shared-memory
 // limit (filled once, under a mutex).
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -76,8 +77,8 @@ WsLayout ws_layout(int head, int B, int G, int V, int r, int nCTA, int flags) {
   off = align256(off + (size_t)2 * G * B * 4);
   L.ml = off;
   off = align256(off + (size_t)G * B * nCTA * 8);
-  L.mlt = off;
-  off = align256(off + (size_t)G * B * nCTA * 8);
+  L.mlt = off;  // per-block partials (CUDA-core path) or per-chunk target partials (tensor cores)
+  off = align256(off + (size_t)G * B * std::max(nCTA, (V + 16383) / 16384) * 8);
   L.l1p = off;
   off = align256(off + (size_t)G * B * nCTA * 4);
   const bool rnn = head == 1;

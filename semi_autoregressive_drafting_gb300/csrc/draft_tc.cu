@@ -20,7 +20,9 @@
 //   * per step, each block publishes one candidate per request with a 64-bit atomicMax on an
 //     order-independent key, then a bounded grid barrier; the Eq 8 label runs its second pass
 //     over the block's slice from y saved in the workspace, after the barrier and while the
-//     next step's first MMAs run;
+//     next step's first MMAs run; the target's normalisers, which do not depend on the drafted
+//     tokens, come from a streaming launch before the draft (target_part_kernel), so the
+//     epilogue never reads the target;
 //   * the two spare warps compute Eq 7's w[:d] . h_k for the block's own requests up front (it
 //     does not depend on the drafted tokens); after the last step one warp per owned (request,
 //     position) finishes the token, the log-normaliser, c_k and Eq 8, then S_k.
@@ -309,6 +311,77 @@ __device__ __forceinline__ int cond_token(const DraftParams& p, int b, int ks, b
   return ok ? x : 0;
 }
 
+// ------------------------------------------------------------------ target normalisers
+// The target's log-normaliser of every (request, position) row does not depend on the drafted
+// tokens, so it is formed before the draft, at streaming speed, instead of inside the latency-
+// bound epilogue: (max, sum exp) of t / T over each 16384-entry chunk, natural units, in
+// mlt[(k B + b) ntp + chunk]; the Eq 8 second pass merges a row's ntp partials.
+constexpr int kTChunk = 16384;
+constexpr int kTThr = 256;
+__host__ __device__ inline int target_chunks(int V) { return (V + kTChunk - 1) / kTChunk; }
+
+__global__ void __launch_bounds__(kTThr) target_part_kernel(const float* __restrict__ tgt, int B, int G,
+                                                            int V, float s2, float2* __restrict__ mlt) {
+  __shared__ float2 red[kTThr / 32];
+  const int ntp = target_chunks(V);
+  const long long blk = blockIdx.x, row = blk / ntp;  // row = b G + k
+  const int ch = (int)(blk % ntp);
+  const int b = (int)(row / G), k = (int)(row % G);
+  const float* t = tgt + row * V;
+  const int v0 = ch * kTChunk, v1 = min(V, v0 + kTChunk);
+  float m = -INFINITY, l = 0.f;  // log2 units here
+  if ((V & 3) == 0) {  // 16-byte aligned rows: all sixteen loads of a thread at once
+    const float4* t4 = (const float4*)(t + v0);
+    const int n4 = (v1 - v0) >> 2;
+    float4 q[kTChunk / 4 / kTThr];
+#pragma unroll
+    for (int u = 0; u < kTChunk / 4 / kTThr; ++u) {
+      const int i = (int)threadIdx.x + u * kTThr;
+      q[u] = i < n4 ? __ldcs(t4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kTChunk / 4 / kTThr; ++u) mx = fmaxf(mx, fmaxf(fmaxf(q[u].x, q[u].y), fmaxf(q[u].z, q[u].w)));
+    if (mx != -INFINITY) {
+      m = mx * s2;
+#pragma unroll
+      for (int u = 0; u < kTChunk / 4 / kTThr; ++u)
+        l += ex2f(fmaf(q[u].x, s2, -m)) + ex2f(fmaf(q[u].y, s2, -m)) + ex2f(fmaf(q[u].z, s2, -m)) +
+             ex2f(fmaf(q[u].w, s2, -m));
+    }
+  } else {
+    for (int v = v0 + (int)threadIdx.x; v < v1; v += kTThr) {
+      const float y = t[v] * s2;
+      if (y > m) {
+        l = l * ex2f(m - y) + 1.f;
+        m = y;
+      } else {
+        l += ex2f(y - m);
+      }
+    }
+  }
+  auto merge2 = [](float& a, float& c, float a2, float c2) {
+    if (c2 == 0.f) return;
+    if (c == 0.f) {
+      a = a2;
+      c = c2;
+      return;
+    }
+    const float mm = fmaxf(a, a2);
+    c = c * ex2f(a - mm) + c2 * ex2f(a2 - mm);
+    a = mm;
+  };
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) merge2(m, l, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, l, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_float2(m, l);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = -INFINITY, c = 0.f;
+    for (int w = 0; w < kTThr / 32; ++w) merge2(a, c, red[w].x, red[w].y);
+    mlt[((size_t)k * B + b) * ntp + ch] = make_float2(a * kLn2, c);  // natural units
+  }
+}
+
 template <bool RNN, bool TGT>
 __global__ void __launch_bounds__(kThreads, 1)
     draft_tc_kernel(const DraftParams p, const __grid_constant__ CUtensorMap tmap_w2,
@@ -354,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntile = t1 - t0;
   const int nround = pk ? (ntile + 1) / 2 : ntile;  // accumulator rounds per chunk
   const int sl0 = t0 * kNT, sl1 = min(V, t1 * kNT);  // vocab slice [sl0, sl1)
+  const int ntp = target_chunks(V);  // target normaliser partials per row (target_part_kernel)
 
   if (tid == 0) {
     for (int i = 0; i < nstage; ++i) {
@@ -584,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int v = vb + 8 * gi;
     if (!FAST && v >= V) return;
     const bool full = FAST || v + 8 <= V;
-    float z[8], tv[8];
+    float z[8];
     uint4 uq = make_uint4(0, 0, 0, 0);
     bool vq = false;
     if (FAST || nu > 0) {  // staged: 16-byte chunk (cq % 2) * 4 + gi of the row sits at chunk ^ (row % 8)
@@ -599,17 +673,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       bf16x8(uq, uf);
 #pragma unroll
       for (int e = 0; e < 8; ++e) z[e] = uf[e] + __uint_as_float(bs[e]);
-      if (TGT) {
-        if (FAST || vec_t) {
-          const float4 a = *(const float4*)(tgp + urow + v);
-          const float4 c4 = *(const float4*)(tgp + urow + v + 4);
-          tv[0] = a.x; tv[1] = a.y; tv[2] = a.z; tv[3] = a.w;
-          tv[4] = c4.x; tv[5] = c4.y; tv[6] = c4.z; tv[7] = c4.w;
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) tv[e] = tgp[urow + v + e];
-        }
-      }
     } else {  // the slice's ragged end, or U rows without 16-byte alignment
       float uf[8];
       bf16x8(uq, uf);
@@ -618,7 +681,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int vv = v + e;
         const float uval = vq ? uf[e] : (vv < V ? ld_u(Up, urow + vv, p.u_bf16) : 0.f);
         z[e] = vv < V ? uval + __uint_as_float(bs[e]) : -INFINITY;
-        if (TGT) tv[e] = vv < V ? tgp[urow + vv] : -INFINITY;
       }
     }
     if (!FAST && lgp)  // debug output: z
@@ -673,23 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tb = fmaxf(tb, st.best);
       Cp = 1.002f * ex2f(st.m - tb);
     }
-    if (TGT) {
-      float tmax = -INFINITY;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        tv[e] *= s2;
-        tmax = fmaxf(tmax, tv[e]);
-      }
-      if (tmax > st.mt) {
-        st.lt *= ex2f(st.mt - tmax);
-        st.mt = tmax;
-      }
-      float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if (e & 1) a1 += ex2f(tv[e] - st.mt); else a0 += ex2f(tv[e] - st.mt);
-      }
-      st.lt += a0 + a1;
+    if (TGT) {  // the target's normalisers come from target_part_kernel
       float* yo = ybp + (size_t)b * V + v;  // y2 = z s2, read back by the second pass
       if (FAST || (vec_t && full)) {
         *(float4*)yo = make_float4(z[0] * s2, z[1] * s2, z[2] * s2, z[3] * s2);
@@ -708,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto second_pass = [&](int kp) {
     for (int b = ew; b < B; b += kEpiWarps) {
       const float2 a = merge_ml(p.ml + ((size_t)kp * B + b) * nCTA, nCTA, lane);
-      const float2 tt = merge_ml(p.mlt + ((size_t)kp * B + b) * nCTA, nCTA, lane);
+      const float2 tt = merge_ml(p.mlt + ((size_t)kp * B + b) * ntp, ntp, lane);
       const float Ld2 = (a.x + logf(a.y)) * kLog2e, Lt2 = (tt.x + logf(tt.y)) * kLog2e;
       const float* yr = ybp + (size_t)b * V;
       const float* tr = tgp + ((size_t)b * G + kp) * V;
@@ -850,7 +896,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row_ok && t + 3 * tstep < ntile) {  // this thread's U and target lines, 3 rounds ahead
           const size_t vp = urow + (size_t)(t0 + t + 3 * tstep) * kNT + cq * 32;
           if (nu > 0) prefetch_line((const __nv_bfloat16*)Up + vp);
-          if (TGT) prefetch_line(tgp + vp);
         }
         // the tile's U: staged by TMA, kept until the tile is done; else read from global
         int us = -1;
@@ -932,7 +977,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         cond_token(p, b, ks, &valid);
         if (valid && ntile > 0 && sl1 > sl0) atomicMax(&p.keys[(size_t)ks * B + b], make_key(st.best, st.tok));
         p.ml[((size_t)ks * B + b) * nCTA + cta] = make_float2(st.m, st.l);
-        if (tgt) p.mlt[((size_t)ks * B + b) * nCTA + cta] = make_float2(st.mt, st.lt);
       }
       esync<kEpiThreads>();
     }
@@ -1096,6 +1140,13 @@ cudaError_t launch_draft_tc(DraftParams& p, int nblocks, cudaStream_t stream) {
   std::memset(&tmap_u, 0, sizeof tmap_u);
   if (p.tc_nu > 0 && !encode_u_bf16_3d(&tmap_u, p.U, p.B, p.gamma, p.V, p.tc_pk ? 64 : 128))
     return cudaErrorInvalidValue;
+  if (tg) {  // the target's normalisers first, on the same stream
+    const int ntp = target_chunks(p.V);
+    target_part_kernel<<<(unsigned)((long long)p.B * p.gamma * ntp), kTThr, 0, stream>>>(
+        p.target, p.B, p.gamma, p.V, p.invT * kLog2e, p.mlt);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   int na = p.tc_na, ns = p.nstages, nu = p.tc_nu;
   void* args[] = {(void*)&p, (void*)&tmap, (void*)&tmap_u, (void*)&na, (void*)&ns, (void*)&nu};
   return cudaLaunchCooperativeKernel(kern, dim3(nblocks), dim3(kThreads), args, p.smem_bytes, stream);
