@@ -39,9 +39,9 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: every timed block starts with a cold
 # without a capture, or whose kernel changed since, reports null.
 TRAFFIC = {
     "qwen3_4b_markov": ("draft_cc.cu", "a654b711be85aa4d", 83114240),          # 80.62 + 2.49 MB
-    "high_concurrency_sched": ("draft_tc.cu", "4d737546be5bf48d", 5722781952),  # 5715 + 7.4 MB
+    "high_concurrency_sched": ("draft_tc.cu", "3aaea69704e3ef26", 5723947520),  # 5717 + 7.4 MB
     # (qwen3_8b_labels: two launches per call since the target pre-pass; no single-kernel record)
-    "rnn_head": ("draft_tc.cu", "4d737546be5bf48d", 546869248),                 # 541.2 + 5.7 MB
+    "rnn_head": ("draft_tc.cu", "3aaea69704e3ef26", 538618880),                 # 533.8 + 4.8 MB
     # the three verify kernels of one call (bench.py --op verify)
     "verify qwen3_8b_labels": ("verify.cu", "256b8f8a4f1f9538", 659341312),
 }
