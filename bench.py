@@ -435,7 +435,7 @@ def run_loss(args, wl, rank, world, local_rank):
                          "kernel": "loss_part + loss_stat + loss_grad + loss_final"},
             "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": "blocks/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": ds.draft_loss_launches(B, G, V, True) * args.steps,
             "clocks": clk.summary(),
             "ms_per_step_min": min(times), "ms_per_step_median": statistics.median(times),
         }
@@ -611,6 +611,10 @@ def main():
         path = ds.draft_path(head, B, wl.V, wl.r, wl.dtype == "bf16")
         if path == 1 and wl.target_noise is not None:
             launches += 1  # the target's normalisers, before the draft
+        kernel_name = "draft_tc_kernel" if path == 1 else "draft_cc_kernel"
+        # achieved covers the whole call: with launches before the draft kernel (the RNN head's
+        # h-part GEMM, the target's normalisers) their time is in ms_step too
+        scope = "one launch" if launches == 1 else f"whole call, {launches} launches"
         path_name = {0: "cuda-core", 1: "tcgen05, requests on M",
                      2: "tcgen05, vocabulary on M"}.get(path, "none")
         line = {
@@ -626,7 +630,8 @@ def main():
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_kind": f"{peak_kind} copy bandwidth",
                          "algorithmic_bytes_per_launch": alg,
-                         "kernel": "draft_tc_kernel" if path == 1 else "draft_cc_kernel"},
+                         "kernel": kernel_name, "scope": scope,
+                         "traffic_scope": f"{kernel_name}, one launch"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "cuda_graph": graph is not None, "results_copied": res_ok},

@@ -217,7 +217,8 @@ dspark_status dspark_verify(int B, int gamma, int V, float T, uint64_t seed,
  * fp32.  workspace: dspark_draft_loss_workspace_bytes(B, gamma, V) bytes, 256-byte aligned
  * (contents need not be zero).  Limits: 1 <= gamma <= 16, 2 <= V <= 2^24, T finite and > 0.
  * A label outside [0, V) makes every output of its request NaN and sets DSPARK_ERR_INVALID in
- * the workspace status.  Three or four launches on `stream`.
+ * the workspace status.  Three launches on `stream`, four with grad_logits
+ * (dspark_draft_loss_launches).
  */
 size_t dspark_draft_loss_workspace_bytes(int B, int gamma, int V);
 dspark_status dspark_draft_loss(int B, int gamma, int V, float T, const float* draft_logits,
@@ -307,6 +308,10 @@ int dspark_draft_path(int head, int B, int V, int r, dspark_dtype wdt);
  * target (on path 1 a target adds one: its normalisers are formed by a streaming launch before
  * the draft). */
 int dspark_draft_launches(int head, int B, int V, int r, dspark_dtype wdt);
+
+/* Number of kernel launches one dspark_draft_loss call makes on its stream (with_grad: whether
+ * grad_logits is given).  Negative for arguments it would reject. */
+int dspark_draft_loss_launches(int B, int gamma, int V, int with_grad);
 
 #ifdef __cplusplus
 }

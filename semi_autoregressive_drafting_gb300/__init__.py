@@ -19,7 +19,8 @@ import torch
 from . import _lib
 
 __all__ = ["Workspace", "markov_draft", "rnn_draft", "confidence", "tv_label",
-           "prefix_schedule", "draft_path", "draft_launches", "DraftOutput", "DraftPlan",
+           "prefix_schedule", "draft_path", "draft_launches", "draft_loss_launches",
+           "DraftOutput", "DraftPlan",
            "VerifyWorkspace", "verify", "LossWorkspace", "draft_loss", "sts", "CapacityRing"]
 
 _F32, _BF16 = 0, 1
@@ -339,3 +340,8 @@ def draft_path(head: int, B: int, V: int, r: int, bf16: bool = True) -> int:
 
 def draft_launches(head: int, B: int, V: int, r: int, bf16: bool = True) -> int:
     return _lib.load().dspark_draft_launches(head, B, V, r, _BF16 if bf16 else _F32)
+
+
+def draft_loss_launches(B: int, gamma: int, V: int, with_grad: bool = True) -> int:
+    """Kernel launches of one draft_loss call (the sub-batch pipeline and the totals)."""
+    return _lib.load().dspark_draft_loss_launches(B, gamma, V, int(with_grad))

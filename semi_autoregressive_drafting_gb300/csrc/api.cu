@@ -446,6 +446,12 @@ int dspark_draft_path(int head, int B, int V, int r, dspark_dtype wdt) {
   return path_of(head, B, V, r, wdt == DSPARK_BF16, nCTA);
 }
 
+int dspark_draft_loss_launches(int B, int gamma, int V, int with_grad) {
+  if (B < 1 || B > (1 << 20) || gamma < 1 || gamma > 16 || V < 2 || V > (1 << 24)) return -1;
+  // launch_loss: the normalisers, the |p - q| sums, the gradient (when asked) and the totals
+  return with_grad ? 4 : 3;
+}
+
 int dspark_draft_launches(int head, int B, int V, int r, dspark_dtype wdt) {
   const int p = dspark_draft_path(head, B, V, r, wdt);
   if (p < 0) return -1;

@@ -81,3 +81,15 @@ def test_path_selection(lib, monkeypatch):
     assert lib.dspark_draft_path(0, 4, 151936, 72, 1) == 0       # rank not in 64-blocks: CUDA cores
     assert lib.dspark_draft_path(0, 4, 4096, 64, 0) == 0
     assert lib.dspark_draft_path(0, 1, 151936, 250, 1) == -1     # invalid rank
+
+
+def test_launch_counts(lib, monkeypatch):
+    monkeypatch.delenv("DSPARK_DRAFT_PATH", raising=False)
+    assert lib.dspark_draft_launches(0, 1, 151936, 256, 1) == 1     # one persistent launch
+    assert lib.dspark_draft_launches(1, 128, 151936, 256, 1) == 2   # + the RNN head's h-part GEMM
+    assert lib.dspark_draft_launches(0, 1, 151936, 250, 1) == -1
+    assert lib.dspark_draft_loss_launches(64, 7, 151936, 1) == 4    # three phases + totals
+    assert lib.dspark_draft_loss_launches(64, 7, 151936, 0) == 3    # no gradient pass
+    assert lib.dspark_draft_loss_launches(0, 7, 151936, 1) == -1
+    assert lib.dspark_draft_loss_launches(1, 17, 151936, 1) == -1
+    assert lib.dspark_draft_loss_launches(1, 7, 1, 1) == -1
