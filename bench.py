@@ -40,10 +40,13 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: every timed block starts with a cold
 TRAFFIC = {
     "qwen3_4b_markov": ("draft_cc.cu", "a654b711be85aa4d", 83114240),          # 80.62 + 2.49 MB
     "high_concurrency_sched": ("draft_tc.cu", "3aaea69704e3ef26", 5723947520),  # 5717 + 7.4 MB
-    # (qwen3_8b_labels: two launches per call since the target pre-pass; no single-kernel record)
+    # draft_tc_kernel alone; the target's normalisers (272.4 MB) are a launch before it
+    "qwen3_8b_labels": ("draft_tc.cu", "3aaea69704e3ef26", 1085017856),         # 974.3 + 110.7 MB
     "rnn_head": ("draft_tc.cu", "3aaea69704e3ef26", 538618880),                 # 533.8 + 4.8 MB
     # the three verify kernels of one call (bench.py --op verify)
     "verify qwen3_8b_labels": ("verify.cu", "256b8f8a4f1f9538", 659341312),
+    # the four loss kernels of one call (bench.py --op loss), summed from per-kernel MB figures
+    "loss qwen3_8b_labels": ("loss.cu", "363d54374066fc09", 1873500000),
 }
 
 
@@ -419,6 +422,9 @@ def run_loss(args, wl, rank, world, local_rank):
         # the least the step must move: both logit arrays read once, the logit gradient written once
         alg = 3 * B * G * V * 4 + B * G * 4 * 3
         achieved = alg / (ms * 1e-3) / 1e9
+        cap = TRAFFIC.get("loss " + wl.name)
+        src = cap and os.path.join(ROOT, "semi_autoregressive_drafting_gb300", "csrc", cap[0])
+        traffic = cap[2] if cap and _sha(src) == cap[1] else None
         line = {
             "metric": LOSS_METRIC, "value": world * B / (ms * 1e-3), "unit": "blocks/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -429,7 +435,7 @@ def run_loss(args, wl, rank, world, local_rank):
                        "l2": "flushed between timed calls (512 MB write)",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak, "traffic": traffic,
                          "peak_kind": f"{peak_kind} copy bandwidth",
                          "algorithmic_bytes_per_launch": alg,
                          "kernel": "loss_part + loss_stat + loss_grad + loss_final"},
