@@ -45,8 +45,8 @@ TRAFFIC = {
     "rnn_head": ("draft_tc.cu", "3aaea69704e3ef26", 538618880),                 # 533.8 + 4.8 MB
     # the three verify kernels of one call (bench.py --op verify)
     "verify qwen3_8b_labels": ("verify.cu", "256b8f8a4f1f9538", 659341312),
-    # the four loss kernels of one call (bench.py --op loss), summed from per-kernel MB figures
-    "loss qwen3_8b_labels": ("loss.cu", "363d54374066fc09", 1873500000),
+    # the four loss kernels of one call (bench.py --op loss)
+    "loss qwen3_8b_labels": ("loss.cu", "49dca217d245abe9", 1871840512),
 }
 
 

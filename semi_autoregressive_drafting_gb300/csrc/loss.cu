@@ -174,6 +174,25 @@ __device__ __forceinline__ float2 row_norms(const float4* part, long long row, i
   return make_float2(md + __log2f(ld), mt + __log2f(lt));
 }
 
+// The same for one row per warp: lane i merges partials i, i + 32, ..., then a butterfly merge
+// (commutative, so every lane ends with the same value).  One round of loads for nchunk <= 32.
+__device__ __forceinline__ float2 row_norms_warp(const float4* part, long long row, int nchunk) {
+  float md = -INFINITY, ld = 0.f, mt = -INFINITY, lt = 0.f;
+  for (int c = (int)(threadIdx.x & 31); c < nchunk; c += 32) {
+    const float4 q = part[row * nchunk + c];
+    merge_l2(md, ld, q.x, q.y);
+    merge_l2(mt, lt, q.z, q.w);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float a = __shfl_xor_sync(0xffffffffu, md, o), b = __shfl_xor_sync(0xffffffffu, ld, o);
+    const float c2 = __shfl_xor_sync(0xffffffffu, mt, o), e = __shfl_xor_sync(0xffffffffu, lt, o);
+    merge_l2(md, ld, a, b);
+    merge_l2(mt, lt, c2, e);
+  }
+  return make_float2(md + __log2f(ld), mt + __log2f(lt));
+}
+
 __device__ __forceinline__ float sgn(float x) { return x > 0.f ? 1.f : (x < 0.f ? -1.f : 0.f); }
 
 // ------------------------------------------------------------------ 2. |p - q| and s p sums
@@ -186,7 +205,7 @@ __global__ void __launch_bounds__(kLThr) loss_stat_kernel(const float* __restric
   const int v0 = ch * kLChunk, v1 = min(V, v0 + kLChunk);
   const float* d = zd + row * V;
   const float* t = zt + row * V;
-  const float2 L = row_norms(ws.part, row, nchunk);
+  const float2 L = row_norms_warp(ws.part, row, nchunk);
   float l1 = 0.f, sp = 0.f;
   auto acc = [&](float a, float b) {
     const float p = ex2l(fmaf(a, s2, -L.x)), q = ex2l(fmaf(b, s2, -L.y));
@@ -211,36 +230,41 @@ __global__ void __launch_bounds__(kLThr) loss_stat_kernel(const float* __restric
 }
 
 // ------------------------------------------------------------------ 3. dL / d draft logits
-__global__ void __launch_bounds__(kLThr) loss_grad_kernel(
+__global__ void __launch_bounds__(kLThr, 3) loss_grad_kernel(
     const float* __restrict__ zd, const float* __restrict__ zt, const int32_t* __restrict__ lab,
     int G, int V, float s2, float invT, float a_ce, float a_tv, int nchunk, LossWs ws,
     float* __restrict__ grad) {
   const long long blk = blockIdx.x, row = blk / nchunk;
   const int ch = (int)(blk % nchunk);
   const int v0 = ch * kLChunk, v1 = min(V, v0 + kLChunk);
+  const float* d = zd + row * V;
+  const float* t = zt + row * V;
+  const int n4 = (v1 - v0) >> 2;
+  Chunk c;
+  if ((V & 3) == 0) load_chunk(c, d + v0, t + v0, n4);  // in flight during the row's totals
+  const int lane = (int)(threadIdx.x & 31);
   const int x = lab[row];
   float* g = grad + row * V;
-  bool ok = true;  // every label of the request (an invalid one makes all its outputs NaN)
-  for (long long j = row - row % G; j < row - row % G + G; ++j) ok = ok && lab[j] >= 0 && lab[j] < V;
+  // every label of the request, one lane each (an invalid one makes all its outputs NaN)
+  const long long j0 = row - row % G;
+  const int lj = lane < G ? lab[j0 + lane] : 0;
+  const bool ok = __all_sync(0xffffffffu, lj >= 0 && lj < V);
   if (!ok) {  // invalid request: NaN gradient (the final kernel reports it)
     for (int v = v0 + (int)threadIdx.x; v < v1; v += kLThr) g[v] = NAN;
     return;
   }
-  const float2 L = row_norms(ws.part, row, nchunk);
-  float S = 0.f;
-  for (int c = 0; c < nchunk; ++c) S += ws.stat[row * nchunk + c].y;
+  const float2 L = row_norms_warp(ws.part, row, nchunk);
+  float S = 0.f;  // sum s p over the row: lane-strided, then a butterfly (the same in every lane)
+  for (int ch2 = lane; ch2 < nchunk; ch2 += 32) S += ws.stat[row * nchunk + ch2].y;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
   const int k0 = (int)(row % G);  // position k - 1
   const float wT = __expf(-(float)k0 / (float)G) * invT;
-  const float* d = zd + row * V;
-  const float* t = zt + row * V;
   auto gv = [&](float a, float b, int v) {
     const float p = ex2l(fmaf(a, s2, -L.x)), q = ex2l(fmaf(b, s2, -L.y));
     return wT * (a_ce * (p - (v == x ? 1.f : 0.f)) + a_tv * p * (sgn(p - q) - S));
   };
   if ((V & 3) == 0) {
-    Chunk c;
-    const int n4 = (v1 - v0) >> 2;
-    load_chunk(c, d + v0, t + v0, n4);
 #pragma unroll
     for (int u = 0; u < kLPer; ++u) {
       const int i = (int)threadIdx.x + u * kLThr;
