@@ -61,7 +61,7 @@ typedef enum {
   DSPARK_ERR_WORKSPACE = 2,   /* workspace NULL, misaligned, or smaller than required        */
   DSPARK_ERR_CUDA = 3,        /* a CUDA runtime call failed; see dspark_last_error()         */
   DSPARK_ERR_TIMEOUT = 4,     /* a device-side wait between thread blocks ran out (device)   */
-  DSPARK_ERR_UNSUPPORTED = 5  /* valid arguments this build has no kernel for                */
+  DSPARK_ERR_UNSUPPORTED = 5  /* valid arguments that no kernel of the library runs            */
 } dspark_status;
 
 typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;

@@ -176,7 +176,7 @@ dspark_status run_draft(const DraftArgs& a) {
   const int w_bf16 = a.wdt == DSPARK_BF16, u_bf16 = a.udt == DSPARK_BF16;
   const int path = path_of(a.head, a.B, a.V, a.r, w_bf16, nCTA);
   if (path < 0)
-    return fail(DSPARK_ERR_UNSUPPORTED, "no kernel for head=%d B=%d r=%d dtype=%d in this build",
+    return fail(DSPARK_ERR_UNSUPPORTED, "no kernel of the library runs head=%d B=%d r=%d dtype=%d",
                 a.head, a.B, a.r, (int)a.wdt);
 
   DraftParams p;
