@@ -50,6 +50,22 @@ TRAFFIC = {
 }
 
 
+def ranks_max(dist, values, device="cuda"):
+    """Each timing's maximum over the ranks (the slowest replica sets the job's time); the
+    values unchanged on one process (dist None)."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rate(world, units_per_rank, ms):
+    """Whole-job throughput: every rank processes units_per_rank units per step of ms."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def _sha(path):
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
@@ -287,10 +303,7 @@ def run_verify(args, wl, rank, world, local_rank):
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
     e2e_ms /= e2e_steps
-    if dist:
-        tt = torch.tensor([ms, e2e_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = tt.tolist()
+    ms, e2e_ms = ranks_max(dist, [ms, e2e_ms])
     if rank == 0:
         peak, peak_kind = load_peaks()
         # what the step must move: every draft row and every target row once (the
@@ -301,7 +314,7 @@ def run_verify(args, wl, rank, world, local_rank):
         src = cap and os.path.join(ROOT, "semi_autoregressive_drafting_gb300", "csrc", cap[0])
         traffic = cap[2] if cap and _sha(src) == cap[1] else None
         line = {
-            "metric": VERIFY_METRIC, "value": world * B / (ms * 1e-3), "unit": "blocks/s",
+            "metric": VERIFY_METRIC, "value": job_rate(world, B, ms), "unit": "blocks/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
@@ -314,7 +327,7 @@ def run_verify(args, wl, rank, world, local_rank):
                          "peak_kind": f"{peak_kind} copy bandwidth",
                          "algorithmic_bytes_per_launch": alg,
                          "kernel": "verify_part_kernel + verify_decide_kernel + verify_draw_kernel"},
-            "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": "blocks/s",
+            "e2e": {"value": job_rate(world, B, e2e_ms), "unit": "blocks/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": 3 * args.steps,
             "clocks": clk.summary(),
@@ -413,10 +426,7 @@ def run_loss(args, wl, rank, world, local_rank):
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
     e2e_ms /= e2e_steps
-    if dist:
-        tt = torch.tensor([ms, e2e_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = tt.tolist()
+    ms, e2e_ms = ranks_max(dist, [ms, e2e_ms])
     if rank == 0:
         peak, peak_kind = load_peaks()
         # the least the step must move: both logit arrays read once, the logit gradient written once
@@ -426,7 +436,7 @@ def run_loss(args, wl, rank, world, local_rank):
         src = cap and os.path.join(ROOT, "semi_autoregressive_drafting_gb300", "csrc", cap[0])
         traffic = cap[2] if cap and _sha(src) == cap[1] else None
         line = {
-            "metric": LOSS_METRIC, "value": world * B / (ms * 1e-3), "unit": "blocks/s",
+            "metric": LOSS_METRIC, "value": job_rate(world, B, ms), "unit": "blocks/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
@@ -439,7 +449,7 @@ def run_loss(args, wl, rank, world, local_rank):
                          "peak_kind": f"{peak_kind} copy bandwidth",
                          "algorithmic_bytes_per_launch": alg,
                          "kernel": "loss_part + loss_stat + loss_grad + loss_final"},
-            "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": "blocks/s",
+            "e2e": {"value": job_rate(world, B, e2e_ms), "unit": "blocks/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": ds.draft_loss_launches(B, G, V, True) * args.steps,
             "clocks": clk.summary(),
@@ -598,12 +608,9 @@ def main():
     assert ws.status() == 0, "draft kernel reported a device error (end-to-end loop)"
 
     # ---- max over ranks
-    if dist:
-        tt = torch.tensor([ms_step, e2e_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step, e2e_ms = tt.tolist()
-    value = world * B * G / (ms_step * 1e-3)
-    e2e_value = world * B * G / (e2e_ms * 1e-3)
+    ms_step, e2e_ms = ranks_max(dist, [ms_step, e2e_ms])
+    value = job_rate(world, B * G, ms_step)
+    e2e_value = job_rate(world, B * G, e2e_ms)
 
     if rank == 0:
         peak, peak_kind = load_peaks()
