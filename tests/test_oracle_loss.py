@@ -2,22 +2,36 @@
 and their gradients.
 
 * The position weights w_k = exp(-(k-1)/gamma) against the values the same page prints in its
-  delta table (D2): [1, .78, .61, .47] at gamma = 4 (exactly, to the printed two decimals) and
-  [1, .87, .75, .65, .57, .49, .43] at gamma = 7 (to 0.01: two of those entries, .57 and .43, do
-  not round from the formula the page states, which gives .565 and .424).  They are read off
-  dL/d(confidence logit) = a_conf w_k (c - c*) at c = 1/2, c* = 1.
+  delta table (D2), stored in tests/golden/loss_constants.txt: [1, .78, .61, .47] at gamma = 4
+  (exactly, to the printed two decimals) and [1, .87, .75, .65, .57, .49, .43] at gamma = 7 (to
+  0.01: two of those entries, .57 and .43, do not round from the formula the page states, which
+  gives .565 and .424).  They are read off dL/d(confidence logit) = a_conf w_k (c - c*) at
+  c = 1/2, c* = 1.
 * Every analytic gradient against central differences of the oracle's own loss.  c* is a label
   (no gradient through it), so the logit gradient is checked with a_conf = 0; the confidence
   logits do not move c*, so their gradient is checked with every weighting.
 * L1 on probabilities, not logits (D6): logits shifted by a constant give L_tv = 0 and c* = 1.
 * L_ce gathers log p at the label (D5): a uniform draft gives ln V per position, a one-hot draft 0.
-* The alpha defaults (D4): L = 0.1 L_ce + 0.9 L_tv + 1.0 L_conf.
+* The alpha defaults (D4, in the same golden file): L = 0.1 L_ce + 0.9 L_tv + 1.0 L_conf.
 * Disjoint supports give ||p - q||_1 = 2, so c* = 0 and L_conf = -sum w ln(1 - c).
 """
+import os
+
 import numpy as np
 import pytest
 
 from oracle import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "loss_constants.txt")
+
+
+def printed(name):
+    """The numbers on the line `name` of the golden file of printed loss constants."""
+    for line in open(GOLDEN):
+        f = line.split()
+        if f and f[0] == name:
+            return [float(x) for x in f[1:]]
+    raise KeyError(name)
 
 
 def inputs(B, G, V, seed, noise=1.0):
@@ -29,15 +43,14 @@ def inputs(B, G, V, seed, noise=1.0):
     return zd, zt, lab, cf
 
 
-@pytest.mark.parametrize("G,printed,tol", [(4, [1, .78, .61, .47], 1e-12),
-                                           (7, [1, .87, .75, .65, .57, .49, .43], 0.0100001)])
-def test_position_weights_match_the_printed_values(G, printed, tol):
+@pytest.mark.parametrize("G,tol", [(4, 1e-12), (7, 0.0100001)])
+def test_position_weights_match_the_printed_values(G, tol):
     V = 5
     zd = np.zeros((1, G, V), np.float32)
     r = oracle.draft_loss(T=1.0, draft_logits=zd, target_logits=zd, labels=np.zeros((1, G), np.int32),
                           conf_logits=np.zeros((1, G), np.float32), alpha=(0.1, 0.9, 1.0))
     w = -2.0 * r.grad_conf[0]  # a_conf = 1, c = 1/2, c* = 1
-    assert np.all(np.abs(np.round(w, 2) - printed) <= tol)
+    assert np.all(np.abs(np.round(w, 2) - printed(f"weights_gamma{G}")) <= tol)
     assert abs(w[0] - 1.0) < 1e-15 and abs(w[-1] - np.exp(-(G - 1) / G)) < 1e-15
 
 
@@ -105,7 +118,7 @@ def test_cross_entropy_gathers_at_the_label():
 def test_alpha_defaults_combine_the_parts():
     zd, zt, lab, cf = inputs(3, 7, 50, seed=8)
     r = oracle.draft_loss(T=1.0, draft_logits=zd, target_logits=zt, labels=lab, conf_logits=cf)
-    assert np.allclose(r.loss, r.parts @ np.array([0.1, 0.9, 1.0]), rtol=0, atol=1e-12)
+    assert np.allclose(r.loss, r.parts @ np.array(printed("alpha")), rtol=0, atol=1e-12)
 
 
 def test_disjoint_supports():
