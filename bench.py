@@ -3,12 +3,14 @@
 
 One step = one draft block (all gamma positions) of the workload: W1 gather, bias product,
 logits, temperature softmax normaliser, Philox Gumbel-max sampling, Eq 7 confidence and the
-prefix survival, all in libdspark's kernels.  The default workload is the Qwen3-4B-shaped
-latency regime (B=1, gamma=7, V=151936, r=256, d=2560, bf16).  The metric is draft tokens/s
-(B * gamma per block), plus the achieved HBM bandwidth of the draft kernel against the measured
-copy bandwidth.
+prefix survival, all in libdspark's kernels.  The default workload is the largest one that
+fits one GPU, the high-concurrency tensor-core regime (B=512, gamma=7, V=262144, r=256,
+d=3840, bf16); ``--workload`` picks another (qwen3_4b_markov is the B=1 latency regime).  The
+metric is draft tokens/s (B * gamma per block), plus the achieved HBM bandwidth of the draft
+call against the measured copy bandwidth and, on the tensor-core paths, the bias product's
+bf16 throughput against the measured cuBLAS burst peak.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload W]
 
 With N > 1 (torchrun), every rank drafts its own independent requests (weak scaling, no
 collective on the data path); value = all ranks' tokens / the slowest rank's time.
@@ -108,26 +110,126 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
+def load_tensor_peak():
+    """Measured dense bf16 throughput (cuBLAS burst: the draft call is timed on its own)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        if "bf16_tflops" in j:
+            return float(j["bf16_tflops"]), "measured cuBLAS bf16 burst"
+    return 1900.0, "fallback bf16 burst"
+
+
+def algorithmic_flops(wl) -> int:
+    """Dense multiply-adds of one block, 2 flops each: the bias product e W2^T (B x r x V per
+    step) and, for the RNN head, the joint projection Wj z_k (B x 3r x (2r + d) per step)."""
+    per_step = 2 * wl.B * wl.r * wl.V
+    if wl.head == "rnn":
+        per_step += 2 * wl.B * 3 * wl.r * (2 * wl.r + wl.d)
+    return wl.gamma * per_step
+
+
+# What limits each workload's draft call, from its ncu captures (profiles/).  The roofline's
+# "bound" is the roof the call's arithmetic intensity puts it under (HBM for every workload:
+# the B = 512 bias product has about 169 flop/B against a ridge near 285); "limiter" names what
+# the counters show actually sets the time.
+LIMITER = {
+    "qwen3_4b_markov": "latency of the gamma - 1 sequential grid steps: W2 stays in TMEM and L2 "
+                       "across steps, so DRAM moves about 0.15x the algorithmic bytes "
+                       "(profiles/draft_cc_qwen3_4b_markov.md)",
+    "high_concurrency_sched": "instruction issue in the epilogue: Philox noise, the normaliser "
+                              "and the exact skip test for every (request, vocabulary entry) "
+                              "(profiles/draft_tc_high_concurrency_sched.md)",
+    "qwen3_8b_labels": "instruction issue in the epilogue plus the Eq 8 second pass "
+                       "(profiles/draft_tc_qwen3_8b_labels.md)",
+    "rnn_head": "instruction issue in the epilogue and the request owners' recurrent update "
+                "(profiles/draft_tc_rnn_head.md)",
+    "tiny_markov": "launch and grid-step latency (1.1 MB per step)",
+}
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    """SM clock and clock-event (throttle) reasons of one GPU, sampled while the timed region
+    runs.  NVML's read-only queries are polled every 2 ms from a host thread (a timed region of a
+    few tens of milliseconds still gets samples); without NVML, nvidia-smi every 200 ms.  The
+    first sample is taken before __enter__ returns, so the samples cover the whole region."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_s: float = 0.002):
         self.index = index
+        self.period = period_s
         self.proc = None
         self.lines = []
+        self.samples = []      # (sm_mhz, reason bits) from NVML
+        self.smax = None
+        self.source = None
+        self._stop = threading.Event()
+        self._thread = None
+
+    # ---- NVML (libnvidia-ml, part of the driver), read-only queries
+    def _nvml_open(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            return None
+        dev = ctypes.c_void_p()
+        handle_ok = False
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(self.index).uuid)
+            u = u if u.startswith("GPU-") else "GPU-" + u
+            handle_ok = nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(dev)) == 0
+        except Exception:
+            handle_ok = False
+        if not handle_ok and nv.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(dev)) != 0:
+            return None
+        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(dev, 1, ctypes.byref(mx)) == 0:  # 1 = NVML_CLOCK_SM
+            self.smax = float(mx.value)
+        return nv, dev, reasons_fn
+
+    def _nvml_sample(self, nv, dev, reasons_fn):
+        import ctypes
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        if nv.nvmlDeviceGetClockInfo(dev, 1, ctypes.byref(clk)) != 0:
+            return
+        if reasons_fn(dev, ctypes.byref(rs)) != 0:
+            rs.value = 0
+        self.samples.append((float(clk.value), int(rs.value)))
+
+    def _nvml_loop(self, h):
+        while not self._stop.is_set():
+            self._nvml_sample(*h)
+            time.sleep(self.period)
 
     def __enter__(self):
+        h = None
+        try:
+            h = self._nvml_open()
+        except (OSError, AttributeError):
+            h = None
+        if h is not None:
+            self.source = f"nvml every {self.period * 1e3:.0f} ms"
+            self._nvml_sample(*h)
+            self._thread = threading.Thread(target=self._nvml_loop, args=(h,), daemon=True)
+            self._thread.start()
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
+            self._thread = threading.Thread(target=self._read, daemon=True)
+            self._thread.start()
+            self.source = "nvidia-smi every 200 ms"
         except OSError:
             self.proc = None
         return self
@@ -137,15 +239,23 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *exc):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
 
     def summary(self):
-        sm, smax, reasons = [], None, set()
+        sm, smax, reasons = [], self.smax, set()
+        for mhz, bits in self.samples:
+            sm.append(mhz)
+            for bit, name in self.REASONS.items():
+                if bits & bit:
+                    reasons.add(name)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -160,7 +270,7 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": self.source}
 
 
 def run_reference(args, wl):
@@ -461,19 +571,23 @@ def run_loss(args, wl, rank, world, local_rank):
         dist.destroy_process_group()
 
 
-def main():
+def build_parser():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=6000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="qwen3_4b_markov")
+    ap.add_argument("--workload", default="high_concurrency_sched")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", choices=["draft", "verify", "loss"], default="draft",
                     help="draft: the draft block (default); verify: the speculative accept/reject "
                          "step on the workload's B, gamma, V; loss: the training losses (Eqs 9-12) "
                          "and their gradients on that shape")
-    args = ap.parse_args()
+    return ap
+
+
+def main():
+    args = build_parser().parse_args()
     args.warmup = max(args.warmup, 3)
 
     rank = int(os.environ.get("RANK", "0"))
@@ -630,6 +744,24 @@ def main():
         scope = "one launch" if launches == 1 else f"whole call, {launches} launches"
         path_name = {0: "cuda-core", 1: "tcgen05, requests on M",
                      2: "tcgen05, vocabulary on M"}.get(path, "none")
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_kind": f"{peak_kind} copy bandwidth",
+                "algorithmic_bytes_per_launch": alg,
+                "kernel": kernel_name, "scope": scope,
+                "traffic_scope": f"{kernel_name}, one launch"}
+        if traffic is not None:
+            # the bytes that actually crossed HBM (ncu) over the same time: below the
+            # algorithmic fraction when the kernel keeps data on chip across steps
+            roof["dram_frac"] = traffic / (ms_step * 1e-3) / 1e9 / peak
+        if path in (1, 2):
+            tpeak, tkind = load_tensor_peak()
+            flops = algorithmic_flops(wl)
+            tach = flops / (ms_step * 1e-3) / 1e12
+            roof["tensor"] = {"achieved": tach, "peak": tpeak, "unit": "TFLOP/s",
+                              "frac": tach / tpeak, "peak_kind": tkind,
+                              "algorithmic_flops_per_launch": flops}
+        roof["limiter"] = LIMITER.get(wl.name, "not profiled")
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -639,12 +771,7 @@ def main():
                        "T": wl.T, "l2": "flushed between timed blocks (512 MB write)",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                        "path": path_name},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "peak_kind": f"{peak_kind} copy bandwidth",
-                         "algorithmic_bytes_per_launch": alg,
-                         "kernel": kernel_name, "scope": scope,
-                         "traffic_scope": f"{kernel_name}, one launch"},
+            "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "cuda_graph": graph is not None, "results_copied": res_ok},

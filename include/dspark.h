@@ -261,11 +261,15 @@ dspark_status dspark_sts(int N, int gamma, const float* conf_logits, const int32
  *   - Arguments and outputs are those of dspark_markov_draft, minus the workspace.
  *   - status: optional device int32 that receives this call's device status (DSPARK_OK, or the
  *     DSPARK_ERR_INVALID / DSPARK_ERR_TIMEOUT cases described for dspark_markov_draft), written on
- *     `stream` after the draft; NULL to skip.
+ *     `stream` after the draft; NULL to skip.  It is written only when the call returns
+ *     DSPARK_OK: a call rejected on the host leaves it untouched, so check the return code
+ *     before reading it.
  *   - Limit: problems whose dspark_workspace_bytes(0, B, gamma, V, r, d, flags) exceeds 1 MiB are
  *     rejected with DSPARK_ERR_WORKSPACE (in practice the small-batch path, B <= 4).
  *   - The first call on each device looks up the array's device address (once per device, with
- *     that device current); make that first call before any stream capture.
+ *     that device current); make that first call before any stream capture.  The address is
+ *     kept for the life of the process: after cudaDeviceReset on a device, this entry point must
+ *     not be called on that device again in the same process.
  *   - Allocates nothing: each call clears the part of the array it uses (the array keeps the
  *     previous call's contents) and enqueues the draft.  All calls on a device share the one
  *     array, so calls that overlap on the GPU (different streams without ordering) race.

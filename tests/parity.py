@@ -81,25 +81,41 @@ def close(name, gpu, ref, tol=TOL):
     return worst
 
 
-def compare_floats(out, o, rows=None, logits=True):
-    sel = (lambda a: a) if rows is None else (lambda a: a[rows])
-    errs = {"lse": close("lse", sel(out.lse.cpu().numpy()), o.lse)}
+def _rows(a, rows):
+    """The selected request rows of a GPU output, taken on the device before the copy."""
+    if rows is None:
+        return a.cpu().numpy()
+    return a[torch.as_tensor(rows, device=a.device)].cpu().numpy()
+
+
+def compare_floats(out, o, rows=None, logits=True, z_rows=None):
+    """Floats within TOL.  z_rows (a subset of rows) limits the element-wise logits comparison
+    to those requests."""
+    sel = lambda a: _rows(a, rows)
+    errs = {"lse": close("lse", sel(out.lse), o.lse)}
     if o.c is not None and out.c is not None:
-        errs["c"] = close("c", sel(out.c.cpu().numpy()), o.c)
-        errs["S"] = close("S", sel(out.S.cpu().numpy()), o.S)
+        errs["c"] = close("c", sel(out.c), o.c)
+        errs["S"] = close("S", sel(out.S), o.S)
     if o.cstar is not None and out.cstar is not None:
-        errs["cstar"] = close("cstar", sel(out.cstar.cpu().numpy()), o.cstar)
-        errs["l1"] = close("l1", sel(out.l1.cpu().numpy()), o.l1)
+        errs["cstar"] = close("cstar", sel(out.cstar), o.cstar)
+        errs["l1"] = close("l1", sel(out.l1), o.l1)
     if logits and o.z is not None and out.logits is not None:
-        errs["logits"] = close("logits", sel(out.logits.cpu().numpy()), o.z)
+        if z_rows is None:
+            errs["logits"] = close("logits", sel(out.logits), o.z)
+        else:
+            pos = [list(rows).index(r) for r in z_rows] if rows is not None else list(z_rows)
+            errs["logits"] = close("logits", _rows(out.logits, z_rows), o.z[pos])
     if o.s_final is not None and out.s_out is not None:
-        errs["s_out"] = close("s_out", sel(out.s_out.cpu().numpy()), o.s_final)
+        errs["s_out"] = close("s_out", sel(out.s_out), o.s_final)
     return errs
 
 
 def run_case(wl, *, target_noise=None, want_logits=True, rows=None, check_free=True, ds=None,
-             s0_scale=None):
-    """Free-running and teacher-forced GPU draft against the oracle on the same inputs."""
+             s0_scale=None, z_rows=None):
+    """Free-running and teacher-forced GPU draft against the oracle on the same inputs.
+    z_rows (a subset of rows): compare the logits z element-wise on those requests only."""
+    if z_rows is not None:
+        want_logits = True
     if target_noise is not None:
         wl = wl.with_(target_noise=target_noise)
     t = inputs.generate(wl)
@@ -118,19 +134,18 @@ def run_case(wl, *, target_noise=None, want_logits=True, rows=None, check_free=T
                                         s0=d.get("s0"), **kw, **k)
     else:
         call = lambda **k: ds.markov_draft(d["W1"], d["W2"], d["U"], d["x0"], h=d["h"], **kw, **k)
-    sel = (lambda a: a) if rows is None else (lambda a: a[rows])
     ties = 0
     if check_free:
         free = call()
         torch.cuda.synchronize()
         assert ws.status() == 0
-        ties += check_tokens_free(sel(free.tokens.cpu().numpy()), o)
+        ties += check_tokens_free(_rows(free.tokens, rows), o)
     forced = np.zeros((wl.B, wl.gamma), np.int32)
     forced[rows if rows is not None else slice(None)] = o.tokens
     tf = call(forced=torch.from_numpy(forced).cuda(), want_logits=want_logits)
     torch.cuda.synchronize()
     assert ws.status() == 0
-    ties += check_tokens_forced(sel(tf.tokens.cpu().numpy()), o)
-    errs = compare_floats(tf, o, rows=rows, logits=want_logits)
+    ties += check_tokens_forced(_rows(tf.tokens, rows), o)
+    errs = compare_floats(tf, o, rows=rows, logits=want_logits, z_rows=z_rows)
     print(f"{wl.name} B={wl.B} V={wl.V} r={wl.r}: near-ties {ties}, max errors {errs}")
     return ties, errs

@@ -36,3 +36,35 @@ def test_traffic_records_name_existing_sources():
         assert re.fullmatch(r"[0-9a-f]{16}", sha), key
         assert isinstance(nbytes, int) and nbytes > 0, key
         assert key.split()[-1] in inputs.WORKLOADS, key
+
+
+def test_default_workload_is_the_largest_single_gpu_config():
+    # the high-concurrency tensor-core regime: B = 512, V = 262144
+    args = bench.build_parser().parse_args([])
+    wl = inputs.WORKLOADS[args.workload]
+    assert args.workload == "high_concurrency_sched"
+    assert (wl.B, wl.gamma, wl.V, wl.r) == (512, 7, 262144, 256)
+    assert all(bench.algorithmic_bytes(w) <= bench.algorithmic_bytes(wl)
+               for w in inputs.WORKLOADS.values())
+
+
+def test_algorithmic_flops_by_hand():
+    wl = inputs.WORKLOADS["high_concurrency_sched"]
+    assert bench.algorithmic_flops(wl) == 2 * 512 * 256 * 262144 * 7  # 481 GFLOP per block
+    rnn = inputs.WORKLOADS["rnn_head"]
+    B, r, V, d, G = 128, 256, 151936, 5120, 7
+    assert bench.algorithmic_flops(rnn) == G * (2 * B * r * V + 2 * B * 3 * r * (2 * r + d))
+
+
+def test_every_workload_names_its_limiter():
+    for name in inputs.WORKLOADS:
+        assert bench.LIMITER.get(name), name
+
+
+def test_clock_summary_from_nvml_samples():
+    c = bench.ClockSampler(0)
+    c.samples = [(2070.0, 0), (2055.0, 0x4), (2070.0, 0x1)]
+    c.smax = 2070.0
+    s = c.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]  # idle (0x1) is not a throttle reason

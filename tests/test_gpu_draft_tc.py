@@ -60,18 +60,31 @@ def test_tc_invalid_anchor_and_repeatability():
         assert torch.equal(getattr(a, f), getattr(b, f)), f
 
 
+def sampled_rows(B, n=32, seed=0):
+    """n distinct requests of B: the first and last, the rest drawn at random (sorted)."""
+    rng = np.random.default_rng(seed)
+    mid = rng.choice(np.arange(1, B - 1), size=min(n, B) - 2, replace=False)
+    return sorted({0, B - 1, *mid.tolist()})
+
+
 @pytest.mark.slow
 def test_qwen3_8b_labels_full_sampled_rows():
+    # the whole workload on the GPU, in the configuration the benchmark times; 32 of its 64
+    # requests compared with the oracle (tokens, lse, c, S, c*, l1), z element-wise on two
     wl = inputs.WORKLOADS["qwen3_8b_labels"]
-    ties, _ = _run(wl, rows=[0, 17, 42, 63], want_logits=False)
-    assert ties <= 1
+    rows = sampled_rows(wl.B, seed=3)
+    ties, _ = _run(wl, rows=rows, z_rows=[rows[0], rows[-1]])
+    assert ties <= 2
 
 
 @pytest.mark.slow
 def test_high_concurrency_full_sampled_rows():
+    # 32 of the 512 requests (all four 128-request chunks), z element-wise on two
     wl = inputs.WORKLOADS["high_concurrency_sched"]
-    ties, _ = _run(wl, rows=[0, 129, 300, 511], want_logits=False)
-    assert ties <= 1
+    rows = sampled_rows(wl.B, seed=4)
+    assert len({r // 128 for r in rows}) == 4
+    ties, _ = _run(wl, rows=rows, z_rows=[rows[1], rows[-1]])
+    assert ties <= 2
 
 
 @pytest.mark.parametrize("B,G", [(64, 15), (130, 15)])

@@ -7,6 +7,7 @@ on the vocabulary-major tensor-core variant).  Same rules as
 the Markov tests: tokens bit-exact up to counted near-ties, floats (and the final state) within
 2e-3.
 """
+import numpy as np
 import pytest
 
 import semi_autoregressive_drafting_gb300 as ds
@@ -52,5 +53,8 @@ def test_rnn_tensor_core_two_chunks_target():
 
 @pytest.mark.slow
 def test_rnn_head_full_sampled_rows():
-    ties, _ = parity.run_case(RNN, ds=ds, rows=[0, 50, 127], want_logits=False)
-    assert ties <= 1
+    # 32 of the 128 requests (tokens, lse, c, S and the final state), z element-wise on two
+    rng = np.random.default_rng(5)
+    rows = sorted({0, 127, *rng.choice(np.arange(1, 127), size=30, replace=False).tolist()})
+    ties, _ = parity.run_case(RNN, ds=ds, rows=rows, z_rows=[rows[0], rows[-1]])
+    assert ties <= 2
