@@ -10,6 +10,7 @@ portable C++ and builds the same way on x86-64 and aarch64 hosts.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -43,34 +44,52 @@ def build(force: bool = False) -> str:
 def _load():
     global _lib
     if _lib is None:
-        lib = ctypes.CDLL(build())
-        P = ctypes.c_void_p
-        I = ctypes.c_int
-        lib.orc_philox4x32_10.argtypes = [P, P, P]
-        lib.orc_philox4x32_10.restype = None
-        lib.orc_uniform.argtypes = [ctypes.c_uint64, I, I, ctypes.c_int64]
-        lib.orc_uniform.restype = ctypes.c_double
-        lib.orc_gumbel.argtypes = [ctypes.c_uint64, I, I, ctypes.c_int64]
-        lib.orc_gumbel.restype = ctypes.c_double
-        lib.orc_draft.argtypes = ([I, I, I, I, I, I, ctypes.c_double, ctypes.c_uint64, I,
-                                   P, P, P, I, P, P, P, P, P, P, P, P, I]
-                                  + [P] * 11 + [I])
-        lib.orc_draft.restype = I
-        lib.orc_confidence.argtypes = [I, I, I, I, I, I, P, I, P, P, P, P, P, P]
-        lib.orc_confidence.restype = I
-        lib.orc_tv_label.argtypes = [I, I, ctypes.c_double, P, P, P, P, I]
-        lib.orc_tv_label.restype = None
-        lib.orc_verify.argtypes = [I, I, I, ctypes.c_double, ctypes.c_uint64] + [P] * 9 + [I]
-        lib.orc_verify.restype = I
-        lib.orc_draft_loss.argtypes = ([I, I, I, ctypes.c_double, P, P, P, P] + [ctypes.c_double] * 3
-                                       + [P] * 4 + [I])
-        lib.orc_draft_loss.restype = I
-        lib.orc_sts.argtypes = [I, I, P, P, I, P, I, P, P, P]
-        lib.orc_sts.restype = I
-        lib.orc_prefix_schedule.argtypes = [I, I, P, P, P, P]
-        lib.orc_prefix_schedule.restype = I
-        _lib = lib
+        _lib = _bind(ctypes.CDLL(build()))
     return _lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Route every call of this front end to another build of the oracle while the block runs.
+    The planted-mistake tests compile mutated copies of ``dspark_oracle.cpp`` and check that the
+    pins reject each one."""
+    global _lib
+    saved = _lib
+    _lib = _bind(ctypes.CDLL(path))
+    try:
+        yield
+    finally:
+        _lib = saved
+
+
+def _bind(lib):
+    """Declare the argument and result types of the oracle's exported functions on ``lib``."""
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    lib.orc_philox4x32_10.argtypes = [P, P, P]
+    lib.orc_philox4x32_10.restype = None
+    lib.orc_uniform.argtypes = [ctypes.c_uint64, I, I, ctypes.c_int64]
+    lib.orc_uniform.restype = ctypes.c_double
+    lib.orc_gumbel.argtypes = [ctypes.c_uint64, I, I, ctypes.c_int64]
+    lib.orc_gumbel.restype = ctypes.c_double
+    lib.orc_draft.argtypes = ([I, I, I, I, I, I, ctypes.c_double, ctypes.c_uint64, I,
+                               P, P, P, I, P, P, P, P, P, P, P, P, I]
+                              + [P] * 11 + [I])
+    lib.orc_draft.restype = I
+    lib.orc_confidence.argtypes = [I, I, I, I, I, I, P, I, P, P, P, P, P, P]
+    lib.orc_confidence.restype = I
+    lib.orc_tv_label.argtypes = [I, I, ctypes.c_double, P, P, P, P, I]
+    lib.orc_tv_label.restype = None
+    lib.orc_verify.argtypes = [I, I, I, ctypes.c_double, ctypes.c_uint64] + [P] * 9 + [I]
+    lib.orc_verify.restype = I
+    lib.orc_draft_loss.argtypes = ([I, I, I, ctypes.c_double, P, P, P, P] + [ctypes.c_double] * 3
+                                   + [P] * 4 + [I])
+    lib.orc_draft_loss.restype = I
+    lib.orc_sts.argtypes = [I, I, P, P, I, P, I, P, P, P]
+    lib.orc_sts.restype = I
+    lib.orc_prefix_schedule.argtypes = [I, I, P, P, P, P]
+    lib.orc_prefix_schedule.restype = I
+    return lib
 
 
 def _ptr(a):

@@ -141,3 +141,24 @@ def test_invalid_label():
     lab[1, 1] = 6
     r = oracle.draft_loss(T=1.0, draft_logits=zd, target_logits=zt, labels=lab, conf_logits=cf)
     assert r.status == 1 and np.isnan(r.loss[1]) and not np.isnan(r.loss[0])
+
+
+def test_confidence_label_one_hot_against_uniform():
+    # Eq 8 inside L_conf at a value strictly between 0 and 1: a one-hot draft against a uniform
+    # target has c* = 1/V ("DSpark -- paper verification", delta table D7), so with the
+    # confidence logit l (c = sigmoid(l) != 1/2):
+    #   L_conf = -w [ (1/V) ln c + (1 - 1/V) ln(1 - c) ],  dL/dl = a_conf w (c - 1/V)
+    G, V = 3, 8
+    big = -1e4
+    zd = np.full((1, G, V), big, np.float32)
+    zd[0, :, 5] = 0.0
+    zt = np.zeros((1, G, V), np.float32)
+    cf = np.array([[1.0, -0.5, 2.0]], np.float32)
+    r = oracle.draft_loss(T=1.0, draft_logits=zd, target_logits=zt, labels=np.zeros((1, G), np.int32),
+                          conf_logits=cf, alpha=(0.0, 0.0, 1.0))
+    w = np.exp(-np.arange(G) / G)
+    c = 1 / (1 + np.exp(-cf[0].astype(np.float64)))
+    cs = 1.0 / V
+    want = -(w * (cs * np.log(c) + (1 - cs) * np.log(1 - c))).sum()
+    assert abs(r.parts[0, 2] - want) < 1e-9
+    assert np.allclose(r.grad_conf[0], w * (c - cs), rtol=0, atol=1e-12)
