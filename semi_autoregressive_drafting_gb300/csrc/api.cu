@@ -227,6 +227,16 @@ dspark_status run_draft(const DraftArgs& a) {
   p.rnn_flag = (unsigned*)(ws + L.rnn_flag);
   p.ybuf = (float*)(ws + L.ybuf);
 
+  // Failure-path test hook: DSPARK_TEST_STUCK_WAIT = grid | mbar (read at every call) makes one
+  // named wait of the draft kernel wait for a signal that never comes -- one more grid-barrier
+  // arrival than there are blocks, or an mbarrier no thread arrives on -- with a 20 us limit, so
+  // that the call ends with DSPARK_ERR_TIMEOUT through the kernel's ordinary unwinding.  Unset
+  // (normal use), nothing changes.
+  if (const char* f = std::getenv("DSPARK_TEST_STUCK_WAIT")) {
+    p.test_stuck = !std::strcmp(f, "grid") ? 1 : !std::strcmp(f, "mbar") ? 2 : 0;
+    p.test_wait_ns = 20000ull;
+  }
+
   const int units = (a.V + 7) / 8;
   p.slice_max = ((units + nCTA - 1) / nCTA) * 8;
   const int ues = u_bf16 ? 2 : 4;

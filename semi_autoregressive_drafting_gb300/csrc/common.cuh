@@ -330,6 +330,21 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
   }
   return __shfl_sync(0xffffffffu, ok, 0);
 }
+// The same with the time bound given (the draft kernels' failure-path test hook).
+__device__ __forceinline__ bool mbar_wait_warp_lim(uint64_t* bar, uint32_t parity,
+                                                   unsigned long long limit_ns) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0 && !mbar_try_wait(bar, parity)) {
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait_sleep(bar, parity, 1000)) {
+      if (globaltimer() - t0 > limit_ns) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok, 0);
+}
 // Bounded wait for the phase with the given parity; false when the time bound ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;

@@ -64,6 +64,11 @@ struct DraftParams {
   int tc_nu;           // tensor-core path: U tiles staged in shared memory (0 = direct loads)
   int tc_pk;           // tensor-core path: at most 64 requests, vocabulary tiles in pairs
   size_t smem_bytes;
+  // failure-path test hook (0 in normal use): 1 = the per-step wait between thread blocks, 2 = an
+  // mbarrier wait of the epilogue warps, each made to wait for a signal that never comes, with
+  // the limit test_wait_ns; the kernel then unwinds exactly as on a real timeout
+  int test_stuck;
+  unsigned long long test_wait_ns;
 };
 
 // Host launchers (defined in the .cu files).  Return a cudaError_t.

@@ -104,7 +104,7 @@ __host__ __device__ inline CCLayout cc_layout(const DraftParams& p, int NB) {
   L.bars = off;
   // ring full/empty, U full/empty; tensor-core variant: efull, mdone, accfull[32], tready[16],
   // rfull[16]
-  off += (size_t)(2 * p.nstages + 4 + (p.tcv ? 2 + 32 + 16 + 16 : 0)) * 8;
+  off += (size_t)(2 * p.nstages + 4 + (p.tcv ? 2 + 32 + 16 + 16 : 0) + 1) * 8;  // + never
   L.total = align_up(off, 128) + (p.tcv ? 1024 : 0);  // slack to align the base to 1024
   return L;
 }
@@ -258,9 +258,11 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 
 // Grid barrier and argmax in one: wait (bounded) until every block has published its tagged
 // key for step ks, then return the largest.  One warp; each lane covers every 32nd block.
+// (The failure-path test hook polls for a tag no block writes, with a short limit.)
 __device__ __forceinline__ bool poll_keys(const unsigned long long* keys, int n, int ks, int lane,
-                                          bool acquire, unsigned long long* best) {
-  const unsigned long long tag = (unsigned long long)(ks + 1);
+                                          bool acquire, unsigned long long* best, bool stuck,
+                                          unsigned long long limit_ns) {
+  const unsigned long long tag = (unsigned long long)(ks + 1) + (stuck ? 0x40ull : 0ull);
   unsigned long long t0 = 0;
   for (;;) {
     unsigned long long m = 0;
@@ -283,7 +285,7 @@ __device__ __forceinline__ bool poll_keys(const unsigned long long* keys, int n,
       return true;
     }
     if (t0 == 0) t0 = globaltimer();
-    else if (globaltimer() - t0 > kWaitLimitNs) return false;
+    else if (globaltimer() - t0 > limit_ns) return false;
     __nanosleep(32);
   }
 }
@@ -520,6 +522,8 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
   uint64_t* accfull = mdone + 1;  // TCV: [32] tile t's accumulator holds step ks's bias
   uint64_t* tready = accfull + 32;  // TCV: [16] slab j has been copied into TMEM
   uint64_t* rfull = tready + 16;    // TCV: [16] resident slab i has landed
+  // no thread arrives on it (failure-path test hook); the last barrier of the region
+  uint64_t* never = full + 2 * p.nstages + 4 + (TCV ? 2 + 32 + 16 + 16 : 0);
   uint8_t* res = smem + Lay.res;
   uint8_t* ebf = smem + Lay.ebf;
 
@@ -568,6 +572,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
       mbar_init(&ufull[i], 1);
       mbar_init(&uempty[i], 1);
     }
+    mbar_init(never, 1);
     fence_mbar_init();
     ms->S_run = 1.f;
     ms->abort = 0;
@@ -884,6 +889,8 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
     const float* tb = tbuf + (size_t)(buf * NB + bq) * SLM;
     const float* gb = gbuf + (size_t)bq * SLM;
     bool wfail = false;
+    if (p.test_stuck == 2 && ks == 0)  // failure-path test hook: a wait nothing will end
+      wfail = !mbar_wait_warp_lim(never, 0, p.test_wait_ns);
     // +U_k, /T, online (max, sum-exp), Gumbel-max update for slice entry vl of request bq
     auto epilogue = [&](int vl, float bias) {
       const int v = v0 + vl;
@@ -913,7 +920,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
       if (ks == 0) {
         // slabs bound for TMEM: the group's four warps copy rows 32 qw + lane of each (one
         // 16-byte chunk at a time out of the swizzled slab) into TMEM columns [32 j, 32 j + 32)
-        for (int j = grp; j < nres; j += kGroups) {
+        for (int j = grp; j < nres && !wfail; j += kGroups) {
           const int slot = j % NS;  // ring use j
           const bool okw = __all_sync(0xffffffffu, wait_stage(ms->stage_tag, full, slot, j, NS));
           if (gsync_or(grp, !okw)) {
@@ -983,7 +990,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
     // Four warps share each stage: warp q of a group takes rows [q R/4, (q+1) R/4) in
     // sub-groups of SR rows, so a slot is handed back a quarter of a stage's work after its
     // bytes land.  Stages go round-robin to the groups.
-    for (int s = grp; s < (TCV ? 0 : nst); s += kGroups) {
+    for (int s = grp; s < (TCV ? 0 : nst) && !wfail; s += kGroups) {
       const int rows = min(R, SL - s * R);
       const int rq0 = qw * (R / 4), rq1 = min(rows, rq0 + R / 4);
       if (R == 32 && NCV == 1) {
@@ -1203,7 +1210,8 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
     if (warp < B) {
       const int b = warp;
       unsigned long long best = 0;
-      ok = poll_keys(p.keys + ((size_t)ks * B + b) * nCTA, nCTA, ks, lane, tgt, &best);
+      ok = poll_keys(p.keys + ((size_t)ks * B + b) * nCTA, nCTA, ks, lane, tgt, &best,
+                     p.test_stuck == 1, p.test_stuck == 1 ? p.test_wait_ns : kWaitLimitNs);
       if (lane == 0 && ok) {
         const bool was_valid = ms->valid[b];
         const int xk = was_valid ? (int)tagged_token(best) : -1;

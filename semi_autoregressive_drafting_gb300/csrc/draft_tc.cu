@@ -100,7 +100,7 @@ __host__ __device__ inline TCLayout tc_layout(int r, int na, int nstage, bool rn
   L.misc = off;
   off = align_up_t(off + sizeof(TMisc), 128);
   L.bars = off;
-  off += (size_t)(2 * nstage + 2 * kAcc + 2 * na + 3 + 2 * nu) * 8;
+  off += (size_t)(2 * nstage + 2 * kAcc + 2 * na + 3 + 2 * nu + 1) * 8;
   L.total = align_up_t(off, 1024) + 1024;  // + slack to align the dynamic base to 1024
   return L;
 }
@@ -382,6 +382,13 @@ __global__ void __launch_bounds__(kTThr) target_part_kernel(const float* __restr
   }
 }
 
+// Vocabulary tile visited at position t of unit u (one request chunk of one step): the units
+// alternate direction over the block's tiles, so the W2 tiles a unit reads first are the ones
+// the unit before it read last, still in L2 (W2 is loaded evict-last, U evict-first).  With
+// several 128-request chunks W2 is then re-read mostly from L2 instead of once per chunk from
+// DRAM, and from one step to the next the same holds.
+__device__ __forceinline__ int tile_at(int t, int u, int ntile) { return (u & 1) ? ntile - 1 - t : t; }
+
 template <bool RNN, bool TGT>
 __global__ void __launch_bounds__(kThreads, 1)
     draft_tc_kernel(const DraftParams p, const __grid_constant__ CUtensorMap tmap_w2,
@@ -410,6 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* hdot_ready = mma_done + 1;  // the spare warps have written w[:d] . h_k (Eq 7)
   uint64_t* u_full = hdot_ready + 1;  // [nu] a U tile has landed
   uint64_t* u_empty = u_full + nu;   // [nu] every epilogue warp has read it
+  uint64_t* never = u_empty + nu;    // no thread arrives on it (failure-path test hook)
   uint8_t* ubuf = smem + Lay.ubuf;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -449,6 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&u_full[i], 1);
       mbar_init(&u_empty[i], kEpiWarps);
     }
+    mbar_init(never, 1);
     fence_mbar_init();
     ms->abort = 0;
   }
@@ -473,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < ntile && !stop; ++t) {
             // U of the round that starts with tile t (packed: tiles t and t + 1, 64 rows each,
             // into rows 0-63 and 64-127 of the two 64-entry boxes), ahead of use
+            const int u = ks * nchunk + c;
             if (nu > 0 && (!pk || (t & 1) == 0)) {
               const int us = ui % nu;
               if (ui >= nu &&
@@ -481,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               }
               uint8_t* dst = ubuf + (size_t)us * kUTile;
-              const int x = (t0 + t) * kNT;
+              const int x = (t0 + tile_at(t, u, ntile)) * kNT;
               if (!pk) {
                 mbar_expect_tx(&u_full[us], kUTile);
                 tc::tma_load_3d(dst, &tmap_u, x, ks, c * kM, &u_full[us], pol_u);
@@ -492,13 +502,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tma_load_3d(dst, &tmap_u, x, ks, 0, &u_full[us], pol_u);
                 tc::tma_load_3d(dst + kSlab, &tmap_u, x + 64, ks, 0, &u_full[us], pol_u);
                 if (two) {
-                  tc::tma_load_3d(dst + kSlab / 2, &tmap_u, x + kNT, ks, 0, &u_full[us], pol_u);
-                  tc::tma_load_3d(dst + kSlab + kSlab / 2, &tmap_u, x + kNT + 64, ks, 0,
+                  const int x2 = (t0 + tile_at(t + 1, u, ntile)) * kNT;
+                  tc::tma_load_3d(dst + kSlab / 2, &tmap_u, x2, ks, 0, &u_full[us], pol_u);
+                  tc::tma_load_3d(dst + kSlab + kSlab / 2, &tmap_u, x2 + 64, ks, 0,
                                   &u_full[us], pol_u);
                 }
               }
               ++ui;
             }
+            const int yt = (t0 + tile_at(t, u, ntile)) * kNT;
             for (int s = 0; s < nslab; ++s, ++g) {
               const int slot = g % nstage;
               if (g >= nstage &&
@@ -507,8 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               }
               mbar_expect_tx(&full[slot], kSlab);
-              tc::tma_load_2d(ring + (size_t)slot * kSlab, &tmap_w2, s * 64, (t0 + t) * kNT,
-                              &full[slot], pol);
+              tc::tma_load_2d(ring + (size_t)slot * kSlab, &tmap_w2, s * 64, yt, &full[slot], pol);
             }
           }
       if (stop) atomicMax(&hdr->status, kErrTimeout);
@@ -640,20 +651,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* const ybp = p.ybuf;
 
   // One group of 8 consecutive vocabulary entries v..v+7 of this thread's row: logits (Eq 4),
-  // the online normaliser, Philox Gumbel-max with the exact skip; with a target, its
-  // normaliser, and y saved for the Eq 8 second pass.  st.m, st.mt and st.best are in log2
-  // units here; the group's max is taken on z (the scale is positive, and rounding is
-  // monotone, so fl(max z * s2) is the max of fl(z * s2)), and each exponential is one FMA and
-  // one ex2.  Skip test: with w = 1 - u (exact) and q = exp(y - best), an entry with
+  // the online normaliser, Philox Gumbel-max with the exact skip; with a target, y saved for the
+  // Eq 8 second pass.  st.m, st.best and tb are in log2 units here (y2 = z s2), and pairs of
+  // entries go through the packed fp32 instructions (add, fma on float2).
+  //
+  // Normaliser: st.m is a reference point, not the running maximum.  The row's first group sets
+  // it to that group's maximum; lsum accumulates 2^(y2 - st.m) over the row.  Later groups skip
+  // the maximum and are rescaled only when their sum passes 2^64 (an entry more than 64
+  // octaves above the reference; inf included), which routes them to the rare path below.
+  //
+  // Skip test: with w = 1 - u (u the entry's uniform) and q = exp(y - best), an entry with
   // w >= 1.001 q cannot win (-ln u >= w, so its score is below best - 0.0009 in natural units).
-  // f = 1 + w - 2^-24 is read straight from the bits, and f >= fl(1 + 1.002 q') (q' = the
-  // computed q, within 1e-5 of q) implies w >= 1.002 q' >= 1.001 q, so a skipped entry is one
-  // the exact fp32 comparison would also reject.  Cp = 1.002 exp(m - best), q' = pe Cp / 1.002.
+  // f = 0x3F800000 | (bits >> 9) (one funnel shift) is the float 1 + u - 2^-24 = 2 - 2^-24 - w,
+  // on the 2^-23 grid of [1, 2).  P = pe Cp is the computed 1.002 q (within 1e-5 of it), and
+  // X = fl(2 - P) (one fma).  An entry is a candidate iff f >= X; a skipped one has
+  // f <= X - 2^-23 <= 2 - P - 2^-24, i.e. w >= P >= 1.001 q, so it is one the exact fp32
+  // comparison would also reject.  (P = 0 x inf gives X = NaN: not a candidate, and such an
+  // entry, y = -inf or 126 octaves below the first group's maximum, cannot win.)
   // FAST (a compile-time constant at each call): all 8 entries exist, U is staged, no debug
   // output, and the target (if any) has 16-byte aligned rows.
   auto group = [&](auto fast_tag, int gi, int vb, const uint32_t* bs, const uint8_t* ub,
-                   size_t urow, int b, TSlot& st, float& tb, float& Cp, const PhiloxFixed& pfx,
-                   volatile float* sb_own) {
+                   size_t urow, int b, TSlot& st, float2& lsum, float& tb, float& Cp,
+                   const PhiloxFixed& pfx, volatile float* sb_own) {
     constexpr bool FAST = decltype(fast_tag)::value;
     const int v = vb + 8 * gi;
     if (!FAST && v >= V) return;
@@ -669,10 +688,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       vq = true;
     }
     if (FAST || (vq && full)) {
-      float uf[8];
-      bf16x8(uq, uf);
+      const uint32_t uw[4] = {uq.x, uq.y, uq.z, uq.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) z[e] = uf[e] + __uint_as_float(bs[e]);
+      for (int i = 0; i < 4; ++i) {
+        const float2 zz = __fadd2_rn(
+            make_float2(__uint_as_float(uw[i] << 16), __uint_as_float(uw[i] & 0xFFFF0000u)),
+            make_float2(__uint_as_float(bs[2 * i]), __uint_as_float(bs[2 * i + 1])));
+        z[2 * i] = zz.x;
+        z[2 * i + 1] = zz.y;
+      }
     } else {  // the slice's ragged end, or U rows without 16-byte alignment
       float uf[8];
       bf16x8(uq, uf);
@@ -687,14 +711,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 8; ++e)
         if (v + e < V) lgp[urow + v + e] = z[e];
-    const float gmax = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])),
-                             fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7]))) * s2;
-    if (gmax > st.m) {  // rescale the running sum to the new max, once per group
-      st.l *= ex2f(st.m - gmax);
-      st.m = gmax;
+    if (st.m == -INFINITY) {  // the row's first group: the normaliser's reference point
+      st.m = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])),
+                   fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7]))) * s2;
       Cp = 1.002f * ex2f(st.m - tb);
     }
-    const float nm = -st.m;
     uint32_t wd[8];
     {
       const U4 r0 = philox_var((uint32_t)(v >> 2), pfx, p.rk0, p.rk1);
@@ -702,39 +723,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       wd[0] = r0.x; wd[1] = r0.y; wd[2] = r0.z; wd[3] = r0.w;
       wd[4] = r1.x; wd[5] = r1.y; wd[6] = r1.z; wd[7] = r1.w;
     }
-    float ls0 = 0.f, ls1 = 0.f;
-    uint32_t mask = 0;  // entries that might beat the running best
+    const float2 s22 = make_float2(s2, s2);
+    float2 nm2 = make_float2(-st.m, -st.m);
+    float2 pe[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float pe = ex2f(fmaf(z[e], s2, nm));
-      if (e & 1) ls1 += pe; else ls0 += pe;
-      const float f = __uint_as_float(0x3F800000u | (~wd[e] >> 9));
-      if (f < fmaf(pe, Cp, 1.f)) mask |= 1u << e;
+    for (int i = 0; i < 4; ++i) {
+      const float2 t2 = __ffma2_rn(make_float2(z[2 * i], z[2 * i + 1]), s22, nm2);
+      pe[i] = make_float2(ex2f(t2.x), ex2f(t2.y));
     }
-    st.l += ls0 + ls1;
-    if (mask) {  // the candidates in order (ties keep the smaller entry); the lanes of a warp
-                 // hold different requests, so this runs whenever any lane has one
-      while (mask) {
-        const int e = __ffs(mask) - 1;
-        mask &= mask - 1;
-        float ze = z[0];
-        uint32_t we = wd[0];
+    float2 gs = __fadd2_rn(__fadd2_rn(pe[0], pe[1]), __fadd2_rn(pe[2], pe[3]));
+    bool any = gs.x > 0x1p64f || gs.y > 0x1p64f;
+    const float2 ncp2 = make_float2(-Cp, -Cp), two2 = make_float2(2.f, 2.f);
+    float X[8];
 #pragma unroll
-        for (int j = 1; j < 8; ++j)
-          if (e == j) {
-            ze = z[j];
-            we = wd[j];
-          }
-        const float sc = ze * s2 - gumbel_log2(we);
-        if (sc > st.best) {
-          st.best = sc;
-          st.tok = (uint32_t)(v + e);
+    for (int i = 0; i < 4; ++i) {
+      const float2 x2 = __ffma2_rn(pe[i], ncp2, two2);
+      X[2 * i] = x2.x;
+      X[2 * i + 1] = x2.y;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) any = any || __uint_as_float(__funnelshift_r(wd[e], 0x7Fu, 9)) >= X[e];
+    if (any) {  // rare: a rescale of the reference, or entries that might beat the running best
+      if (gs.x + gs.y > 0x1p64f) {
+        const float gmax = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])),
+                                 fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7]))) * s2;
+        const float sc = ex2f(st.m - gmax);
+        lsum = make_float2(lsum.x * sc, lsum.y * sc);
+        st.m = gmax;
+        Cp = 1.002f * ex2f(st.m - tb);
+        nm2 = make_float2(-st.m, -st.m);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 t2 = __ffma2_rn(make_float2(z[2 * i], z[2 * i + 1]), s22, nm2);
+          pe[i] = make_float2(ex2f(t2.x), ex2f(t2.y));
+          X[2 * i] = fmaf(pe[i].x, -Cp, 2.f);
+          X[2 * i + 1] = fmaf(pe[i].y, -Cp, 2.f);
         }
+        gs = __fadd2_rn(__fadd2_rn(pe[0], pe[1]), __fadd2_rn(pe[2], pe[3]));
       }
-      *sb_own = st.best;
-      tb = fmaxf(tb, st.best);
-      Cp = 1.002f * ex2f(st.m - tb);
+      uint32_t mask = 0;  // entries that might beat the running best
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (__uint_as_float(__funnelshift_r(wd[e], 0x7Fu, 9)) >= X[e]) mask |= 1u << e;
+      if (mask) {  // the candidates in order; the lanes of a warp hold different requests, so
+                   // this runs whenever any lane has one
+        while (mask) {
+          const int e = __ffs(mask) - 1;
+          mask &= mask - 1;
+          float ze = z[0];
+          uint32_t we = wd[0];
+#pragma unroll
+          for (int j = 1; j < 8; ++j)
+            if (e == j) {
+              ze = z[j];
+              we = wd[j];
+            }
+          const float sc = ze * s2 - gumbel_log2(we);
+          // ties go to the smaller entry whatever order the tiles are visited in
+          if (sc > st.best || (sc == st.best && (uint32_t)(v + e) < st.tok)) {
+            st.best = sc;
+            st.tok = (uint32_t)(v + e);
+          }
+        }
+        *sb_own = st.best;
+        tb = fmaxf(tb, st.best);
+        Cp = 1.002f * ex2f(st.m - tb);
+      }
     }
+    lsum = __fadd2_rn(lsum, gs);
     if (TGT) {  // the target's normalisers come from target_part_kernel
       float* yo = ybp + (size_t)b * V + v;  // y2 = z s2, read back by the second pass
       if (FAST || (vec_t && full)) {
@@ -879,6 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const PhiloxFixed pfx = philox_fix((uint32_t)ks, (uint32_t)b, kNoiseTag, p.seed_lo, p.seed_hi);
       TSlot st;
       tslot_init(st);
+      float2 lsum = make_float2(0.f, 0.f);  // sum of 2^(y2 - st.m) over the row so far, in two halves
       // The skip threshold uses tb, the best score known for this request in the block: this
       // thread's own and the other parts' (the 4 column quarters, and in packed mode the two
       // tiles of a round, hold the same requests), published in shared memory.  An entry
@@ -890,11 +947,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tstep = pk ? 2 : 1;  // this warp's tile advances by tstep per round
       for (int rd = 0; rd < nround; ++rd, ++acc_i) {
         const int acc = acc_i % kAcc;
-        const int t = pk ? 2 * rd + half : rd;  // this warp's vocabulary tile of the round
+        const int t = pk ? 2 * rd + half : rd;  // this warp's tile position of the round
         const bool tile_ok = t < ntile;          // (packed, odd count: the last round has one)
-        const int vb = (t0 + t) * kNT + cq * 32;  // first vocab entry of this thread's 32
-        if (row_ok && t + 3 * tstep < ntile) {  // this thread's U and target lines, 3 rounds ahead
-          const size_t vp = urow + (size_t)(t0 + t + 3 * tstep) * kNT + cq * 32;
+        const int vb = (t0 + tile_at(t, u, ntile)) * kNT + cq * 32;  // first entry of this thread's 32
+        if (row_ok && t + 3 * tstep < ntile) {  // this thread's U line, 3 rounds ahead
+          const size_t vp = urow + (size_t)(t0 + tile_at(t + 3 * tstep, u, ntile)) * kNT + cq * 32;
           if (nu > 0) prefetch_line((const __nv_bfloat16*)Up + vp);
         }
         // the tile's U: staged by TMA, kept until the tile is done; else read from global
@@ -909,7 +966,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const uint8_t* ub = nu > 0 ? ubuf + (size_t)us * kUTile + (cq >> 1) * kSlab + lrow * 128 : nullptr;
-        const bool ok = mbar_wait_warp(&acc_full[acc], (uint32_t)((acc_i / kAcc) & 1));
+        const bool ok = p.test_stuck == 2 ? mbar_wait_warp_lim(never, 0, p.test_wait_ns)
+                                          : mbar_wait_warp(&acc_full[acc], (uint32_t)((acc_i / kAcc) & 1));
         if (!ok) {
           failed = true;
           break;
@@ -935,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t bias[8];
             __syncwarp();
             tc::tmem_ld8_wait(tcol + 8 * gi, bias);
-            if (row_ok) group(std::true_type{}, gi, vb, bias, ub, urow, b, st, tb, Cp, pfx, sb_own);
+            if (row_ok) group(std::true_type{}, gi, vb, bias, ub, urow, b, st, lsum, tb, Cp, pfx, sb_own);
           }
         } else {
 #pragma unroll 1
@@ -943,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t bias[8];
             __syncwarp();
             tc::tmem_ld8_wait(tcol + 8 * gi, bias);
-            if (row_ok && tile_ok) group(std::false_type{}, gi, vb, bias, ub, urow, b, st, tb, Cp, pfx, sb_own);
+            if (row_ok && tile_ok) group(std::false_type{}, gi, vb, bias, ub, urow, b, st, lsum, tb, Cp, pfx, sb_own);
           }
         }
         tc::fence_before_sync();
@@ -959,6 +1017,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // back to natural units for the normalisers (the published best stays in log2 units: it
       // is only compared with other blocks' log2 scores)
+      st.l = lsum.x + lsum.y;
       st.m *= kLn2;
       st.mt *= kLn2;
       // ---- merge each request's partial states (column quarters; packed: also the two tiles
@@ -988,11 +1047,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ok = 1;
       __threadfence();
       red_release_add(&hdr->arrive, 1u);
-      const unsigned target = (unsigned)(ks + 1) * gridDim.x;
+      // (the test hook waits for one arrival more than there are blocks, with a short limit)
+      const unsigned target = (unsigned)(ks + 1) * gridDim.x + (p.test_stuck == 1 ? 1u : 0u);
+      const unsigned long long lim = p.test_stuck == 1 ? p.test_wait_ns : kWaitLimitNs;
       if (ld_acquire(&hdr->arrive) < target) {
         const unsigned long long tw = globaltimer();
         while (ld_acquire(&hdr->arrive) < target) {
-          if (globaltimer() - tw > kWaitLimitNs) {
+          if (globaltimer() - tw > lim) {
             ok = 0;
             break;
           }
