@@ -150,18 +150,19 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // log2(-ln u) for the Philox word `bits`, u = (2 (bits >> 9) + 1) 2^-24: the Gumbel noise in
-// log2 units is minus this.  t = -ln u = -ln(1 - w) with w = 1 - u (exact) is the series
-// w + w^2/2 + ... + w^5/5 for w <= 1/16 (truncation below w^5/6 = 1.6e-7 relative), else logf;
-// the outer logarithm is lg2.approx (absolute error about 2^-22, below one ulp of a score).
+// log2 units is minus this.  t = -ln u = -ln(1 - w), w = 1 - u (exact): the series
+// w + w^2/2 + ... + w^5/5 for w <= 1/16 (truncation below w^5/6 = 1.6e-7 relative), else
+// -log2(u) ln 2 with lg2.approx (|log2 u| >= 0.093 there, so the relative error stays below
+// 3e-6); both are computed and one is selected, so the lanes of a warp do not diverge.  The
+// outer logarithm is lg2.approx too.  The score's error is then below 5e-6 (log2 units), far
+// inside the 1e-4 band the sampler's parity treats as a near-tie.
 __device__ __forceinline__ float gumbel_log2(uint32_t bits) {
   const float u = __uint_as_float(0x3F800000u | (bits >> 9)) - 0.99999994f;  // exact
   const float w = 1.f - u;                                                    // exact
-  float t;
-  if (w <= 0.0625f)
-    t = w * fmaf(w, fmaf(w, fmaf(w, fmaf(w, 0.2f, 0.25f), 0.33333334f), 0.5f), 1.f);
-  else
-    t = -logf(u);
-  float l2;
+  const float ts = w * fmaf(w, fmaf(w, fmaf(w, fmaf(w, 0.2f, 0.25f), 0.33333334f), 0.5f), 1.f);
+  float lu, l2;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lu) : "f"(u));
+  const float t = w <= 0.0625f ? ts : -lu * 0.6931471805599453f;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(t));
   return l2;
 }
@@ -428,10 +429,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool tgt = TGT;  // a target is given (Eq 8): fixed per instantiation
   WsHeader* hdr = p.hdr;
 
+  // Work split.  The blocks form ngrp groups, one per 128-request chunk (while there are no
+  // more chunks than blocks); group g takes chunks g, g + ngrp, ... and its nslice blocks split
+  // the vocabulary.  So a block gathers its chunk's conditioning rows once per step and walks a
+  // wide vocabulary slice with one running best per request, instead of walking a narrow slice
+  // once per chunk; the ngrp blocks that share a slice have adjacent ids and read the same W2
+  // tiles at about the same time, so L2 serves the repeats.  Blocks past ngrp * nslice have no
+  // tiles (they still take part in the barriers).
+  const int ngrp = min(nchunk, nCTA);
+  const int nslice = nCTA / ngrp;
+  const int grp = cta % ngrp, slc = cta / ngrp;
+  const int nck = grp < nchunk ? (nchunk - 1 - grp) / ngrp + 1 : 0;  // chunks of this block
+
   // vocab tiles of this block
   const int ntile_all = (V + kNT - 1) / kNT;
-  const int t0 = (int)(((long long)ntile_all * cta) / nCTA);
-  const int t1 = (int)(((long long)ntile_all * (cta + 1)) / nCTA);
+  const int t0 = slc < nslice ? (int)(((long long)ntile_all * slc) / nslice) : 0;
+  const int t1 = slc < nslice ? (int)(((long long)ntile_all * (slc + 1)) / nslice) : 0;
   const int ntile = t1 - t0;
   const int nround = pk ? (ntile + 1) / 2 : ntile;  // accumulator rounds per chunk
   const int sl0 = t0 * kNT, sl1 = min(V, t1 * kNT);  // vocab slice [sl0, sl1)
@@ -478,11 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0, ui = 0;
       bool stop = false;
       for (int ks = 0; ks < G && !stop; ++ks)
-        for (int c = 0; c < nchunk && !stop; ++c)
+        for (int ci = 0; ci < nck && !stop; ++ci)
           for (int t = 0; t < ntile && !stop; ++t) {
+            const int c = grp + ci * ngrp;  // the chunk
             // U of the round that starts with tile t (packed: tiles t and t + 1, 64 rows each,
             // into rows 0-63 and 64-127 of the two 64-entry boxes), ahead of use
-            const int u = ks * nchunk + c;
+            const int u = ks * nck + ci;  // this block's unit (step, chunk)
             if (nu > 0 && (!pk || (t & 1) == 0)) {
               const int us = ui % nu;
               if (ui >= nu &&
@@ -538,8 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0, acc_i = 0;
       bool stop = false;
       for (int ks = 0; ks < G && !stop; ++ks)
-        for (int c = 0; c < nchunk && !stop; ++c) {
-          const int u = ks * nchunk + c, ab = u % na;
+        for (int ci = 0; ci < nck && !stop; ++ci) {
+          const int u = ks * nck + ci, ab = u % na;
           if (!wait_or_abort(&a_full[ab], (uint32_t)((u / na) & 1), &ms->abort)) {
             stop = true;
             break;
@@ -711,17 +725,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 8; ++e)
         if (v + e < V) lgp[urow + v + e] = z[e];
-    if (st.m == -INFINITY) {  // the row's first group: the normaliser's reference point
-      st.m = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])),
-                   fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7]))) * s2;
-      Cp = 1.002f * ex2f(st.m - tb);
-    }
     uint32_t wd[8];
     {
       const U4 r0 = philox_var((uint32_t)(v >> 2), pfx, p.rk0, p.rk1);
       const U4 r1 = philox_var((uint32_t)(v >> 2) + 1u, pfx, p.rk0, p.rk1);
       wd[0] = r0.x; wd[1] = r0.y; wd[2] = r0.z; wd[3] = r0.w;
       wd[4] = r1.x; wd[5] = r1.y; wd[6] = r1.z; wd[7] = r1.w;
+    }
+    if (st.m == -INFINITY) {  // the row's first group: the normaliser's reference point, and
+      // the running best seeded with the exact score of the group's largest entry (a real
+      // score, so a lower bound of the row's best: without it every entry of the group would be
+      // a candidate).  That entry is tested again below and changes nothing.
+      int es = 0;
+      float zs = z[0];
+#pragma unroll
+      for (int e = 1; e < 8; ++e)
+        if (z[e] > zs) {
+          zs = z[e];
+          es = e;
+        }
+      st.m = zs * s2;
+      if (zs != -INFINITY) {
+        uint32_t ws = wd[0];
+#pragma unroll
+        for (int e = 1; e < 8; ++e)
+          if (es == e) ws = wd[e];
+        const float sc = zs * s2 - gumbel_log2(ws);
+        if (sc > st.best || (sc == st.best && (uint32_t)(v + es) < st.tok)) {
+          st.best = sc;
+          st.tok = (uint32_t)(v + es);
+        }
+        *sb_own = st.best;
+        tb = fmaxf(tb, st.best);
+      }
+      Cp = 1.002f * ex2f(st.m - tb);
     }
     const float2 s22 = make_float2(s2, s2);
     float2 nm2 = make_float2(-st.m, -st.m);
@@ -770,14 +807,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (mask) {
           const int e = __ffs(mask) - 1;
           mask &= mask - 1;
-          float ze = z[0];
-          uint32_t we = wd[0];
-#pragma unroll
-          for (int j = 1; j < 8; ++j)
-            if (e == j) {
-              ze = z[j];
-              we = wd[j];
-            }
+          // z[e], wd[e] by a three-level select on the bits of e (registers cannot be indexed)
+          const bool b0 = e & 1, b1 = e & 2, b2 = e & 4;
+          const float z01 = b0 ? z[1] : z[0], z23 = b0 ? z[3] : z[2];
+          const float z45 = b0 ? z[5] : z[4], z67 = b0 ? z[7] : z[6];
+          const uint32_t w01 = b0 ? wd[1] : wd[0], w23 = b0 ? wd[3] : wd[2];
+          const uint32_t w45 = b0 ? wd[5] : wd[4], w67 = b0 ? wd[7] : wd[6];
+          const float ze = b2 ? (b1 ? z67 : z45) : (b1 ? z23 : z01);
+          const uint32_t we = b2 ? (b1 ? w67 : w45) : (b1 ? w23 : w01);
           const float sc = ze * s2 - gumbel_log2(we);
           // ties go to the smaller entry whatever order the tiles are visited in
           if (sc > st.best || (sc == st.best && (uint32_t)(v + e) < st.tok)) {
@@ -808,8 +845,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // normalisers of p^d and p^t, then the slice's sum of |p^d - p^t| for each request (y2 from
   // the workspace, the target re-read; eight 16-byte loads of each in flight per lane)
   auto second_pass = [&](int kp) {
-    for (int b = ew; b < B; b += kEpiWarps) {
-      const float2 a = merge_ml(p.ml + ((size_t)kp * B + b) * nCTA, nCTA, lane);
+    for (int i = ew; i < nck * kM; i += kEpiWarps) {  // the requests of this block's chunks
+      const int b = (grp + (i / kM) * ngrp) * kM + i % kM;
+      if (b >= B) continue;  // (the same for every lane of the warp)
+      const float2 a = merge_ml(p.ml + ((size_t)kp * B + b) * nCTA, nslice, lane);
       const float2 tt = merge_ml(p.mlt + ((size_t)kp * B + b) * ntp, ntp, lane);
       const float Ld2 = (a.x + logf(a.y)) * kLog2e, Lt2 = (tt.x + logf(tt.y)) * kLog2e;
       const float* yr = ybp + (size_t)b * V;
@@ -841,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int v = vt + lane; v < sl1; v += 32)
         acc += fabsf(ex2f(yr[v] - Ld2) - ex2f(tr[v] * s2 - Lt2));
       acc = warp_sum(acc);
-      if (lane == 0) p.l1p[((size_t)kp * B + b) * nCTA + cta] = acc;
+      if (lane == 0) p.l1p[((size_t)kp * B + b) * nCTA + slc] = acc;
     }
   };
 
@@ -862,8 +901,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (et == 0) st_release_u32(&p.rnn_flag[(size_t)ks * B + b], (unsigned)(ks + 1));
       }
     }
-    for (int c = 0; c < nchunk && !failed; ++c) {
-      const int u = ks * nchunk + c, ab = u % na;
+    for (int ci = 0; ci < nck && !failed; ++ci) {
+      const int c = grp + ci * ngrp;  // the chunk
+      const int u = ks * nck + ci, ab = u % na;
       // ---- A operand: the chunk's conditioning rows W1[x_{k-1}], swizzled K-major bf16
       if (u >= na) {
         const bool ok = wait_or_abort(&a_empty[ab], (uint32_t)(((u / na) - 1) & 1), &ms->abort);
@@ -923,7 +963,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (et == 0) mbar_arrive(&a_full[ab]);
 
       // Eq 8 of the previous step, while the MMAs of this step's first rounds run
-      if (tgt && c == 0 && ks > 0) {
+      if (tgt && ci == 0 && ks > 0) {
         second_pass(ks - 1);
         esync<kEpiThreads>();
       }
@@ -1035,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool valid = false;
         cond_token(p, b, ks, &valid);
         if (valid && ntile > 0 && sl1 > sl0) atomicMax(&p.keys[(size_t)ks * B + b], make_key(st.best, st.tok));
-        p.ml[((size_t)ks * B + b) * nCTA + cta] = make_float2(st.m, st.l);
+        p.ml[((size_t)ks * B + b) * nCTA + slc] = make_float2(st.m, st.l);
       }
       esync<kEpiThreads>();
     }
@@ -1095,7 +1135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int x = cond_token(p, b, k, &valid);
     if (!valid && lane == 0) atomicMax(&hdr->status, kErrInvalid);
     const int tok = valid ? (int)key_token(ld_acquire64(&p.keys[(size_t)k * B + b])) : -1;
-    const float2 ml = merge_ml(p.ml + ((size_t)k * B + b) * nCTA, nCTA, lane);
+    const float2 ml = merge_ml(p.ml + ((size_t)k * B + b) * nCTA, nslice, lane);
     if (conf) {
       const float z7 = ((volatile float*)p.hdot)[o] + eq7_edot(p, x, lane);
       if (lane == 0) p.c[o] = valid ? sigmoidf_acc(z7) : NAN;
@@ -1105,7 +1145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       p.lse[o] = valid ? ml.x + logf(ml.y) : NAN;
     }
     if (tgt && k + 1 < G) {
-      const float s = warp_sum_n(p.l1p + ((size_t)k * B + b) * nCTA, nCTA, lane);
+      const float s = warp_sum_n(p.l1p + ((size_t)k * B + b) * nCTA, nslice, lane);
       if (lane == 0) {
         p.l1[o] = valid ? s : NAN;
         p.cstar[o] = valid ? fminf(1.f, fmaxf(0.f, 1.f - 0.5f * s)) : NAN;
@@ -1140,7 +1180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __threadfence();
     if (tgt)
       for (int b = ew; b < B; b += kEpiWarps) {
-        const float s = warp_sum_n(p.l1p + ((size_t)(G - 1) * B + b) * nCTA, nCTA, lane);
+        const float s = warp_sum_n(p.l1p + ((size_t)(G - 1) * B + b) * nCTA, nslice, lane);
         if (lane == 0) {
           const size_t o = (size_t)b * G + G - 1;
           const bool vb = ((volatile int32_t*)p.tokens)[o] >= 0;
@@ -1167,8 +1207,10 @@ int draft_tc_supported(int B, int r, int w_bf16) { return w_bf16 && B >= 1 && r 
 bool draft_tc_configure(DraftParams& p, size_t smem_optin) {
   // U tiles are staged by TMA when U is bf16 with 16-byte aligned rows; prefer (at most 64
   // requests) vocabulary tiles in pairs so that all 128 TMEM lanes and epilogue warps work, then
-  // two staged U tiles, then two A buffers, then the deepest W2 ring (at least 3 stages)
-  const int nu_max = p.u_bf16 && p.V % 8 == 0 ? 2 : 0;
+  // the most staged U tiles (up to 3: measured at B = 512, one staged tile costs 1.5x, a third
+  // one saves 3% over two), then two A buffers, then the deepest W2 ring (at least 3 stages;
+  // 3 and 5 measured the same)
+  const int nu_max = p.u_bf16 && p.V % 8 == 0 ? 3 : 0;
   for (int pk = p.B <= 64 ? 1 : 0; pk >= 0; --pk)
     for (int nu = nu_max; nu >= 0; --nu)
       for (int na = 2; na >= 1; --na)

@@ -30,6 +30,22 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same descriptor for an MN-major operand (its M or N dimension contiguous in memory): the
+// tile is stored as 128-byte rows of 64 MN-consecutive elements, one row per K index, in
+// 128-byte-swizzled atoms of 8 K-rows (1024 B).  Consecutive 8-row groups along K are 1024 B
+// apart (stride byte offset) and consecutive 64-element blocks along MN are `lbo` bytes apart
+// (leading byte offset).  A 2-D TMA box of 64 MN elements x R K-rows with the 128-byte swizzle
+// writes exactly this layout, one box per 64-element block.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A and B, fp32 accumulation, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                      // D format: f32
@@ -38,6 +54,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | ((uint32_t)(N >> 3) << 17)   // N / 8
          | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
+// Operand-major bits of the same descriptor: A (bit 15) or B (bit 16) is MN-major.
+constexpr uint32_t kIdescAMajorMN = 1u << 15;
+constexpr uint32_t kIdescBMajorMN = 1u << 16;
 
 // ------------------------------------------------------------------ TMEM
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {
