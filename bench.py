@@ -579,6 +579,9 @@ def build_parser():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="high_concurrency_sched")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--w2-layout", choices=["vr", "rv"], default="vr",
+                    help="W2 as a linear layer's [V][r] weight (vr) or as the pages write it, "
+                         "[r][V] (rv)")
     ap.add_argument("--op", choices=["draft", "verify", "loss"], default="draft",
                     help="draft: the draft block (default); verify: the speculative accept/reject "
                          "step on the workload's B, gamma, V; loss: the training losses (Eqs 9-12) "
@@ -620,8 +623,10 @@ def main():
 
     host = inputs.generate(wl)
     dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    if args.w2_layout == "rv":
+        dev["W2"] = dev["W2"].t().contiguous()
     ws = ds.Workspace(0 if wl.head == "markov" else 1, wl.B, wl.gamma, wl.V, wl.r, wl.d,
-                      target=wl.target_noise is not None)
+                      target=wl.target_noise is not None, w2_layout=args.w2_layout)
     stream = torch.cuda.current_stream()
     B, G = wl.B, wl.gamma
 
@@ -629,7 +634,7 @@ def main():
         return ds.DraftPlan(0 if wl.head == "markov" else 1, dev["W1"], dev["W2"], U, x0, T=wl.T,
                             seed=wl.seed, h=h, w=dev["w"], Wj=dev.get("Wj"), target=target,
                             forced=None, s0=None, want_logits=False, workspace=ws, stream=stream,
-                            out=out)
+                            out=out, w2_layout=args.w2_layout)
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     resident = plan(dev["U"], dev["h"], dev["x0"], dev.get("target"))
@@ -738,6 +743,8 @@ def main():
         path = ds.draft_path(head, B, wl.V, wl.r, wl.dtype == "bf16")
         if path == 1 and wl.target_noise is not None:
             launches += 1  # the target's normalisers, before the draft
+        if path in (0, 2) and args.w2_layout == "rv":
+            launches += 1  # W2's transpose for the small-batch kernels
         kernel_name = "draft_tc_kernel" if path == 1 else "draft_cc_kernel"
         # achieved covers the whole call: with launches before the draft kernel (the RNN head's
         # h-part GEMM, the target's normalisers) their time is in ms_step too
@@ -770,7 +777,7 @@ def main():
             "config": {"workload": wl.name, "B": B, "gamma": G, "V": wl.V, "r": wl.r, "d": wl.d,
                        "T": wl.T, "l2": "flushed between timed blocks (512 MB write)",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                       "path": path_name},
+                       "path": path_name, "w2_layout": args.w2_layout},
             "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,

@@ -26,8 +26,10 @@
  *
  * Layouts (row-major)
  *   W1      [V][r]        embedding table of the sequential head (Eq 5 lookup)
- *   W2      [V][r]        logit projection stored as a linear layer's weight: row v holds the
- *                         r coefficients of vocab entry v, so B_k[v] = sum_j a_j * W2[v][j]
+ *   W2      [r][V]        the pages' orientation (DSPARK_W2_RV: W2 in R^{r x V}, B_k = a W2), or
+ *           [V][r]        a linear layer's weight (DSPARK_W2_VR: row v holds the r coefficients
+ *                         of vocab entry v); the draft calls take either (argument w2_layout):
+ *                         B_k[v] = sum_j a_j W2[j][v] = sum_j a_j W2^T[v][j]
  *   Wj      [3r][2r+d]    RNN joint projection, rows [gate; candidate; output], columns
  *                         [s_{k-1}; W1[x_{k-1}]; h_k] (Eq 6, delta table D8); no bias
  *   w       [d+r]         confidence weight: w[0:d] multiplies h_k, w[d:d+r] multiplies
@@ -68,12 +70,23 @@ typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
 
 typedef enum { DSPARK_HEAD_MARKOV = 0, DSPARK_HEAD_RNN = 1 } dspark_head;
 
+/* Storage of W2 ("DSpark -- paper verification", section 1, Eq 5: W2 in R^{r x V}).
+ * DSPARK_W2_RV: [r][V], the pages' orientation.  DSPARK_W2_VR: [V][r], the weight of a linear
+ * layer from r to V.  The tensor-core kernel with the requests on M reads either natively (an
+ * MN-major or a K-major operand, the same bytes at the same speed).  The small-batch kernels
+ * (B <= 4) read [V][r]: for DSPARK_W2_RV they first transpose W2 into the workspace (one more
+ * launch, 2 V r element reads and writes), which the workspace must be sized for
+ * (DSPARK_WS_W2_RV). */
+typedef enum { DSPARK_W2_VR = 0, DSPARK_W2_RV = 1 } dspark_w2_layout;
+
 /* dspark_workspace_bytes flags */
 #define DSPARK_WS_TARGET 1 /* the calls will pass target logits (Eq 8 labels) */
+#define DSPARK_WS_W2_RV 2  /* the calls will pass W2 as [r][V] (room for its transpose at B <= 4) */
 
 /*
  * Bytes of workspace the draft calls need for this problem (`flags`: DSPARK_WS_TARGET when
- * target logits will be passed; at B > 4 that reserves room for y, B * V floats).  The
+ * target logits will be passed; at B > 4 that reserves room for y, B * V floats; plus
+ * DSPARK_WS_W2_RV when W2 will be passed as [r][V]; at B <= 4 that reserves V * r * 4 bytes).  The
  * workspace is caller-owned device memory, 256-byte aligned, that must be ZEROED ONCE before
  * its first use; every
  * successful call leaves it ready for the next call.  One workspace serves one call at a time:
@@ -93,6 +106,8 @@ size_t dspark_workspace_bytes(int head, int B, int gamma, int V, int r, int d, i
  *   c*_k = clamp(1 - 1/2 || softmax(y) - softmax(target[b][k] / T) ||_1, 0, 1)  (Eq 8),
  *   l1_k = || softmax(y) - softmax(target[b][k] / T) ||_1.
  * W2 and U are streamed from HBM once per step.
+ *   W2, w2_layout  W2 as [r][V] (DSPARK_W2_RV) or [V][r] (DSPARK_W2_VR), see dspark_w2_layout;
+ *            [r][V] on the tensor-core path needs V a multiple of 8 (16-byte rows).
  *
  *   forced   NULL: step k+1 conditions on the sampled x_k.  Otherwise [B][gamma] int32
  *            teacher-forcing tokens: step k+1 conditions on forced[b][k-1] ([P3] "Training
@@ -108,7 +123,8 @@ size_t dspark_workspace_bytes(int head, int B, int gamma, int V, int r, int d, i
  */
 dspark_status dspark_markov_draft(int B, int gamma, int V, int r, int d, float T, uint64_t seed,
                                   dspark_dtype wdt, const void* W1, const void* W2,
-                                  const void* w, dspark_dtype udt, const void* U, const void* h,
+                                  dspark_w2_layout w2_layout, const void* w, dspark_dtype udt,
+                                  const void* U, const void* h,
                                   const int32_t* x0, const int32_t* forced, const float* target,
                                   int32_t* tokens, float* lse, float* c, float* S, float* cstar,
                                   float* l1, float* logits, void* workspace,
@@ -126,8 +142,9 @@ dspark_status dspark_markov_draft(int B, int gamma, int V, int r, int d, float T
  * same stream.  All other arguments, outputs and errors as dspark_markov_draft.
  */
 dspark_status dspark_rnn_draft(int B, int gamma, int V, int r, int d, float T, uint64_t seed,
-                               dspark_dtype wdt, const void* W1, const void* W2, const void* w,
-                               const void* Wj, dspark_dtype udt, const void* U, const void* h,
+                               dspark_dtype wdt, const void* W1, const void* W2,
+                               dspark_w2_layout w2_layout, const void* w, const void* Wj,
+                               dspark_dtype udt, const void* U, const void* h,
                                const int32_t* x0, const int32_t* forced, const float* target,
                                const float* s0, int32_t* tokens, float* lse, float* c, float* S,
                                float* cstar, float* l1, float* logits, float* s_out,
@@ -258,7 +275,8 @@ dspark_status dspark_sts(int N, int gamma, const float* conf_logits, const int32
  * their decode path, or code handed only pre-allocated input and output buffers cannot create a
  * workspace; this call keeps the draft's scratch in a 1 MiB array built into the library, which
  * every GPU that loads the library holds until the process exits.
- *   - Arguments and outputs are those of dspark_markov_draft, minus the workspace.
+ *   - Arguments and outputs are those of dspark_markov_draft, minus the workspace and the W2
+ *     layout: W2 is [V][r] here (the [r][V] form needs a transposed copy the array cannot hold).
  *   - status: optional device int32 that receives this call's device status (DSPARK_OK, or the
  *     DSPARK_ERR_INVALID / DSPARK_ERR_TIMEOUT cases described for dspark_markov_draft), written on
  *     `stream` after the draft; NULL to skip.  It is written only when the call returns

@@ -6,7 +6,8 @@ output tensors with PyTorch (device memory is PyTorch's job) and calls the C ABI
 fallback path, and a missing library raises.
 
 Names follow the pages: B requests, block size gamma, vocab V, Markov rank r, hidden size d,
-temperature T; W1 (embedding, [V][r]), W2 (logit projection stored [V][r]), w (confidence
+temperature T; W1 (embedding, [V][r]), W2 (logit projection: [r][V] as the pages write it with
+``w2_layout="rv"``, or a linear layer's [V][r] weight with the default ``"vr"``), w (confidence
 weight [d + r]), Wj (RNN joint projection [3r][2r + d]), U (base logits [B][gamma][V]),
 h (hidden states [B][gamma][d]), x0 (anchors [B]).
 """
@@ -24,6 +25,13 @@ __all__ = ["Workspace", "markov_draft", "rnn_draft", "confidence", "tv_label",
            "VerifyWorkspace", "verify", "LossWorkspace", "draft_loss", "sts", "CapacityRing"]
 
 _F32, _BF16 = 0, 1
+_W2_LAYOUT = {"vr": 0, "rv": 1}
+
+
+def _w2_code(layout: str) -> int:
+    if layout not in _W2_LAYOUT:
+        raise ValueError(f"w2_layout must be 'vr' ([V][r]) or 'rv' ([r][V]), not {layout!r}")
+    return _W2_LAYOUT[layout]
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -54,9 +62,10 @@ class Workspace:
     or smaller shape, one call at a time (stream order)."""
 
     def __init__(self, head: int, B: int, gamma: int, V: int, r: int, d: int, device=None,
-                 target: bool = False):
+                 target: bool = False, w2_layout: str = "vr"):
         lib = _lib.load()
-        n = lib.dspark_workspace_bytes(head, B, gamma, V, r, d, 1 if target else 0)
+        flags = (1 if target else 0) | (2 if _w2_code(w2_layout) == 1 else 0)
+        n = lib.dspark_workspace_bytes(head, B, gamma, V, r, d, flags)
         if n == 0:
             raise ValueError("invalid draft shape for a workspace")
         self.nbytes = int(n)
@@ -84,14 +93,18 @@ class DraftPlan:
     same input and output buffers (one C call, no per-call allocation or checks)."""
 
     def __init__(self, head, W1, W2, U, x0, *, T, seed, h, w, Wj, target, forced, s0,
-                 want_logits, workspace, stream, out=None):
+                 want_logits, workspace, stream, out=None, w2_layout="vr"):
         lib = _lib.load()
         B, gamma, V = U.shape
         r = W1.shape[1]
         d = h.shape[2] if h is not None else 0
         dev = U.device
+        w2c = _w2_code(w2_layout)
+        if tuple(W2.shape) != ((r, V) if w2c == 1 else (V, r)):
+            raise ValueError(f"W2 must be {'[r][V]' if w2c == 1 else '[V][r]'} for w2_layout={w2_layout!r}")
         if workspace is None:
-            workspace = Workspace(head, B, gamma, V, r, d, device=dev, target=target is not None)
+            workspace = Workspace(head, B, gamma, V, r, d, device=dev, target=target is not None,
+                                  w2_layout=w2_layout)
         f32 = dict(dtype=torch.float32, device=dev)
         o = dict(out or {})
         conf = h is not None and w is not None
@@ -125,12 +138,12 @@ class DraftPlan:
         ws = [workspace.buf.data_ptr(), workspace.nbytes, _stream(stream)]
         if head == 0:
             self._fn = lib.dspark_markov_draft
-            self._args = (B, gamma, V, r, d, float(T), int(seed), wdt, _ptr(W1), _ptr(W2),
+            self._args = (B, gamma, V, r, d, float(T), int(seed), wdt, _ptr(W1), _ptr(W2), w2c,
                           _ptr(w), udt, _ptr(U), _ptr(h), *common_in, *outs, *ws)
             self._where = "dspark_markov_draft"
         else:
             self._fn = lib.dspark_rnn_draft
-            self._args = (B, gamma, V, r, d, float(T), int(seed), wdt, _ptr(W1), _ptr(W2),
+            self._args = (B, gamma, V, r, d, float(T), int(seed), wdt, _ptr(W1), _ptr(W2), w2c,
                           _ptr(w), _ptr(Wj), udt, _ptr(U), _ptr(h), *common_in, _ptr(s0), *outs,
                           _ptr(s_out), *ws)
             self._where = "dspark_rnn_draft"
@@ -154,20 +167,23 @@ def _draft(head, W1, W2, U, x0, **kw):
 
 
 def markov_draft(W1, W2, U, x0, *, T=1.0, seed=0, h=None, w=None, target=None, forced=None,
-                 want_logits=False, workspace=None, stream=None, out=None) -> DraftOutput:
+                 want_logits=False, workspace=None, stream=None, out=None,
+                 w2_layout="vr") -> DraftOutput:
     """One draft block with the Markov head (Eq 5), sampling, Eq 7 confidence and S_k, and
-    the Eq 8 label when ``target`` is given.  See ``dspark_markov_draft``."""
+    the Eq 8 label when ``target`` is given.  ``w2_layout``: "vr" for W2 [V][r], "rv" for
+    [r][V].  See ``dspark_markov_draft``."""
     return _draft(0, W1, W2, U, x0, T=T, seed=seed, h=h, w=w, Wj=None, target=target,
                   forced=forced, s0=None, want_logits=want_logits, workspace=workspace,
-                  stream=stream, out=out)
+                  stream=stream, out=out, w2_layout=w2_layout)
 
 
 def rnn_draft(W1, W2, Wj, U, h, x0, *, T=1.0, seed=0, w=None, target=None, forced=None, s0=None,
-              want_logits=False, workspace=None, stream=None, out=None) -> DraftOutput:
+              want_logits=False, workspace=None, stream=None, out=None,
+              w2_layout="vr") -> DraftOutput:
     """One draft block with the RNN head (Eq 6).  See ``dspark_rnn_draft``."""
     return _draft(1, W1, W2, U, x0, T=T, seed=seed, h=h, w=w, Wj=Wj, target=target,
                   forced=forced, s0=s0, want_logits=want_logits, workspace=workspace,
-                  stream=stream, out=out)
+                  stream=stream, out=out, w2_layout=w2_layout)
 
 
 def confidence(W1, w, h, x0, tokens, *, stream=None):

@@ -22,9 +22,9 @@ STATUS = {0: "DSPARK_OK", 1: "DSPARK_ERR_INVALID", 2: "DSPARK_ERR_WORKSPACE",
 # exported symbol -> (restype, argtypes)
 SIGNATURES = {
     "dspark_workspace_bytes": (SZ, [I, I, I, I, I, I, I]),
-    "dspark_markov_draft": (I, [I, I, I, I, I, F, U64, I, P, P, P, I, P, P, P, P, P,
+    "dspark_markov_draft": (I, [I, I, I, I, I, F, U64, I, P, P, I, P, I, P, P, P, P, P,
                                 P, P, P, P, P, P, P, P, SZ, P]),
-    "dspark_rnn_draft": (I, [I, I, I, I, I, F, U64, I, P, P, P, P, I, P, P, P, P, P, P,
+    "dspark_rnn_draft": (I, [I, I, I, I, I, F, U64, I, P, P, I, P, P, I, P, P, P, P, P, P,
                              P, P, P, P, P, P, P, P, P, SZ, P]),
     "dspark_markov_draft_noalloc": (I, [I, I, I, I, I, F, U64, I, P, P, P, I, P, P, P, P, P,
                                         P, P, P, P, P, P, P, P, P]),

@@ -64,7 +64,7 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 struct WsLayout {
-  size_t keys, hdot, ml, mlt, l1p, rnn_s, rnn_a, rnn_gh, rnn_flag, ybuf, total;
+  size_t keys, hdot, ml, mlt, l1p, rnn_s, rnn_a, rnn_gh, rnn_flag, ybuf, w2t, total;
 };
 
 // flags: DSPARK_WS_TARGET reserves the y buffer the tensor-core path needs for Eq 8
@@ -92,6 +92,9 @@ WsLayout ws_layout(int head, int B, int G, int V, int r, int nCTA, int flags) {
   off = align256(off + (rnn ? (size_t)G * B * 4 : 0));
   L.ybuf = off;
   off = align256(off + ((flags & DSPARK_WS_TARGET) && B > 4 ? (size_t)B * V * 4 : 0));
+  // W2 given as [r][V]: the small-batch kernels (B <= 4) read its [V][r] transpose from here
+  L.w2t = off;
+  off = align256(off + ((flags & DSPARK_WS_W2_RV) && B <= 4 ? (size_t)V * r * 4 : 0));
   L.total = off;
   return L;
 }
@@ -129,7 +132,9 @@ struct DraftArgs {
   float T;
   uint64_t seed;
   dspark_dtype wdt, udt;
-  const void *W1, *W2, *w, *Wj, *U, *h;
+  const void *W1, *W2;
+  int w2_layout;
+  const void *w, *Wj, *U, *h;
   const int32_t *x0, *forced;
   const float *target, *s0;
   int32_t* tokens;
@@ -147,6 +152,8 @@ dspark_status run_draft(const DraftArgs& a) {
   if (!(a.T > 0.f) || !std::isfinite(a.T)) return fail(DSPARK_ERR_INVALID, "T must be finite and > 0");
   if ((a.wdt != DSPARK_F32 && a.wdt != DSPARK_BF16) || (a.udt != DSPARK_F32 && a.udt != DSPARK_BF16))
     return fail(DSPARK_ERR_INVALID, "unknown dtype");
+  if (a.w2_layout != DSPARK_W2_VR && a.w2_layout != DSPARK_W2_RV)
+    return fail(DSPARK_ERR_INVALID, "unknown W2 layout %d", a.w2_layout);
   if (!a.W1 || !a.W2 || !a.U || !a.x0 || !a.tokens || !a.lse)
     return fail(DSPARK_ERR_INVALID, "W1, W2, U, x0, tokens and lse are required");
   if (!aligned(a.W1, 16) || !aligned(a.W2, 16) || !aligned(a.U, 16) ||
@@ -170,7 +177,9 @@ dspark_status run_draft(const DraftArgs& a) {
   DevInfo di;
   if (!dev_info(&di)) return fail(DSPARK_ERR_CUDA, "cannot query the current device");
   const int nCTA = di.sms;
-  const WsLayout L = ws_layout(a.head, a.B, a.G, a.V, a.r, nCTA, a.target ? DSPARK_WS_TARGET : 0);
+  const bool w2rv = a.w2_layout == DSPARK_W2_RV;
+  const WsLayout L = ws_layout(a.head, a.B, a.G, a.V, a.r, nCTA,
+                               (a.target ? DSPARK_WS_TARGET : 0) | (w2rv ? DSPARK_WS_W2_RV : 0));
   if (!a.ws || !aligned(a.ws, 256) || a.ws_bytes < L.total)
     return fail(DSPARK_ERR_WORKSPACE, "workspace must be 256-byte aligned and >= %zu bytes", L.total);
   const int w_bf16 = a.wdt == DSPARK_BF16, u_bf16 = a.udt == DSPARK_BF16;
@@ -254,6 +263,12 @@ dspark_status run_draft(const DraftArgs& a) {
   }
 
   if (path == 0 || path == 2) {
+    if (w2rv) {  // these kernels read [V][r]: transpose W2 into the workspace first
+      void* w2t = (uint8_t*)a.ws + L.w2t;
+      cudaError_t e = launch_transpose(a.W2, w2t, a.r, a.V, w_bf16 ? 2 : 4, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "W2 transpose launch");
+      p.W2 = w2t;
+    }
     p.tcv = path == 2;
     if (p.tcv && !draft_cc_configure(p, (size_t)di.smem_optin) && !std::getenv("DSPARK_DRAFT_PATH") &&
         draft_cc_supported(a.B, a.r, w_bf16))
@@ -264,6 +279,9 @@ dspark_status run_draft(const DraftArgs& a) {
     if (e != cudaSuccess) return cuda_fail(e, "draft_cc launch");
   } else {
     if (a.V > (1 << 24) - 1) return fail(DSPARK_ERR_UNSUPPORTED, "V too large for the tensor-core path");
+    if (w2rv && a.V % 8 != 0)
+      return fail(DSPARK_ERR_UNSUPPORTED, "W2 as [r][V] on the tensor-core path needs V a multiple of 8");
+    p.w2_rv = w2rv;
     if (!draft_tc_configure(p, (size_t)di.smem_optin))
       return fail(DSPARK_ERR_UNSUPPORTED, "rank too large for shared memory");
     cudaError_t e = launch_draft_tc(p, nCTA, stream);
@@ -289,27 +307,29 @@ size_t dspark_workspace_bytes(int head, int B, int gamma, int V, int r, int d, i
 
 dspark_status dspark_markov_draft(int B, int gamma, int V, int r, int d, float T, uint64_t seed,
                                   dspark_dtype wdt, const void* W1, const void* W2,
-                                  const void* w, dspark_dtype udt, const void* U, const void* h,
+                                  dspark_w2_layout w2_layout, const void* w, dspark_dtype udt,
+                                  const void* U, const void* h,
                                   const int32_t* x0, const int32_t* forced, const float* target,
                                   int32_t* tokens, float* lse, float* c, float* S, float* cstar,
                                   float* l1, float* logits, void* workspace,
                                   size_t workspace_bytes, void* stream) {
   DraftArgs a{0,       B,      gamma,  V,      r,      d,     T,     seed,    wdt,
-              udt,     W1,     W2,     w,      nullptr, U,    h,     x0,      forced,
+              udt,     W1,     W2,     (int)w2_layout,     w,      nullptr, U,    h,     x0,      forced,
               target,  nullptr, tokens, lse,   c,      S,     cstar, l1,      logits,
               nullptr, workspace, workspace_bytes, stream};
   return run_draft(a);
 }
 
 dspark_status dspark_rnn_draft(int B, int gamma, int V, int r, int d, float T, uint64_t seed,
-                               dspark_dtype wdt, const void* W1, const void* W2, const void* w,
-                               const void* Wj, dspark_dtype udt, const void* U, const void* h,
+                               dspark_dtype wdt, const void* W1, const void* W2,
+                               dspark_w2_layout w2_layout, const void* w, const void* Wj,
+                               dspark_dtype udt, const void* U, const void* h,
                                const int32_t* x0, const int32_t* forced, const float* target,
                                const float* s0, int32_t* tokens, float* lse, float* c, float* S,
                                float* cstar, float* l1, float* logits, float* s_out,
                                void* workspace, size_t workspace_bytes, void* stream) {
   DraftArgs a{1,      B,     gamma,  V,     r,     d,     T,      seed,      wdt,
-              udt,    W1,    W2,     w,     Wj,    U,     h,      x0,        forced,
+              udt,    W1,    W2,     (int)w2_layout,     w,     Wj,    U,     h,      x0,        forced,
               target, s0,    tokens, lse,   c,     S,     cstar,  l1,        logits,
               s_out,  workspace, workspace_bytes, stream};
   return run_draft(a);

@@ -222,6 +222,29 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(int B, int G, i
   for (int i = tid; i < mstar; i += kSchedThreads) atomicAdd(&len[(int)(keys[i] & 0xFFFFFFu)], 1);
 }
 
+
+// dst[c][r] = src[r][c] through a 32 x 32 shared-memory tile (one padding column, so the
+// column-wise reads hit 32 different banks); 32 x 8 threads, four rows each.  The small-batch
+// draft kernels read W2 as [V][r]; a caller holding the pages' [r][V] gets it transposed here.
+template <typename T>
+__global__ void __launch_bounds__(256) transpose_kernel(const T* __restrict__ src, T* __restrict__ dst,
+                                                        int rows, int cols) {
+  __shared__ T tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < 32; i += 8) {
+    const int r = r0 + ty + i, c = c0 + tx;
+    if (r < rows && c < cols) tile[ty + i][tx] = src[(size_t)r * cols + c];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 32; i += 8) {
+    const int c = c0 + ty + i, r = r0 + tx;
+    if (r < rows && c < cols) dst[(size_t)c * rows + r] = tile[tx][ty + i];
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_confidence(int B, int G, int V, int r, int d, int w_bf16, const void* W1,
@@ -250,6 +273,15 @@ cudaError_t launch_prefix_schedule(int B, int G, const float* S, const double* s
                                        (int)smem);
   if (e != cudaSuccess) return e;
   schedule_kernel<<<1, kSchedThreads, smem, stream>>>(B, G, M, Mp2, S, sps, len, theta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose(const void* src, void* dst, int rows, int cols, int es, cudaStream_t stream) {
+  const dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32));
+  if (es == 2)
+    transpose_kernel<uint16_t><<<grid, 256, 0, stream>>>((const uint16_t*)src, (uint16_t*)dst, rows, cols);
+  else
+    transpose_kernel<uint32_t><<<grid, 256, 0, stream>>>((const uint32_t*)src, (uint32_t*)dst, rows, cols);
   return cudaGetLastError();
 }
 

@@ -533,7 +533,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               }
               mbar_expect_tx(&full[slot], kSlab);
-              tc::tma_load_2d(ring + (size_t)slot * kSlab, &tmap_w2, s * 64, yt, &full[slot], pol);
+              if (!p.w2_rv) {  // [V][r]: 128 vocabulary rows x 64 K (K-major)
+                tc::tma_load_2d(ring + (size_t)slot * kSlab, &tmap_w2, s * 64, yt, &full[slot], pol);
+              } else {  // [r][V]: two boxes of 64 vocabulary entries x 64 K rows (MN-major)
+                tc::tma_load_2d(ring + (size_t)slot * kSlab, &tmap_w2, yt, s * 64, &full[slot], pol);
+                tc::tma_load_2d(ring + (size_t)slot * kSlab + kSlab / 2, &tmap_w2, yt + 64, s * 64,
+                                &full[slot], pol);
+              }
             }
           }
       if (stop) atomicMax(&hdr->status, kErrTimeout);
@@ -548,7 +554,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // =========================================================== MMA issuer + TMEM owner
   if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16_f32(kM, kNT);
+      // W2 as [r][V] is an MN-major B operand: 64-entry blocks 8 KB apart, K steps of 16 rows
+      // 2 KB apart; as [V][r] it is K-major, K steps 32 bytes apart along the swizzled rows
+      // (descriptors are built once per slab; a K step adds to the 16-byte-unit address field,
+      // which cannot carry: every address stays inside its slab, below the 256 KB window)
+      const bool bmn = p.w2_rv != 0;
+      const uint32_t idesc = tc::idesc_bf16_f32(kM, kNT) | (bmn ? tc::kIdescBMajorMN : 0u);
+      const uint64_t bstep = bmn ? 2048 >> 4 : 32 >> 4;
       int g = 0, acc_i = 0;
       bool stop = false;
       for (int ks = 0; ks < G && !stop; ++ks)
@@ -582,16 +594,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_after_sync();
                 const uint32_t b_base = smem_u32(ring + (size_t)slot * kSlab);
                 const uint32_t a_s = a_base + s * ab_bytes + a_row;
+                const uint64_t bd = bmn ? tc::sdesc_sw128_mn(b_base, kSlab / 2) : tc::sdesc_sw128(b_base);
+                const uint64_t ad = tc::sdesc_sw128(a_s);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                  tc::mma_bf16(tmem + acc * kNT, tc::sdesc_sw128(a_s + kk * 32),
-                               tc::sdesc_sw128(b_base + kk * 32), idesc, (h | s | kk) != 0);
+                  tc::mma_bf16(tmem + acc * kNT, ad + 2 * kk, bd + bstep * kk, idesc, (h | s | kk) != 0);
                 if (RNN) {  // a_k = hi + lo: the low halves against the same W2 slab
-                  const uint32_t a_lo = a_s + nslab * ab_bytes;
+                  const uint64_t alo = tc::sdesc_sw128(a_s + nslab * ab_bytes);
 #pragma unroll
                   for (int kk = 0; kk < 4; ++kk)
-                    tc::mma_bf16(tmem + acc * kNT, tc::sdesc_sw128(a_lo + kk * 32),
-                                 tc::sdesc_sw128(b_base + kk * 32), idesc, 1u);
+                    tc::mma_bf16(tmem + acc * kNT, alo + 2 * kk, bd + bstep * kk, idesc, 1u);
                 }
                 tc::mma_commit(&empty[slot]);
               }
@@ -990,10 +1002,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = pk ? 2 * rd + half : rd;  // this warp's tile position of the round
         const bool tile_ok = t < ntile;          // (packed, odd count: the last round has one)
         const int vb = (t0 + tile_at(t, u, ntile)) * kNT + cq * 32;  // first entry of this thread's 32
-        if (row_ok && t + 3 * tstep < ntile) {  // this thread's U line, 3 rounds ahead
-          const size_t vp = urow + (size_t)(t0 + tile_at(t + 3 * tstep, u, ntile)) * kNT + cq * 32;
-          if (nu > 0) prefetch_line((const __nv_bfloat16*)Up + vp);
-        }
         // the tile's U: staged by TMA, kept until the tile is done; else read from global
         int us = -1;
         if (nu > 0) {
@@ -1229,8 +1237,10 @@ bool draft_tc_configure(DraftParams& p, size_t smem_optin) {
 }
 
 cudaError_t launch_draft_tc(DraftParams& p, int nblocks, cudaStream_t stream) {
-  CUtensorMap tmap;
-  if (!encode_bf16_2d(&tmap, p.W2, p.V, p.r, p.r, kNT)) return cudaErrorInvalidValue;
+  CUtensorMap tmap;  // W2 tiles: [V][r] in boxes of 128 rows x 64 K, [r][V] in 64 x 64 boxes
+  if (!(p.w2_rv ? encode_bf16_2d(&tmap, p.W2, p.r, p.V, p.V, 64)
+                : encode_bf16_2d(&tmap, p.W2, p.V, p.r, p.r, kNT)))
+    return cudaErrorInvalidValue;
   const bool tg = p.target != nullptr;
   const void* kern = p.head == 1 ? (tg ? (const void*)draft_tc_kernel<true, true>
                                        : (const void*)draft_tc_kernel<true, false>)

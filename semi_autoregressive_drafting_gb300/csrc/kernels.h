@@ -6,6 +6,8 @@
 
 namespace dspark {
 
+// dst[c][r] = src[r][c] for a rows x cols matrix of 2- or 4-byte elements (es), both row-major.
+cudaError_t launch_transpose(const void* src, void* dst, int rows, int cols, int es, cudaStream_t stream);
 cudaError_t launch_confidence(int B, int G, int V, int r, int d, int w_bf16, const void* W1,
                               const void* w, int u_bf16, const void* h, const int32_t* x0,
                               const int32_t* tokens, float* c, float* S, cudaStream_t stream);

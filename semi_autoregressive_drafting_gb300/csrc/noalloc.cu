@@ -85,7 +85,7 @@ extern "C" dspark_status dspark_markov_draft_noalloc(
       return DSPARK_ERR_CUDA;
     }
   }
-  st = dspark_markov_draft(B, gamma, V, r, d, T, seed, wdt, W1, W2, w, udt, U, h, x0, forced,
+  st = dspark_markov_draft(B, gamma, V, r, d, T, seed, wdt, W1, W2, DSPARK_W2_VR, w, udt, U, h, x0, forced,
                            target, tokens, lse, c, S, cstar, l1, logits, ws, kNoAllocScratchBytes,
                            stream);
   if (st != DSPARK_OK) return st;

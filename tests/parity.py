@@ -111,9 +111,10 @@ def compare_floats(out, o, rows=None, logits=True, z_rows=None):
 
 
 def run_case(wl, *, target_noise=None, want_logits=True, rows=None, check_free=True, ds=None,
-             s0_scale=None, z_rows=None):
+             s0_scale=None, z_rows=None, w2_layout="vr"):
     """Free-running and teacher-forced GPU draft against the oracle on the same inputs.
-    z_rows (a subset of rows): compare the logits z element-wise on those requests only."""
+    z_rows (a subset of rows): compare the logits z element-wise on those requests only.
+    w2_layout "rv": the library gets W2 as [r][V] (the oracle keeps its [V][r] copy)."""
     if z_rows is not None:
         want_logits = True
     if target_noise is not None:
@@ -127,8 +128,12 @@ def run_case(wl, *, target_noise=None, want_logits=True, rows=None, check_free=T
     o = oracle_draft(wl, t, rows=rows, want_z=want_logits)
     assert o.status == 0
     has_t = d.get("target") is not None
-    ws = ds.Workspace(1 if rnn else 0, wl.B, wl.gamma, wl.V, wl.r, wl.d, target=has_t)
-    kw = dict(T=wl.T, seed=wl.seed, w=d["w"], target=d.get("target"), workspace=ws)
+    if w2_layout == "rv":
+        d["W2"] = d["W2"].t().contiguous()
+    ws = ds.Workspace(1 if rnn else 0, wl.B, wl.gamma, wl.V, wl.r, wl.d, target=has_t,
+                      w2_layout=w2_layout)
+    kw = dict(T=wl.T, seed=wl.seed, w=d["w"], target=d.get("target"), workspace=ws,
+              w2_layout=w2_layout)
     if rnn:
         call = lambda **k: ds.rnn_draft(d["W1"], d["W2"], d["Wj"], d["U"], d["h"], d["x0"],
                                         s0=d.get("s0"), **kw, **k)
@@ -147,5 +152,5 @@ def run_case(wl, *, target_noise=None, want_logits=True, rows=None, check_free=T
     assert ws.status() == 0
     ties += check_tokens_forced(_rows(tf.tokens, rows), o)
     errs = compare_floats(tf, o, rows=rows, logits=want_logits, z_rows=z_rows)
-    print(f"{wl.name} B={wl.B} V={wl.V} r={wl.r}: near-ties {ties}, max errors {errs}")
+    print(f"{wl.name} B={wl.B} V={wl.V} r={wl.r} W2 {w2_layout}: near-ties {ties}, max errors {errs}")
     return ties, errs

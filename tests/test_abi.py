@@ -47,14 +47,17 @@ def test_no_torch_in_the_abi():
 def test_host_validation_without_gpu(lib):
     V, r = 4096, 64
     p = ctypes.c_void_p(16)
-    args = lambda B, G, V, r, d, T: (B, G, V, r, d, T, 0, 0, p, p, None, 0, p, None, p, None,
-                                     None, p, p, None, None, None, None, None, p, 1 << 20, None)
+    args = lambda B, G, V, r, d, T, lay=0: (B, G, V, r, d, T, 0, 0, p, p, lay, None, 0, p, None, p,
+                                            None, None, p, p, None, None, None, None, None, p,
+                                            1 << 20, None)
     assert lib.dspark_markov_draft(*args(0, 7, V, r, 0, 1.0)) == 1      # B = 0
     assert lib.dspark_markov_draft(*args(1, 17, V, r, 0, 1.0)) == 1     # gamma > 16
     assert lib.dspark_markov_draft(*args(1, 7, V, 60, 0, 1.0)) == 1     # r not a multiple of 8
     assert lib.dspark_markov_draft(*args(1, 7, V, r, 0, 0.0)) == 1      # T = 0
     assert lib.dspark_markov_draft(*args(1, 7, V, r, 0, float("nan"))) == 1
     assert b"T must be" in lib.dspark_last_error()
+    assert lib.dspark_markov_draft(*args(1, 7, V, r, 0, 1.0, 2)) == 1   # unknown W2 layout
+    assert b"W2 layout" in lib.dspark_last_error()
     assert lib.dspark_prefix_schedule(1000, 17, p, p, p, p, None) == 1
     assert lib.dspark_tv_label(0, 10, 1.0, p, p, p, None, None) == 1
 

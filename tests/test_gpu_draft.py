@@ -33,8 +33,14 @@ def _use_path(monkeypatch, name, code, wl, head=0):
     assert ds.draft_path(head, wl.B, wl.V, wl.r, wl.dtype == "bf16") == code
 
 
-def test_tiny_markov_workload():
-    _run_case(TINY)
+# W2 as the pages write it ([r][V]) or as a linear layer's weight ([V][r]); the small-batch
+# kernels read the [r][V] form through a transposed copy in the workspace
+LAYOUTS = ["vr", "rv"]
+
+
+@pytest.mark.parametrize("lay", LAYOUTS)
+def test_tiny_markov_workload(lay):
+    _run_case(TINY, w2_layout=lay)
 
 
 @pytest.mark.parametrize("B", [1, 2, 3])
@@ -47,8 +53,9 @@ def test_block_sizes(gamma):
     _run_case(TINY.with_(gamma=gamma, seed=20 + gamma))
 
 
-def test_temperature_and_target_fp32():
-    _run_case(TINY.with_(T=0.7, seed=31), target_noise=1.0)
+@pytest.mark.parametrize("lay", LAYOUTS)
+def test_temperature_and_target_fp32(lay):
+    _run_case(TINY.with_(T=0.7, seed=31), target_noise=1.0, w2_layout=lay)
 
 
 def test_ragged_vocab_unaligned_rows():
@@ -68,12 +75,13 @@ def test_bf16_small_with_target(monkeypatch, name, code):
     _run_case(wl, target_noise=1.0)
 
 
+@pytest.mark.parametrize("lay", LAYOUTS)
 @pytest.mark.parametrize("name,code", SMALL_PATHS)
 @pytest.mark.parametrize("B", [1, 2, 4])
-def test_bf16_batches_both_paths(monkeypatch, name, code, B):
+def test_bf16_batches_both_paths(monkeypatch, name, code, B, lay):
     wl = inputs.WORKLOADS["qwen3_4b_markov"].with_(V=30000, d=256, B=B, seed=50 + B)
     _use_path(monkeypatch, name, code, wl)
-    _run_case(wl)
+    _run_case(wl, w2_layout=lay)
 
 
 @pytest.mark.parametrize("V", [1000, 130, 40])
@@ -115,11 +123,12 @@ def test_qwen3_4b_vocab_small_hidden(monkeypatch, name, code):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("lay", LAYOUTS)
 @pytest.mark.parametrize("name,code", SMALL_PATHS)
-def test_qwen3_4b_markov_full(monkeypatch, name, code):
+def test_qwen3_4b_markov_full(monkeypatch, name, code, lay):
     wl = inputs.WORKLOADS["qwen3_4b_markov"]
     _use_path(monkeypatch, name, code, wl)
-    ties, _ = _run_case(wl, want_logits=False)
+    ties, _ = _run_case(wl, want_logits=False, w2_layout=lay)
     assert ties <= 1
 
 

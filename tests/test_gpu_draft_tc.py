@@ -24,22 +24,40 @@ def _run(wl, **kw):
     return parity.run_case(wl, ds=ds, **kw)
 
 
+# W2 as the pages write it ([r][V], an MN-major operand) or as a linear layer's weight ([V][r],
+# K-major); [r][V] needs V a multiple of 8 on this path, so its ragged cases use V = 20008
+LAYOUTS = ["vr", "rv"]
+
+
+@pytest.mark.parametrize("lay", LAYOUTS)
 @pytest.mark.parametrize("B", [5, 8, 64])
-def test_tc_small_vocab(B):
-    _run(BASE.with_(B=B, V=9000, d=256, seed=60 + B))
+def test_tc_small_vocab(B, lay):
+    _run(BASE.with_(B=B, V=9000, d=256, seed=60 + B), w2_layout=lay)
 
 
-def test_tc_two_chunks_ragged_vocab():
-    _run(BASE.with_(B=130, V=20001, d=128, seed=70), want_logits=False)
+@pytest.mark.parametrize("lay,V", [("vr", 20001), ("rv", 20008)])
+def test_tc_two_chunks_ragged_vocab(lay, V):
+    _run(BASE.with_(B=130, V=V, d=128, seed=70), want_logits=False, w2_layout=lay)
 
 
+@pytest.mark.parametrize("lay", LAYOUTS)
 @pytest.mark.parametrize("r", [64, 192, 512])
-def test_tc_ranks(r):
-    _run(BASE.with_(B=16, V=12000, r=r, d=64, seed=80 + r // 64))
+def test_tc_ranks(r, lay):
+    _run(BASE.with_(B=16, V=12000, r=r, d=64, seed=80 + r // 64), w2_layout=lay)
 
 
-def test_tc_target_labels():
-    _run(BASE.with_(B=24, V=30000, d=256, T=0.8, seed=90), target_noise=1.0)
+@pytest.mark.parametrize("lay", LAYOUTS)
+def test_tc_target_labels(lay):
+    _run(BASE.with_(B=24, V=30000, d=256, T=0.8, seed=90), target_noise=1.0, w2_layout=lay)
+
+
+def test_tc_rv_needs_16_byte_rows():
+    # [r][V] with V not a multiple of 8 cannot be tiled by TMA: rejected on the host
+    wl = BASE.with_(B=8, V=9001, d=64, seed=95)
+    t = parity.to_dev(inputs.generate(wl))
+    with pytest.raises(ds._lib.DsparkError, match="multiple of 8"):
+        ds.markov_draft(t["W1"], t["W2"].t().contiguous(), t["U"], t["x0"], h=t["h"], w=t["w"],
+                        w2_layout="rv")
 
 
 def test_tc_invalid_anchor_and_repeatability():
@@ -68,22 +86,24 @@ def sampled_rows(B, n=32, seed=0):
 
 
 @pytest.mark.slow
-def test_qwen3_8b_labels_full_sampled_rows():
+@pytest.mark.parametrize("lay", LAYOUTS)
+def test_qwen3_8b_labels_full_sampled_rows(lay):
     # the whole workload on the GPU, in the configuration the benchmark times; 32 of its 64
     # requests compared with the oracle (tokens, lse, c, S, c*, l1), z element-wise on two
     wl = inputs.WORKLOADS["qwen3_8b_labels"]
     rows = sampled_rows(wl.B, seed=3)
-    ties, _ = _run(wl, rows=rows, z_rows=[rows[0], rows[-1]])
+    ties, _ = _run(wl, rows=rows, z_rows=[rows[0], rows[-1]], w2_layout=lay)
     assert ties <= 2
 
 
 @pytest.mark.slow
-def test_high_concurrency_full_sampled_rows():
+@pytest.mark.parametrize("lay", LAYOUTS)
+def test_high_concurrency_full_sampled_rows(lay):
     # 32 of the 512 requests (all four 128-request chunks), z element-wise on two
     wl = inputs.WORKLOADS["high_concurrency_sched"]
     rows = sampled_rows(wl.B, seed=4)
     assert len({r // 128 for r in rows}) == 4
-    ties, _ = _run(wl, rows=rows, z_rows=[rows[1], rows[-1]])
+    ties, _ = _run(wl, rows=rows, z_rows=[rows[1], rows[-1]], w2_layout=lay)
     assert ties <= 2
 
 
@@ -94,8 +114,10 @@ def test_tc_gamma15(B, G):
          target_noise=1.0 if B == 64 else None)
 
 
-@pytest.mark.parametrize("B,V", [(37, 40000), (64, 38537), (6, 2000)])
-def test_tc_paired_tiles(B, V):
+@pytest.mark.parametrize("B,V,lay", [(37, 40000, "vr"), (64, 38537, "vr"), (6, 2000, "vr"),
+                                     (37, 40000, "rv"), (64, 38536, "rv")])
+def test_tc_paired_tiles(B, V, lay):
     # at most 64 requests: vocabulary tiles go in pairs (lanes 64-127 hold the second tile);
     # blocks with an odd tile count end with a single-tile round
-    _run(BASE.with_(B=B, V=V, d=128, seed=100 + B), target_noise=0.5 if B == 37 else None)
+    _run(BASE.with_(B=B, V=V, d=128, seed=100 + B), target_noise=0.5 if B == 37 else None,
+         w2_layout=lay)

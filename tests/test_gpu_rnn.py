@@ -39,11 +39,21 @@ def test_rnn_small_batch_rank64_target(monkeypatch, name, code):
     parity.run_case(wl, ds=ds, target_noise=1.0)
 
 
+@pytest.mark.parametrize("lay", ["vr", "rv"])
 @pytest.mark.parametrize("B", [8, 64])
-def test_rnn_tensor_core(B):
+def test_rnn_tensor_core(B, lay):
     wl = RNN.with_(B=B, V=10000, d=256, seed=110 + B)
     assert ds.draft_path(1, B, wl.V, wl.r) == 1
-    parity.run_case(wl, ds=ds, s0_scale=0.5)
+    parity.run_case(wl, ds=ds, s0_scale=0.5, w2_layout=lay)
+
+
+@pytest.mark.parametrize("name,code", SMALL_PATHS)
+def test_rnn_small_batch_w2_rv(monkeypatch, name, code):
+    # W2 as [r][V] on the small-batch kernels (read through the transposed copy)
+    wl = RNN.with_(B=2, V=12000, d=128, seed=106)
+    monkeypatch.setenv("DSPARK_DRAFT_PATH", name)
+    assert ds.draft_path(1, wl.B, wl.V, wl.r) == code
+    parity.run_case(wl, ds=ds, s0_scale=0.5, w2_layout="rv")
 
 
 def test_rnn_tensor_core_two_chunks_target():
@@ -56,5 +66,6 @@ def test_rnn_head_full_sampled_rows():
     # 32 of the 128 requests (tokens, lse, c, S and the final state), z element-wise on two
     rng = np.random.default_rng(5)
     rows = sorted({0, 127, *rng.choice(np.arange(1, 127), size=30, replace=False).tolist()})
-    ties, _ = parity.run_case(RNN, ds=ds, rows=rows, z_rows=[rows[0], rows[-1]])
-    assert ties <= 2
+    for lay in ("vr", "rv"):
+        ties, _ = parity.run_case(RNN, ds=ds, rows=rows, z_rows=[rows[0], rows[-1]], w2_layout=lay)
+        assert ties <= 2
