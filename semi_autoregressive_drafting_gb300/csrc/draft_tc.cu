@@ -173,9 +173,6 @@ __device__ __forceinline__ float ex2f(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ void prefetch_line(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
 
 // (max, sum-exp) of all blocks' partials, merged by one warp in a fixed order: each lane issues
 // the loads of up to 8 partials, the warp takes their maximum M, then sums l_i exp(m_i - M)
@@ -996,7 +993,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       float tb = -INFINITY;
       float Cp = INFINITY;           // 1.002 exp(m - tb)
       volatile float* const sb_own = sbest + kpart * kM + m;
-      const int tstep = pk ? 2 : 1;  // this warp's tile advances by tstep per round
       for (int rd = 0; rd < nround; ++rd, ++acc_i) {
         const int acc = acc_i % kAcc;
         const int t = pk ? 2 * rd + half : rd;  // this warp's tile position of the round
