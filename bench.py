@@ -41,10 +41,10 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: every timed block starts with a cold
 # without a capture, or whose kernel changed since, reports null.
 TRAFFIC = {
     "qwen3_4b_markov": ("draft_cc.cu", "a654b711be85aa4d", 83114240),          # 80.62 + 2.49 MB
-    "high_concurrency_sched": ("draft_tc.cu", "3aaea69704e3ef26", 5723947520),  # 5717 + 7.4 MB
+    "high_concurrency_sched": ("draft_tc.cu", "1a5777e647e31320", 2411718656),  # 2407 + 4.2 MB
     # draft_tc_kernel alone; the target's normalisers (272.4 MB) are a launch before it
-    "qwen3_8b_labels": ("draft_tc.cu", "3aaea69704e3ef26", 1085017856),         # 974.3 + 110.7 MB
-    "rnn_head": ("draft_tc.cu", "3aaea69704e3ef26", 538618880),                 # 533.8 + 4.8 MB
+    "qwen3_8b_labels": ("draft_tc.cu", "1a5777e647e31320", 643011584),         # 615.3 + 27.8 MB
+    "rnn_head": ("draft_tc.cu", "1a5777e647e31320", 528793088),                 # 524.0 + 4.8 MB
     # the three verify kernels of one call (bench.py --op verify)
     "verify qwen3_8b_labels": ("verify.cu", "256b8f8a4f1f9538", 659341312),
     # the four loss kernels of one call (bench.py --op loss)
@@ -586,7 +586,24 @@ def build_parser():
                     help="draft: the draft block (default); verify: the speculative accept/reject "
                          "step on the workload's B, gamma, V; loss: the training losses (Eqs 9-12) "
                          "and their gradients on that shape")
+    ap.add_argument("--shape", default="",
+                    help="comma-separated overrides of the workload's sizes, e.g. "
+                         "'V=65536,d=512': a smaller case of the same kernels for counter "
+                         "captures; the workload name then carries the overrides")
     return ap
+
+
+def override_shape(wl, spec):
+    """The workload with the sizes in `spec` ('B=512,V=65536') replaced; its name records them."""
+    if not spec:
+        return wl
+    kw = {}
+    for item in spec.split(","):
+        key, _, val = item.partition("=")
+        if key not in ("B", "gamma", "V", "r", "d"):
+            raise SystemExit(f"--shape: unknown size {key!r} (B, gamma, V, r, d)")
+        kw[key] = int(val)
+    return wl.with_(name=f"{wl.name}[{spec}]", **kw)
 
 
 def main():
@@ -598,7 +615,7 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
     from semi_autoregressive_drafting_gb300 import inputs
-    wl = inputs.WORKLOADS[args.workload]
+    wl = override_shape(inputs.WORKLOADS[args.workload], args.shape)
 
     if args.impl == "reference":
         if rank == 0:

@@ -68,3 +68,13 @@ def test_clock_summary_from_nvml_samples():
     s = c.summary()
     assert s["samples"] == 3 and s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
     assert s["reasons"] == ["sw_power_cap"]  # idle (0x1) is not a throttle reason
+
+
+def test_shape_override_renames_and_resizes():
+    wl = bench.override_shape(inputs.WORKLOADS["high_concurrency_sched"], "V=65536,d=512")
+    assert (wl.B, wl.V, wl.d, wl.r) == (512, 65536, 512, 256)
+    assert wl.name == "high_concurrency_sched[V=65536,d=512]"
+    assert wl.name not in bench.TRAFFIC  # a resized case carries no traffic record
+    assert bench.override_shape(wl, "") is wl
+    with pytest.raises(SystemExit):
+        bench.override_shape(wl, "T=2")

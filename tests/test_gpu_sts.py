@@ -1,7 +1,12 @@
 """GPU parity of sequential temperature scaling (dspark_sts) against the fp64 oracle: the chosen
 temperatures are identical, except where the oracle's own ECE at the GPU's choice is within
 1e-5 of its minimum (a near-tie of the grid search; the comparison stops there, since later
-positions then hold different prefixes); ECE values within 2e-3."""
+positions then hold different prefixes).
+
+ECE values within 2e-5 + 4/N: the per-bin sums run in fp32 against fp64 (errors near 1e-6 at
+these sizes), and a sample whose confidence product lies on a bin edge can land in the
+neighbouring bin in one precision and not the other, which moves its |S - y| <= 1 between two
+bins and the ECE by at most 2/N; the bound allows two such samples per value."""
 import numpy as np
 import pytest
 import torch
@@ -38,13 +43,16 @@ def test_sts_matches_oracle(N, taus, bins):
                               torch.from_numpy(grid).cuda(), bins=bins)
     assert st == 0
     tau, ece, eg = tau.cpu().numpy(), ece.cpu().numpy(), eg.cpu().numpy()
+    tol = 2e-5 + 4.0 / N
+    worst = 0.0
     for k in range(len(taus)):
-        parity.close(f"ece_grid[{k}]", eg[k], eg_o[k])
+        worst = max(worst, parity.close(f"ece_grid[{k}]", eg[k], eg_o[k], tol=tol))
         if tau[k] != tau_o[k]:
             g = int(np.argmin(np.abs(grid - tau[k])))
             assert eg_o[k, g] - ece_o[k] < 1e-5, (k, tau[k], tau_o[k])
             break
-        parity.close(f"ece[{k}]", ece[k], ece_o[k])
+        parity.close(f"ece[{k}]", ece[k], ece_o[k], tol=tol)
+    print(f"N={N}: max |ECE gpu - oracle| {worst:.3g} (tolerance {tol:.3g})")
 
 
 def test_sts_invalid_accepted_length():
