@@ -326,6 +326,20 @@ const char* dspark_last_error(void);
  */
 int dspark_draft_path(int head, int B, int V, int r, dspark_dtype wdt);
 
+/*
+ * Blocks per thread-block cluster of the draft kernel paths 0 and 2 use on the current device
+ * (1 = no clusters; path 1 always 1).  Those kernels run one block per SM; the blocks of a
+ * cluster merge their per-step argmax keys and (max, sum-exp) partials in distributed shared
+ * memory, and one block per cluster publishes the merged result to the other clusters.
+ * Clusters are used only when DSPARK_CLUSTER = 2 | 4 | 8 (read at every call) asks for them: a
+ * draft call then fails with DSPARK_ERR_UNSUPPORTED if clusters of that size cannot all be
+ * resident at once, one block per SM (clusters must fit inside one GPC); other values, or
+ * none, mean no clusters.  On GB300 only 2-block clusters tile the 152 SMs, and there the extra
+ * hop per step costs more than the halved merge saves, hence the default.  Negative for
+ * arguments a draft call would reject, or without a device.
+ */
+int dspark_draft_cluster(int head, int B, int V, int r, dspark_dtype wdt);
+
 /* Number of kernel launches one draft call with these arguments makes on its stream, without a
  * target (on path 1 a target adds one: its normalisers are formed by a streaming launch before
  * the draft). */

@@ -358,6 +358,11 @@ def draft_launches(head: int, B: int, V: int, r: int, bf16: bool = True) -> int:
     return _lib.load().dspark_draft_launches(head, B, V, r, _BF16 if bf16 else _F32)
 
 
+def draft_cluster(head: int, B: int, V: int, r: int, bf16: bool = True) -> int:
+    """Blocks per thread-block cluster of the draft kernel these arguments select (1: none)."""
+    return _lib.load().dspark_draft_cluster(head, B, V, r, _BF16 if bf16 else _F32)
+
+
 def draft_loss_launches(B: int, gamma: int, V: int, with_grad: bool = True) -> int:
     """Kernel launches of one draft_loss call (the sub-batch pipeline and the totals)."""
     return _lib.load().dspark_draft_loss_launches(B, gamma, V, int(with_grad))

@@ -41,6 +41,7 @@ SIGNATURES = {
     "dspark_last_error": (ctypes.c_char_p, []),
     "dspark_draft_path": (I, [I, I, I, I, I]),
     "dspark_draft_launches": (I, [I, I, I, I, I]),
+    "dspark_draft_cluster": (I, [I, I, I, I, I]),
     "dspark_draft_loss_launches": (I, [I, I, I, I]),
 }
 

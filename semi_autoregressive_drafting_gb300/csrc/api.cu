@@ -1,7 +1,7 @@
 // api.cu -- the C ABI of libdspark (declared in include/dspark.h): argument validation,
 // workspace layout, kernel-path selection and stream-ordered launches.  No torch types, no
-// allocation; the only process-wide state is a per-device cache of SM count and shared-memory
-// limit (filled once, under a mutex).
+// allocation; the only process-wide state is a per-device cache of SM count, shared-memory
+// limit and the largest thread-block cluster that tiles every SM (filled once, under a mutex).
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
@@ -39,7 +39,45 @@ struct DevInfo {
   bool init = false;
   int sms = 0;
   int smem_optin = 0;
+  int cluster = 1;  // largest of 8, 4, 2 whose clusters of one-block-per-SM blocks fill every SM
 };
+
+// Stand-in for the small-batch draft kernel when sizing clusters: it has the same one block
+// per SM (all the shared memory a block may have), and is never launched.
+__global__ void cluster_probe_kernel() {}
+
+// Largest cluster size C in {8, 4, 2} with sms % C == 0 such that sms / C clusters of
+// whole-SM blocks can be resident at once (clusters must fit inside one GPC, so this depends on
+// how the GPCs' SMs are split); 1 if none.
+int fitting_cluster(int sms, int smem_optin) {
+  if (cudaFuncSetAttribute(cluster_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem_optin) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  for (int c = 8; c >= 2; c /= 2) {
+    if (sms % c) continue;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = (unsigned)c;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)sms);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = (size_t)smem_optin;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)cluster_probe_kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (n * c >= sms) return c;
+  }
+  return 1;
+}
 std::mutex g_mu;
 DevInfo g_dev[64];
 
@@ -54,6 +92,7 @@ bool dev_info(DevInfo* out) {
     if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
         cudaSuccess)
       return false;
+    d.cluster = fitting_cluster(d.sms, d.smem_optin);
     d.init = true;
   }
   *out = d;
@@ -125,6 +164,20 @@ int path_of(int head, int B, int V, int r, int w_bf16, int nCTA) {
   // full-width one, so the tensor cores pay off from B = 3 on; below that the CUDA cores win.
   if (ok[2] && B >= 3) return 2;
   return ok[0] ? 0 : ok[2] ? 2 : ok[1] ? 1 : -1;
+}
+
+// Blocks per cluster of the small-batch kernels (paths 0 and 2): DSPARK_CLUSTER = 2 | 4 | 8,
+// read at every call, asks for clusters of that size (-1 if they cannot tile the SMs); unset,
+// or 1, no clusters.  Measured on GB300 (152 SMs, where only 2-block clusters tile every SM):
+// the per-step hop through the cluster's first block costs more than halving the slots every
+// block polls saves (B = 1, V = 151936: 90 us per block without clusters), so clusters are not
+// the default.
+int cluster_of(const DevInfo& di, int nCTA) {
+  if (const char* f = std::getenv("DSPARK_CLUSTER")) {
+    const int want = std::atoi(f);
+    if (want == 2 || want == 4 || want == 8) return nCTA % want == 0 && want <= di.cluster ? want : -1;
+  }
+  return 1;
 }
 
 struct DraftArgs {
@@ -263,6 +316,8 @@ dspark_status run_draft(const DraftArgs& a) {
   }
 
   if (path == 0 || path == 2) {
+    p.cl = cluster_of(di, nCTA);
+    if (p.cl < 0) return fail(DSPARK_ERR_UNSUPPORTED, "DSPARK_CLUSTER: clusters of that size do not tile the SMs");
     if (w2rv) {  // these kernels read [V][r]: transpose W2 into the workspace first
       void* w2t = (uint8_t*)a.ws + L.w2t;
       cudaError_t e = launch_transpose(a.W2, w2t, a.r, a.V, w_bf16 ? 2 : 4, stream);
@@ -474,6 +529,15 @@ int dspark_draft_path(int head, int B, int V, int r, dspark_dtype wdt) {
   DevInfo di;
   const int nCTA = dev_info(&di) ? di.sms : 152;  // without a device: a GB300's count
   return path_of(head, B, V, r, wdt == DSPARK_BF16, nCTA);
+}
+
+int dspark_draft_cluster(int head, int B, int V, int r, dspark_dtype wdt) {
+  const int path = dspark_draft_path(head, B, V, r, wdt);
+  if (path < 0) return -1;
+  if (path == 1) return 1;
+  DevInfo di;
+  if (!dev_info(&di)) return -1;
+  return cluster_of(di, di.sms);
 }
 
 int dspark_draft_loss_launches(int B, int gamma, int V, int with_grad) {

@@ -355,6 +355,39 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
+// ------------------------------------------------------------------ thread-block clusters
+// (distributed shared memory: a block addresses a peer's shared memory through mapa)
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the variable at `p` (this block's shared memory) in block `rank`
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f2(uint32_t addr, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
+               : "memory");
+}
+// store with release semantics at cluster scope: this thread's earlier writes (local or remote)
+// are visible to any thread of the cluster that reads the value with acquire semantics
+__device__ __forceinline__ void st_release_cluster_u64(uint32_t addr, unsigned long long v) {
+  asm volatile("st.release.cluster.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_cluster_u64(const void* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+// Every thread of every block of the cluster: release what this thread wrote, wait for all
+// (hardware cluster barrier; each thread reaches it after bounded waits only)
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // L2 policy: stream once (weights re-read next step may still hit L2, but do not displace
 // the data that is read twice within a step).
 __device__ __forceinline__ uint64_t policy_evict_first() {

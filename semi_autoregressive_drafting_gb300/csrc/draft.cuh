@@ -64,6 +64,10 @@ struct DraftParams {
   int tc_nu;           // tensor-core path: U tiles staged in shared memory (0 = direct loads)
   int tc_pk;           // tensor-core path: at most 64 requests, vocabulary tiles in pairs
   int w2_rv;           // tensor-core path: W2 stored [r][V] (an MN-major operand), else [V][r]
+  int cl;              // draft_cc: blocks per thread-block cluster (1: no clusters); the
+                       // cluster's blocks merge their per-step results in distributed shared
+                       // memory and one of them publishes the cluster's, so the grid-wide merge
+                       // reads gridDim / cl slots instead of gridDim
   size_t smem_bytes;
   // failure-path test hook (0 in normal use): 1 = the per-step wait between thread blocks, 2 = an
   // mbarrier wait of the epilogue warps, each made to wait for a signal that never comes, with

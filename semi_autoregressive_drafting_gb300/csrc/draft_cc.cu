@@ -57,6 +57,11 @@ struct Misc {
   uint32_t tmem_base;          // TMEM columns caching the first stages of the slice
   float cbuf[64];              // last block: Eq 7 of every (request, step)
   bool cvalid[64];             // last block: the step's token is valid
+  // cluster leader (rank 0): each block's key and (max, sum-exp) partials of p^d and p^t for
+  // the current step, per request, written by the blocks of the cluster (the key last, with
+  // release semantics; its step tag tells the leader it is there)
+  unsigned long long ckey[4][8];
+  float2 cml[4][8], cmlt[4][8];
 };
 
 struct CCLayout {
@@ -531,6 +536,9 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
   constexpr int SR = 8 / NB;  // rows per sub-group: SR rows x NB requests = 8 sums per lane
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nCTA = gridDim.x, cta = blockIdx.x;
+  // clusters of C consecutive blocks (C = 1: none); cluster cid publishes slot cid of nCL
+  const int C = p.cl;
+  const int crk = C > 1 ? (int)cluster_rank() : 0, cid = cta / C, nCL = nCTA / C;
   const int B = p.B, G = p.gamma, V = p.V, r = p.r;
   const bool tgt = p.target != nullptr;
   const bool conf = p.h != nullptr && p.w != nullptr;
@@ -573,6 +581,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
       mbar_init(&uempty[i], 1);
     }
     mbar_init(never, 1);
+    for (int i = 0; i < 4 * 8; ++i) ms->ckey[i / 8][i % 8] = 0ull;  // no step's tag
     fence_mbar_init();
     ms->S_run = 1.f;
     ms->abort = 0;
@@ -596,6 +605,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
   }
   tc::fence_before_sync();
   __syncthreads();  // the last block-wide barrier: from here the producer warp runs on its own
+  if (C > 1) cluster_sync_all();  // every leader's barriers are initialised before any arrival
   tc::fence_after_sync();
 
   // =========================================================== producer warp
@@ -681,6 +691,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
       if (TCV)
         for (int i = 0; i < nres_s; ++i) mbar_wait(&rfull[i], 0);
     }
+    if (C > 1) cluster_sync_all();  // no block leaves while a peer may still write to it
     return;
   }
 
@@ -766,6 +777,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
       if (stop) atomicMax(&hdr->status, kErrTimeout);
       tc::mma_commit(mdone);  // lets the TMEM owner free the columns once these MMAs are done
     }
+    if (C > 1) cluster_sync_all();
     return;
   }
 
@@ -1151,9 +1163,10 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
       }
     }
     csync<kCThreads>();
+    bool ok = true;
     if (warp < B) {
       const int b = warp;
-      const size_t o = ((size_t)ks * B + b) * nCTA + cta;
+      const size_t o = ((size_t)ks * B + b) * nCL + cid;  // the block's (C = 1) or cluster's slot
       const bool has = SL > 0 && ms->valid[b];
       unsigned long long kb = 0;
       if (lane < kCWarps) {
@@ -1166,7 +1179,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
         kb = q > kb ? q : kb;
       }
       const unsigned long long pub = has && kb ? kb : tagged_key_empty(ks);
-      if (!tgt && lane == 0) st_relaxed64(&p.keys[o], pub);
+      if (C == 1 && !tgt && lane == 0) st_relaxed64(&p.keys[o], pub);
       float m = -INFINITY, l = 0.f, mt = -INFINITY, lt = 0.f;
       if (lane < kCWarps) {
         const Slot& q = slots[lane * 4 + b];
@@ -1182,14 +1195,65 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
           lse_merge(mt, lt, __shfl_xor_sync(0xffffffffu, mt, w), __shfl_xor_sync(0xffffffffu, lt, w));
       }
       if (lane == 0) {
-        p.ml[o] = make_float2(m, l);
-        if (tgt) {
-          p.mlt[o] = make_float2(mt, lt);
-          st_release64(&p.keys[o], pub);
+        if (C == 1) {
+          p.ml[o] = make_float2(m, l);
+          if (tgt) {
+            p.mlt[o] = make_float2(mt, lt);
+            st_release64(&p.keys[o], pub);
+          }
+        } else {  // to the cluster's leader, in its shared memory
+          st_cluster_f2(cluster_addr(&ms->cml[b][crk], 0), make_float2(m, l));
+          if (tgt) st_cluster_f2(cluster_addr(&ms->cmlt[b][crk], 0), make_float2(mt, lt));
+          st_release_cluster_u64(cluster_addr(&ms->ckey[b][crk], 0), pub);
         }
         // if this block's candidate wins, every block gathers its W1 row next: warm L2 now
         if (has && kb)
           prefetch_l2((const uint8_t*)p.W1 + (size_t)tagged_token(kb) * row_bytes, (uint32_t)row_bytes);
+      }
+      if (C > 1 && crk == 0) {
+        // leader: once every block of the cluster has written, merge the C results in a fixed
+        // order (largest key; (max, sum-exp) by a butterfly) and publish the cluster's slot
+        unsigned long long kc = 0ull;
+        {
+          bool seen = lane >= C;
+          unsigned long long t0 = 0;
+          for (;;) {  // bounded: until every slot carries step ks's tag
+            if (!seen) {
+              kc = ld_acquire_cluster_u64(&ms->ckey[b][lane]);
+              seen = ((kc >> 24) & 0xFF) == (unsigned long long)(ks + 1);
+            }
+            if (__all_sync(0xffffffffu, seen)) break;
+            if (t0 == 0) t0 = globaltimer();
+            else if (globaltimer() - t0 > kWaitLimitNs) {
+              ok = false;
+              break;
+            }
+          }
+        }
+        if (ok) {
+#pragma unroll
+          for (int w = 16; w > 0; w >>= 1) {
+            const unsigned long long q = __shfl_xor_sync(0xffffffffu, kc, w);
+            kc = q > kc ? q : kc;
+          }
+          if (!tgt && lane == 0) st_relaxed64(&p.keys[o], kc);
+          float2 a = lane < C ? ms->cml[b][lane] : make_float2(-INFINITY, 0.f);
+          float2 t = tgt && lane < C ? ms->cmlt[b][lane] : make_float2(-INFINITY, 0.f);
+#pragma unroll
+          for (int w = 16; w > 0; w >>= 1) {
+            lse_merge(a.x, a.y, __shfl_xor_sync(0xffffffffu, a.x, w), __shfl_xor_sync(0xffffffffu, a.y, w));
+            if (tgt)
+              lse_merge(t.x, t.y, __shfl_xor_sync(0xffffffffu, t.x, w),
+                        __shfl_xor_sync(0xffffffffu, t.y, w));
+          }
+          if (lane == 0) {
+            p.ml[o] = a;
+            if (tgt) {
+              p.mlt[o] = t;
+              st_release64(&p.keys[o], kc);
+            }
+          }
+        }
       }
     }
 
@@ -1206,11 +1270,10 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
       if (lane == 0) p.hdot[(size_t)(B + cta) * G + ks] = acc;  // embedding half
     }
     if (conf && ks == 0 && G > 1) hidden_dots<WT, kCThreads>(p, ms, tid, cta, nCTA);
-    bool ok = true;
-    if (warp < B) {
+    if (warp < B && ok) {
       const int b = warp;
       unsigned long long best = 0;
-      ok = poll_keys(p.keys + ((size_t)ks * B + b) * nCTA, nCTA, ks, lane, tgt, &best,
+      ok = poll_keys(p.keys + ((size_t)ks * B + b) * nCL, nCL, ks, lane, tgt, &best,
                      p.test_stuck == 1, p.test_stuck == 1 ? p.test_wait_ns : kWaitLimitNs);
       if (lane == 0 && ok) {
         const bool was_valid = ms->valid[b];
@@ -1231,8 +1294,8 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
     if (tgt) {
       // Eq 8 second pass over the slice: needs the global normalisers of p^d and p^t
       if (warp < B) {
-        const float2 a = warp_merge_ml(p.ml + ((size_t)ks * B + warp) * nCTA, nCTA, lane);
-        const float2 t = warp_merge_ml(p.mlt + ((size_t)ks * B + warp) * nCTA, nCTA, lane);
+        const float2 a = warp_merge_ml(p.ml + ((size_t)ks * B + warp) * nCL, nCL, lane);
+        const float2 t = warp_merge_ml(p.mlt + ((size_t)ks * B + warp) * nCL, nCL, lane);
         if (lane == 0) {
           ms->Ld[warp] = a.x + logf(a.y);
           ms->Lt[warp] = t.x + logf(t.y);
@@ -1277,6 +1340,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
     // unwind: stop the producer (it drains its own copies), record the timeout
     ms->abort = 1;
     if (tid == 0) atomicMax(&hdr->status, kErrTimeout);
+    if (C > 1) cluster_sync_all();
     return;
   }
 
@@ -1289,7 +1353,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
     const int b = cta;
     for (int k = warp; k < G; k += kCWarps) {
       const bool vb = p.tokens[(size_t)b * G + k] >= 0;
-      const float2 ml = warp_merge_ml(p.ml + ((size_t)k * B + b) * nCTA, nCTA, lane);
+      const float2 ml = warp_merge_ml(p.ml + ((size_t)k * B + b) * nCL, nCL, lane);
       if (lane == 0) p.lse[(size_t)b * G + k] = vb ? ml.x + logf(ml.y) : NAN;
       if (k + 1 < G) {
         const float s = warp_sum_strided(p.l1p + ((size_t)k * B + b) * nCTA, nCTA, lane);
@@ -1340,7 +1404,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
     if (!tgt)
       for (int i = warp; i < B * G; i += kCWarps) {
         const int b = i / G, k = i - b * G;
-        const float2 ml = warp_merge_ml(p.ml + ((size_t)k * B + b) * nCTA, nCTA, lane);
+        const float2 ml = warp_merge_ml(p.ml + ((size_t)k * B + b) * nCL, nCL, lane);
         if (lane == 0) p.lse[i] = vtok[i] >= 0 ? ml.x + logf(ml.y) : NAN;
       }
     if (tgt && warp < B) {
@@ -1353,7 +1417,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
         p.cstar[o] = vb ? fminf(1.f, fmaxf(0.f, 1.f - 0.5f * s)) : NAN;
       }
     }
-    for (int i = tid; i < G * B * nCTA; i += kCThreads) p.keys[i] = 0ull;
+    for (int i = tid; i < G * B * nCL; i += kCThreads) p.keys[i] = 0ull;
     if (RNN)
       for (int i = tid; i < G * B; i += kCThreads) p.rnn_flag[i] = 0u;
     csync<kCThreads>();
@@ -1362,6 +1426,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
       __threadfence();
     }
   }
+  if (C > 1) cluster_sync_all();
 }
 
 template <typename WT, int NB, int NCV, bool TCV>
@@ -1376,8 +1441,28 @@ cudaError_t launch_k(DraftParams& p, const CUtensorMap& tm, int nblocks, cudaStr
                                        (int)p.smem_bytes);
   if (e != cudaSuccess) return e;
   void* args[] = {(void*)&p, (void*)&tm};
-  return cudaLaunchCooperativeKernel((const void*)kern, dim3(nblocks), dim3(kThreads), args,
-                                     p.smem_bytes, stream);
+  if (p.cl <= 1)
+    return cudaLaunchCooperativeKernel((const void*)kern, dim3(nblocks), dim3(kThreads), args,
+                                       p.smem_bytes, stream);
+  // cooperative (every block resident at once: the per-step merge waits on all of them) and in
+  // clusters of p.cl consecutive blocks
+  if (nblocks % p.cl != 0) return cudaErrorInvalidValue;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeCooperative;
+  at[0].val.cooperative = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = (unsigned)p.cl;
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(nblocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = p.smem_bytes;
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelExC(&cfg, (const void*)kern, args);
 }
 
 template <typename WT, int NB, int NCV>

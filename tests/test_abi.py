@@ -75,6 +75,11 @@ def test_path_override(lib, monkeypatch):
     assert lib.dspark_draft_path(0, 4, 151936, 256, 1) == 2
 
 
+def test_cluster_query_without_device(lib):
+    # the query needs a device for the SM layout: negative here, and for rejected arguments
+    assert lib.dspark_draft_cluster(0, 1, 151936, 250, 1) < 0
+
+
 def test_path_selection(lib, monkeypatch):
     monkeypatch.delenv("DSPARK_DRAFT_PATH", raising=False)
     from semi_autoregressive_drafting_gb300 import _lib
