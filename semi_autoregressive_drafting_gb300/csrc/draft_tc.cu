@@ -850,46 +850,93 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
-  // Eq 8 of step kp over this block's slice, once every block has published step kp: the global
-  // normalisers of p^d and p^t, then the slice's sum of |p^d - p^t| for each request (y2 from
-  // the workspace, the target re-read; eight 16-byte loads of each in flight per lane)
+  // Eq 8 of step kp over this block's slice, once every block has published step kp.
+  // (1) The global normalisers of p^d and p^t of each request of a chunk: eight threads per
+  //     request merge the slices' partials in a fixed order, every load of a batch in flight at
+  //     once, then three shuffles; the results go to shared memory (the merge scratch, idle
+  //     until the tiles end).
+  // (2) One warp per request: the slice's sum of |p^d - p^t| from y2 (the workspace, still in
+  //     L2 from the first pass) and the target (prefetched into L2 when the block published
+  //     step kp), eight 16-byte loads of each in flight per lane.
   auto second_pass = [&](int kp) {
-    for (int i = ew; i < nck * kM; i += kEpiWarps) {  // the requests of this block's chunks
-      const int b = (grp + (i / kM) * ngrp) * kM + i % kM;
-      if (b >= B) continue;  // (the same for every lane of the warp)
-      const float2 a = merge_ml(p.ml + ((size_t)kp * B + b) * nCTA, nslice, lane);
-      const float2 tt = merge_ml(p.mlt + ((size_t)kp * B + b) * ntp, ntp, lane);
-      const float Ld2 = (a.x + logf(a.y)) * kLog2e, Lt2 = (tt.x + logf(tt.y)) * kLog2e;
-      const float* yr = ybp + (size_t)b * V;
-      const float* tr = tgp + ((size_t)b * G + kp) * V;
-      float acc = 0.f;
-      int vt = sl0;  // first entry left for the scalar tail
-      if (vec_t) {   // sl0 is a multiple of 128
-        const int n4 = (sl1 - sl0) >> 2;
-        const float4* y4 = (const float4*)(yr + sl0);
-        const float4* t4 = (const float4*)(tr + sl0);
-        for (int i0 = 0; i0 < n4; i0 += 256) {
-          float4 yv[8], tq[8];
+    float2* const LdLt = (float2*)scratch;  // [kM]: (Ld2, Lt2) of the requests of one chunk
+    for (int ci2 = 0; ci2 < nck; ++ci2) {
+      const int cb = (grp + ci2 * ngrp) * kM;  // the chunk's first request
+      const int nr = min(kM, B - cb);
+      for (int r0 = 0; r0 < nr; r0 += kEpiThreads / 8) {
+        const int i = r0 + et / 8, sub = et & 7;
+        float M = -INFINITY, L = 0.f, Mt = -INFINITY, Lt = 0.f;
+        if (i < nr) {
+          // up to 20 slices and 2 target chunks per thread in one round of loads (152 slices
+          // and 16 chunks at most on GB300); more take further rounds
+          const float2* pd = p.ml + ((size_t)kp * B + cb + i) * nCTA;
+          const float2* pt = p.mlt + ((size_t)kp * B + cb + i) * ntp;
+          for (int j0 = sub, t0 = sub; j0 < nslice || t0 < ntp; j0 += 160, t0 += 16) {
+            float2 q[20], qt[2];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int i = i0 + lane + 32 * j;
-            yv[j] = i < n4 ? __ldcs(y4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-            tq[j] = i < n4 ? __ldcs(t4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < 20; ++j)
+              q[j] = j0 + 8 * j < nslice ? pd[j0 + 8 * j] : make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              qt[j] = t0 + 8 * j < ntp ? pt[t0 + 8 * j] : make_float2(-INFINITY, 0.f);
+            float mb = M;
+#pragma unroll
+            for (int j = 0; j < 20; ++j) mb = fmaxf(mb, q[j].x);
+            if (mb > -INFINITY) {
+              float sum = L * __expf(M - mb);
+#pragma unroll
+              for (int j = 0; j < 20; ++j) sum += q[j].y * __expf(q[j].x - mb);
+              M = mb;
+              L = sum;
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) lse_merge(Mt, Lt, qt[j].x, qt[j].y);
           }
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (i0 + lane + 32 * j < n4)
-              acc += fabsf(ex2f(yv[j].x - Ld2) - ex2f(tq[j].x * s2 - Lt2)) +
-                     fabsf(ex2f(yv[j].y - Ld2) - ex2f(tq[j].y * s2 - Lt2)) +
-                     fabsf(ex2f(yv[j].z - Ld2) - ex2f(tq[j].z * s2 - Lt2)) +
-                     fabsf(ex2f(yv[j].w - Ld2) - ex2f(tq[j].w * s2 - Lt2));
         }
-        vt = sl0 + 4 * n4;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {  // the request's eight threads are adjacent lanes
+          lse_merge(M, L, __shfl_xor_sync(0xffffffffu, M, o), __shfl_xor_sync(0xffffffffu, L, o));
+          lse_merge(Mt, Lt, __shfl_xor_sync(0xffffffffu, Mt, o), __shfl_xor_sync(0xffffffffu, Lt, o));
+        }
+        if (i < nr && sub == 0)
+          LdLt[i] = make_float2((M + logf(L)) * kLog2e, (Mt + logf(Lt)) * kLog2e);
       }
-      for (int v = vt + lane; v < sl1; v += 32)
-        acc += fabsf(ex2f(yr[v] - Ld2) - ex2f(tr[v] * s2 - Lt2));
-      acc = warp_sum(acc);
-      if (lane == 0) p.l1p[((size_t)kp * B + b) * nCTA + slc] = acc;
+      esync<kEpiThreads>();
+      for (int i = ew; i < nr; i += kEpiWarps) {
+        const int b = cb + i;
+        const float Ld2 = LdLt[i].x, Lt2 = LdLt[i].y;
+        const float* yr = ybp + (size_t)b * V;
+        const float* tr = tgp + ((size_t)b * G + kp) * V;
+        float acc = 0.f;
+        int vt = sl0;  // first entry left for the scalar tail
+        if (vec_t) {   // sl0 is a multiple of 128
+          const int n4 = (sl1 - sl0) >> 2;
+          const float4* y4 = (const float4*)(yr + sl0);
+          const float4* t4 = (const float4*)(tr + sl0);
+          for (int i0 = 0; i0 < n4; i0 += 256) {
+            float4 yv[8], tq[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int q = i0 + lane + 32 * j;
+              yv[j] = q < n4 ? __ldcs(y4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+              tq[j] = q < n4 ? __ldcs(t4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (i0 + lane + 32 * j < n4)
+                acc += fabsf(ex2f(yv[j].x - Ld2) - ex2f(tq[j].x * s2 - Lt2)) +
+                       fabsf(ex2f(yv[j].y - Ld2) - ex2f(tq[j].y * s2 - Lt2)) +
+                       fabsf(ex2f(yv[j].z - Ld2) - ex2f(tq[j].z * s2 - Lt2)) +
+                       fabsf(ex2f(yv[j].w - Ld2) - ex2f(tq[j].w * s2 - Lt2));
+          }
+          vt = sl0 + 4 * n4;
+        }
+        for (int v = vt + lane; v < sl1; v += 32)
+          acc += fabsf(ex2f(yr[v] - Ld2) - ex2f(tr[v] * s2 - Lt2));
+        acc = warp_sum(acc);
+        if (lane == 0) p.l1p[((size_t)kp * B + b) * nCTA + slc] = acc;
+      }
+      esync<kEpiThreads>();  // LdLt is rewritten for the next chunk
     }
   };
 
@@ -1080,6 +1127,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         cond_token(p, b, ks, &valid);
         if (valid && ntile > 0 && sl1 > sl0) atomicMax(&p.keys[(size_t)ks * B + b], make_key(st.best, st.tok));
         p.ml[((size_t)ks * B + b) * nCTA + slc] = make_float2(st.m, st.l);
+        // the Eq 8 pass of this step reads this row of the target after the barrier: start
+        // fetching the slice into L2 now (16-byte aligned rows; the bytes after the last whole
+        // 16 come by plain loads)
+        if (TGT && vec_t && sl1 > sl0) {
+          const uint32_t bytes = (uint32_t)((sl1 - sl0) * 4) & ~15u;
+          if (bytes) prefetch_l2(tgp + ((size_t)b * G + ks) * V + sl0, bytes);
+        }
       }
       esync<kEpiThreads>();
     }
