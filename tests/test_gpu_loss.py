@@ -2,7 +2,8 @@
 fp64 oracle: losses, their three parts and the confidence gradient within 2e-3 absolute; the
 logit gradient within 2e-3 element-wise and within 1e-4 in relative norm.  Cases cover aligned
 and unaligned vocabularies, a temperature, several chunks per row, an invalid label, the
-loss-only call and the full B = 64, gamma = 7, V = 151936 shape."""
+loss-only call, many rows of a large vocabulary, repeated calls on one workspace, and the full
+B = 64, gamma = 7, V = 151936 shape."""
 import numpy as np
 import pytest
 import torch
@@ -50,6 +51,24 @@ def run(B, G, V, seed, T=1.0, alpha=(0.1, 0.9, 1.0), want_grads=True, lab_fix=No
 @pytest.mark.parametrize("B,G,V", [(4, 7, 5000), (3, 3, 1001), (2, 16, 40000), (9, 1, 2)])
 def test_loss_matches_oracle(B, G, V):
     run(B, G, V, seed=400 + V)
+
+
+def test_loss_many_rows_large_vocabulary():
+    run(24, 2, 262144, seed=405)
+    run(24, 2, 262144, seed=406, want_grads=False)
+
+
+def test_loss_repeat_calls_identical():
+    # the same inputs on one workspace give bit-identical outputs (fixed reduction orders)
+    B, G, V = 8, 7, 30000
+    zd, zt, lab, cf = [x.cuda() for x in make(B, G, V, seed=407)]
+    ws = ds.LossWorkspace(B, G, V)
+    outs = [ds.draft_loss(zd, zt, lab, cf, workspace=ws) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    for o in outs[1:]:
+        for a, b in zip(o, outs[0]):
+            assert torch.equal(a, b)
 
 
 def test_loss_temperature_and_weights():
