@@ -1125,7 +1125,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bool valid = false;
         cond_token(p, b, ks, &valid);
-        if (valid && ntile > 0 && sl1 > sl0) atomicMax(&p.keys[(size_t)ks * B + b], make_key(st.best, st.tok));
+        if (valid && ntile > 0 && sl1 > sl0) {
+          atomicMax(&p.keys[(size_t)ks * B + b], make_key(st.best, st.tok));
+          // if this candidate wins, every block gathers its W1 row next step: warm L2 now
+          if (!p.forced && st.tok < (uint32_t)V && ks + 1 < G)
+            prefetch_l2((const __nv_bfloat16*)p.W1 + (size_t)st.tok * r, (uint32_t)(r * 2));
+        }
         p.ml[((size_t)ks * B + b) * nCTA + slc] = make_float2(st.m, st.l);
         // the Eq 8 pass of this step reads this row of the target after the barrier: start
         // fetching the slice into L2 now (16-byte aligned rows; the bytes after the last whole
