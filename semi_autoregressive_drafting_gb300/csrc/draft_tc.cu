@@ -856,8 +856,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   //     once, then three shuffles; the results go to shared memory (the merge scratch, idle
   //     until the tiles end).
   // (2) One warp per request: the slice's sum of |p^d - p^t| from y2 (the workspace, still in
-  //     L2 from the first pass) and the target (prefetched into L2 when the block published
-  //     step kp), eight 16-byte loads of each in flight per lane.
+  //     L2 from the first pass) and the target, eight 16-byte loads of each in flight per lane.
+  //     (Prefetching the target slice into L2 when the block publishes a step, or the
+  //     candidates' W1 rows, measured slower: both evict data the step reads again.)
   auto second_pass = [&](int kp) {
     float2* const LdLt = (float2*)scratch;  // [kM]: (Ld2, Lt2) of the requests of one chunk
     for (int ci2 = 0; ci2 < nck; ++ci2) {
@@ -1125,20 +1126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bool valid = false;
         cond_token(p, b, ks, &valid);
-        if (valid && ntile > 0 && sl1 > sl0) {
-          atomicMax(&p.keys[(size_t)ks * B + b], make_key(st.best, st.tok));
-          // if this candidate wins, every block gathers its W1 row next step: warm L2 now
-          if (!p.forced && st.tok < (uint32_t)V && ks + 1 < G)
-            prefetch_l2((const __nv_bfloat16*)p.W1 + (size_t)st.tok * r, (uint32_t)(r * 2));
-        }
+        if (valid && ntile > 0 && sl1 > sl0) atomicMax(&p.keys[(size_t)ks * B + b], make_key(st.best, st.tok));
         p.ml[((size_t)ks * B + b) * nCTA + slc] = make_float2(st.m, st.l);
-        // the Eq 8 pass of this step reads this row of the target after the barrier: start
-        // fetching the slice into L2 now (16-byte aligned rows; the bytes after the last whole
-        // 16 come by plain loads)
-        if (TGT && vec_t && sl1 > sl0) {
-          const uint32_t bytes = (uint32_t)((sl1 - sl0) * 4) & ~15u;
-          if (bytes) prefetch_l2(tgp + ((size_t)b * G + ks) * V + sl0, bytes);
-        }
       }
       esync<kEpiThreads>();
     }
