@@ -220,8 +220,14 @@ __global__ void __launch_bounds__(kThr) verify_decide_kernel(
 // is the warp's running best.
 __device__ __forceinline__ float gumbel_l2(uint32_t bits) { return -log2f(-logf(uni(bits))); }
 
+// Philox round keys of the seed (rk0[i] = lo + i 0x9E3779B9, rk1[i] = hi + i 0xBB67AE85), passed
+// as a kernel parameter so that the per-call rounds read them from the constant bank
+struct RoundKeys {
+  uint32_t rk0[10], rk1[10];
+};
+
 __global__ void __launch_bounds__(kThr) verify_draw_kernel(
-    int B, int G, int V, float s2, uint32_t seed_lo, uint32_t seed_hi,
+    int B, int G, int V, float s2, uint32_t seed_lo, uint32_t seed_hi, const RoundKeys rk,
     const float* __restrict__ zd, const float* __restrict__ zt, VerifyWs ws, int nchunk,
     int32_t* __restrict__ n_acc, int32_t* __restrict__ out) {
   __shared__ unsigned long long kred[kThr / 32];
@@ -236,6 +242,9 @@ __global__ void __launch_bounds__(kThr) verify_draw_kernel(
   const float* tr = zt + ((size_t)b * (G + 1) + n) * V;
   const int v0 = ch * kDrawChunk, v1 = min(V, v0 + kDrawChunk);
   const bool vec = (V & 3) == 0;  // rows 16-byte aligned
+  // counter words 1-3 (position, request, stream tag) are fixed for the row: the rounds' parts
+  // that do not depend on word 0 (the vocabulary quad) are formed once
+  const PhiloxFixed pfx = philox_fix((uint32_t)n, (uint32_t)b, kResidualTag, seed_lo, seed_hi);
   float best = -INFINITY, tb = -INFINITY;
   uint32_t tok = 0xFFFFFFFFu;
   // four consecutive entries per thread and iteration: one Philox call, one 16-byte load of each
@@ -258,7 +267,7 @@ __global__ void __launch_bounds__(kThr) verify_draw_kernel(
           yq4[e] = (resid && v4 + e < v1) ? yr[v4 + e] : 0.f;
         }
       }
-      const U4 r = philox4x32_10((uint32_t)(v4 >> 2), (uint32_t)n, (uint32_t)b, kResidualTag, seed_lo, seed_hi);
+      const U4 r = philox_var((uint32_t)(v4 >> 2), pfx, rk.rk0, rk.rk1);
       const uint32_t wd[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -373,8 +382,14 @@ cudaError_t launch_verify(int B, int G, int V, float T, uint64_t seed, const flo
       B, G, V, s2, lo, hi, zd, zt, tok, ws, nchunk, n_acc, out);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  verify_draw_kernel<<<(unsigned)((long long)B * ndraw), kThr, 0, stream>>>(B, G, V, s2, lo, hi, zd, zt,
-                                                                           ws, ndraw, n_acc, out);
+  RoundKeys rk;
+  for (int i = 0; i < 10; ++i) {
+    rk.rk0[i] = lo + (uint32_t)i * 0x9E3779B9u;
+    rk.rk1[i] = hi + (uint32_t)i * 0xBB67AE85u;
+  }
+  verify_draw_kernel<<<(unsigned)((long long)B * ndraw), kThr, 0, stream>>>(B, G, V, s2, lo, hi, rk,
+                                                                           zd, zt, ws, ndraw, n_acc,
+                                                                           out);
   return cudaGetLastError();
 }
 
