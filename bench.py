@@ -40,13 +40,14 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: every timed block starts with a cold
 # source file, the sha256 prefix of the source it was measured on, and the bytes.  A workload
 # without a capture, or whose kernel changed since, reports null.
 TRAFFIC = {
-    "qwen3_4b_markov": ("draft_cc.cu", "a654b711be85aa4d", 83114240),          # 80.62 + 2.49 MB
-    "high_concurrency_sched": ("draft_tc.cu", "1a5777e647e31320", 2411718656),  # 2407 + 4.2 MB
+    "qwen3_4b_markov": ("draft_cc.cu", "868f81d434458dba", 81894912),           # 80.62 + 1.27 MB
+    "tiny_markov": ("draft_cc.cu", "868f81d434458dba", 2330368),                # 2.33 + 0 MB
+    "high_concurrency_sched": ("draft_tc.cu", "417929313242095a", 2411431680),  # 2407 + 4.2 MB
     # draft_tc_kernel alone; the target's normalisers (272.4 MB) are a launch before it
-    "qwen3_8b_labels": ("draft_tc.cu", "1a5777e647e31320", 643011584),         # 615.3 + 27.8 MB
-    "rnn_head": ("draft_tc.cu", "1a5777e647e31320", 528793088),                 # 524.0 + 4.8 MB
+    "qwen3_8b_labels": ("draft_tc.cu", "417929313242095a", 628946176),         # 607.4 + 21.5 MB
+    "rnn_head": ("draft_tc.cu", "417929313242095a", 528982016),                 # 524.2 + 4.8 MB
     # the three verify kernels of one call (bench.py --op verify)
-    "verify qwen3_8b_labels": ("verify.cu", "256b8f8a4f1f9538", 659341312),
+    "verify qwen3_8b_labels": ("verify.cu", "c5b18516acacc741", 661831424),
     # the four loss kernels of one call (bench.py --op loss)
     "loss qwen3_8b_labels": ("loss.cu", "49dca217d245abe9", 1871840512),
 }
