@@ -47,6 +47,18 @@ def test_tc_ranks(r, lay):
 
 
 @pytest.mark.parametrize("lay", LAYOUTS)
+@pytest.mark.parametrize("r", [64, 192, 512])
+def test_tc_unpacked_ranks(r, lay):
+    # more than 64 requests: unpacked tiles, one to eight 64-wide K blocks per A slab
+    _run(BASE.with_(B=80, V=12000, r=r, d=64, seed=84 + r // 64), w2_layout=lay)
+
+
+@pytest.mark.parametrize("lay", LAYOUTS)
+def test_tc_unpacked_target_labels(lay):
+    _run(BASE.with_(B=96, V=30000, d=256, T=0.8, seed=92), target_noise=1.0, w2_layout=lay)
+
+
+@pytest.mark.parametrize("lay", LAYOUTS)
 def test_tc_target_labels(lay):
     _run(BASE.with_(B=24, V=30000, d=256, T=0.8, seed=90), target_noise=1.0, w2_layout=lay)
 
