@@ -261,6 +261,27 @@ __device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long l
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// Whole-warp merges of the per-step results, each a short dependency chain: the largest 64-bit
+// key by two warp reductions (the high words; then the low words of the lanes holding that high
+// word), and (max, sum-exp) by one reduction of the maxima, one exponential per lane and a
+// butterfly sum (fixed order, so the result does not depend on timing).
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long k) {
+  const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(k >> 32));
+  const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(k >> 32) == hi ? (uint32_t)k : 0u);
+  return ((unsigned long long)hi << 32) | lo;
+}
+__device__ __forceinline__ float from_orderable(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+__device__ __forceinline__ void warp_lse(float& m, float& l) {
+  const float M = from_orderable(__reduce_max_sync(0xffffffffu, orderable(m)));
+  float s = l != 0.f ? l * __expf(m - M) : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  m = s != 0.f ? M : -INFINITY;
+  l = s;
+}
+
 // Grid barrier and argmax in one: wait (bounded) until every block has published its tagged
 // key for step ks, then return the largest.  One warp; each lane covers every 32nd block.
 // (The failure-path test hook polls for a tag no block writes, with a short limit.)
@@ -281,12 +302,7 @@ __device__ __forceinline__ bool poll_keys(const unsigned long long* keys, int n,
       // with release stores behind the keys, one fence turns the relaxed loads into an
       // acquire of everything those blocks wrote before publishing
       if (acquire) fence_acq_rel_gpu();
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long q = __shfl_xor_sync(0xffffffffu, m, o);
-        m = q > m ? q : m;
-      }
-      *best = m;
+      *best = warp_max_key(m);
       return true;
     }
     if (t0 == 0) t0 = globaltimer();
@@ -1119,16 +1135,10 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         Slot& a = sb[b];
-        unsigned long long key = a.tok != 0xFFFFFFFFu ? tagged_key(a.best, a.tok, ks) : 0ull;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const unsigned long long q = __shfl_xor_sync(0xffffffffu, key, o);
-          key = q > key ? q : key;
-          lse_merge(a.m, a.l, __shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.l, o));
-          if (tgt)
-            lse_merge(a.mt, a.lt, __shfl_xor_sync(0xffffffffu, a.mt, o),
-                      __shfl_xor_sync(0xffffffffu, a.lt, o));
-        }
+        const unsigned long long key =
+            warp_max_key(a.tok != 0xFFFFFFFFu ? tagged_key(a.best, a.tok, ks) : 0ull);
+        warp_lse(a.m, a.l);
+        if (tgt) warp_lse(a.mt, a.lt);
         if (lane == 0) {
           Slot& o = slots[warp * 4 + b];
           o.best = __uint_as_float((uint32_t)(key >> 32));
@@ -1143,8 +1153,13 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
       unsigned long long key = st.tok != 0xFFFFFFFFu ? tagged_key(st.best, st.tok, ks) : 0ull;
       // lanes of the same request: those 4 NB apart hold the owner results; with one request
       // the batched epilogue leaves results on every lane, so all 32 are merged
+      if (NB == 1) {
+        key = warp_max_key(key);
+        warp_lse(st.m, st.l);
+        if (tgt) warp_lse(st.mt, st.lt);
+      }
 #pragma unroll
-      for (int o = NB == 1 ? 1 : 4 * NB; o < 32; o <<= 1) {
+      for (int o = 4 * NB; NB > 1 && o < 32; o <<= 1) {
         const unsigned long long q = __shfl_xor_sync(0xffffffffu, key, o);
         key = q > key ? q : key;
         lse_merge(st.m, st.l, __shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.l, o));
@@ -1173,11 +1188,7 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
         const Slot& q = slots[lane * 4 + b];
         kb = ((unsigned long long)__float_as_uint(q.best) << 32) | q.tok;
       }
-#pragma unroll
-      for (int w = 16; w > 0; w >>= 1) {
-        const unsigned long long q = __shfl_xor_sync(0xffffffffu, kb, w);
-        kb = q > kb ? q : kb;
-      }
+      kb = warp_max_key(kb);
       const unsigned long long pub = has && kb ? kb : tagged_key_empty(ks);
       if (C == 1 && !tgt && lane == 0) st_relaxed64(&p.keys[o], pub);
       float m = -INFINITY, l = 0.f, mt = -INFINITY, lt = 0.f;
@@ -1188,12 +1199,8 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
         mt = q.mt;
         lt = q.lt;
       }
-#pragma unroll
-      for (int w = 16; w > 0; w >>= 1) {
-        lse_merge(m, l, __shfl_xor_sync(0xffffffffu, m, w), __shfl_xor_sync(0xffffffffu, l, w));
-        if (tgt)
-          lse_merge(mt, lt, __shfl_xor_sync(0xffffffffu, mt, w), __shfl_xor_sync(0xffffffffu, lt, w));
-      }
+      warp_lse(m, l);
+      if (tgt) warp_lse(mt, lt);
       if (lane == 0) {
         if (C == 1) {
           p.ml[o] = make_float2(m, l);
@@ -1231,21 +1238,12 @@ __global__ void __launch_bounds__(CW * 32 + 32 + (TCV ? 32 : 0), 1)
           }
         }
         if (ok) {
-#pragma unroll
-          for (int w = 16; w > 0; w >>= 1) {
-            const unsigned long long q = __shfl_xor_sync(0xffffffffu, kc, w);
-            kc = q > kc ? q : kc;
-          }
+          kc = warp_max_key(kc);
           if (!tgt && lane == 0) st_relaxed64(&p.keys[o], kc);
           float2 a = lane < C ? ms->cml[b][lane] : make_float2(-INFINITY, 0.f);
           float2 t = tgt && lane < C ? ms->cmlt[b][lane] : make_float2(-INFINITY, 0.f);
-#pragma unroll
-          for (int w = 16; w > 0; w >>= 1) {
-            lse_merge(a.x, a.y, __shfl_xor_sync(0xffffffffu, a.x, w), __shfl_xor_sync(0xffffffffu, a.y, w));
-            if (tgt)
-              lse_merge(t.x, t.y, __shfl_xor_sync(0xffffffffu, t.x, w),
-                        __shfl_xor_sync(0xffffffffu, t.y, w));
-          }
+          warp_lse(a.x, a.y);
+          if (tgt) warp_lse(t.x, t.y);
           if (lane == 0) {
             p.ml[o] = a;
             if (tgt) {
