@@ -40,8 +40,8 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: every timed block starts with a cold
 # source file, the sha256 prefix of the source it was measured on, and the bytes.  A workload
 # without a capture, or whose kernel changed since, reports null.
 TRAFFIC = {
-    "qwen3_4b_markov": ("draft_cc.cu", "868f81d434458dba", 81894912),           # 80.62 + 1.27 MB
-    "tiny_markov": ("draft_cc.cu", "868f81d434458dba", 2330368),                # 2.33 + 0 MB
+    "qwen3_4b_markov": ("draft_cc.cu", "b7f16e7f9de10484", 81911552),           # 80.61 + 1.30 MB
+    "tiny_markov": ("draft_cc.cu", "b7f16e7f9de10484", 2327552),                # 2.33 + 0 MB
     "high_concurrency_sched": ("draft_tc.cu", "417929313242095a", 2411431680),  # 2407 + 4.2 MB
     # draft_tc_kernel alone; the target's normalisers (272.4 MB) are a launch before it
     "qwen3_8b_labels": ("draft_tc.cu", "417929313242095a", 628946176),         # 607.4 + 21.5 MB
