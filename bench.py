@@ -49,7 +49,7 @@ TRAFFIC = {
     # the three verify kernels of one call (bench.py --op verify)
     "verify qwen3_8b_labels": ("verify.cu", "c5b18516acacc741", 661831424),
     # the four loss kernels of one call (bench.py --op loss)
-    "loss qwen3_8b_labels": ("loss.cu", "49dca217d245abe9", 1871840512),
+    "loss qwen3_8b_labels": ("loss.cu", "4c19b76551491e6e", 1871557376),
 }
 
 

@@ -72,13 +72,21 @@ __host__ __device__ inline size_t lws_layout(int B, int G, int V, size_t* off) {
 struct Chunk {
   float4 d[kLPer], t[kLPer];
 };
+// (last: the rows' last read, streamed evict-first; otherwise the lines stay in L2 normally, so
+// that the next launch, which starts with the rows this one read last, finds some of them)
+template <bool LAST>
 __device__ __forceinline__ void load_chunk(Chunk& c, const float* zd, const float* zt, int n4) {
 #pragma unroll
   for (int u = 0; u < kLPer; ++u) {
     const int i = (int)threadIdx.x + u * kLThr;
     const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    c.d[u] = i < n4 ? __ldcs((const float4*)zd + i) : ninf;
-    c.t[u] = i < n4 ? __ldcs((const float4*)zt + i) : ninf;
+    if (LAST) {
+      c.d[u] = i < n4 ? __ldcs((const float4*)zd + i) : ninf;
+      c.t[u] = i < n4 ? __ldcs((const float4*)zt + i) : ninf;
+    } else {
+      c.d[u] = i < n4 ? __ldcg((const float4*)zd + i) : ninf;
+      c.t[u] = i < n4 ? __ldcg((const float4*)zt + i) : ninf;
+    }
   }
 }
 
@@ -113,7 +121,7 @@ __global__ void __launch_bounds__(kLThr) loss_part_kernel(const float* __restric
   float md = -INFINITY, ld = 0.f, mt = -INFINITY, lt = 0.f;
   if ((V & 3) == 0) {
     Chunk c;
-    load_chunk(c, d + v0, t + v0, (v1 - v0) >> 2);
+    load_chunk<false>(c, d + v0, t + v0, (v1 - v0) >> 2);
     float xd = -INFINITY, xt = -INFINITY;
 #pragma unroll
     for (int u = 0; u < kLPer; ++u) {
@@ -196,11 +204,14 @@ __device__ __forceinline__ float2 row_norms_warp(const float4* part, long long r
 __device__ __forceinline__ float sgn(float x) { return x > 0.f ? 1.f : (x < 0.f ? -1.f : 0.f); }
 
 // ------------------------------------------------------------------ 2. |p - q| and s p sums
+// (the blocks take the chunks in reverse order, so that the first ones read the rows the
+// normaliser launch read last, while they are still in L2; LAST: no gradient launch follows)
+template <bool LAST>
 __global__ void __launch_bounds__(kLThr) loss_stat_kernel(const float* __restrict__ zd,
                                                           const float* __restrict__ zt, int V,
                                                           float s2, int nchunk, LossWs ws) {
   __shared__ float2 red[kLThr / 32];
-  const long long blk = blockIdx.x, row = blk / nchunk;
+  const long long blk = (long long)gridDim.x - 1 - blockIdx.x, row = blk / nchunk;
   const int ch = (int)(blk % nchunk);
   const int v0 = ch * kLChunk, v1 = min(V, v0 + kLChunk);
   const float* d = zd + row * V;
@@ -214,7 +225,7 @@ __global__ void __launch_bounds__(kLThr) loss_stat_kernel(const float* __restric
   };
   if ((V & 3) == 0) {
     Chunk c;
-    load_chunk(c, d + v0, t + v0, (v1 - v0) >> 2);
+    load_chunk<LAST>(c, d + v0, t + v0, (v1 - v0) >> 2);
 #pragma unroll
     for (int u = 0; u < kLPer; ++u) {  // padding entries are -inf: p = q = 0 adds nothing
       acc(c.d[u].x, c.t[u].x);
@@ -241,7 +252,7 @@ __global__ void __launch_bounds__(kLThr, 3) loss_grad_kernel(
   const float* t = zt + row * V;
   const int n4 = (v1 - v0) >> 2;
   Chunk c;
-  if ((V & 3) == 0) load_chunk(c, d + v0, t + v0, n4);  // in flight during the row's totals
+  if ((V & 3) == 0) load_chunk<true>(c, d + v0, t + v0, n4);  // in flight during the totals
   const int lane = (int)(threadIdx.x & 31);
   const int x = lab[row];
   float* g = grad + row * V;
@@ -355,7 +366,10 @@ cudaError_t launch_loss(int B, int G, int V, float T, const float* zd, const flo
   loss_part_kernel<<<(unsigned)(rows * nchunk), kLThr, 0, stream>>>(zd, zt, V, s2, nchunk, ws.part);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  loss_stat_kernel<<<(unsigned)(rows * nchunk), kLThr, 0, stream>>>(zd, zt, V, s2, nchunk, ws);
+  if (grad_z)
+    loss_stat_kernel<false><<<(unsigned)(rows * nchunk), kLThr, 0, stream>>>(zd, zt, V, s2, nchunk, ws);
+  else
+    loss_stat_kernel<true><<<(unsigned)(rows * nchunk), kLThr, 0, stream>>>(zd, zt, V, s2, nchunk, ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (grad_z) {
     loss_grad_kernel<<<(unsigned)(rows * nchunk), kLThr, 0, stream>>>(zd, zt, lab, G, V, s2, 1.f / T,
