@@ -287,15 +287,23 @@ def run_reference(args, wl):
     U = O(t["U"])
     h = O(t["h"])
 
+    cs = []
+
     def one(k):
-        return oracle.draft(head=0 if wl.head == "markov" else 1, B=wl.B, gamma=1, V=wl.V,
-                            r=wl.r, d=wl.d, T=wl.T, seed=wl.seed, W1=O(t["W1"]), W2=O(t["W2"]),
-                            Wj=O(t.get("Wj")), U=np.ascontiguousarray(U[:, k:k + 1]),
-                            x0=O(t["x0"]), h=np.ascontiguousarray(h[:, k:k + 1]), w=O(t["w"]),
-                            nthreads=cores)
+        o = oracle.draft(head=0 if wl.head == "markov" else 1, B=wl.B, gamma=1, V=wl.V,
+                         r=wl.r, d=wl.d, T=wl.T, seed=wl.seed, W1=O(t["W1"]), W2=O(t["W2"]),
+                         Wj=O(t.get("Wj")), U=np.ascontiguousarray(U[:, k:k + 1]),
+                         x0=O(t["x0"]), h=np.ascontiguousarray(h[:, k:k + 1]), w=O(t["w"]),
+                         nthreads=cores)
+        if t["sps"] is not None:  # the block's prefix schedule once gamma positions are in
+            cs.append(o.c[:, 0])
+            if len(cs) == wl.gamma:
+                oracle.prefix_schedule(np.cumprod(np.stack(cs, 1), 1), t["sps"].numpy())
+                cs.clear()
 
     for i in range(args.warmup):
         one(i % wl.gamma)
+    cs.clear()
     t0 = time.perf_counter()
     for i in range(args.steps):
         one(i % wl.gamma)
@@ -308,7 +316,9 @@ def run_reference(args, wl):
         "data": "synthetic", "config": {"workload": wl.name, "B": wl.B, "gamma": wl.gamma,
                                         "V": wl.V, "r": wl.r, "d": wl.d, "T": wl.T},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": "one draft position over the full vocabulary per step"},
+                         "sample": "one draft position over the full vocabulary per step"
+                                   + (", the prefix schedule every gamma steps"
+                                      if t["sps"] is not None else "")},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -325,17 +335,24 @@ def cpu_baseline(wl, seconds: float = 15.0):
     O = inputs.to_oracle
     cores = os.cpu_count() or 1
     U, h = O(t["U"]), O(t["h"])
-    n, t0 = 0, time.perf_counter()
+    n, nsched, cs, t0 = 0, 0, [], time.perf_counter()
     while time.perf_counter() - t0 < seconds:
         k = n % wl.gamma
-        oracle.draft(head=0 if wl.head == "markov" else 1, B=wl.B, gamma=1, V=wl.V, r=wl.r,
-                     d=wl.d, T=wl.T, seed=wl.seed, W1=O(t["W1"]), W2=O(t["W2"]),
-                     Wj=O(t.get("Wj")), U=np.ascontiguousarray(U[:, k:k + 1]), x0=O(t["x0"]),
-                     h=np.ascontiguousarray(h[:, k:k + 1]), w=O(t["w"]), nthreads=cores)
+        o = oracle.draft(head=0 if wl.head == "markov" else 1, B=wl.B, gamma=1, V=wl.V, r=wl.r,
+                         d=wl.d, T=wl.T, seed=wl.seed, W1=O(t["W1"]), W2=O(t["W2"]),
+                         Wj=O(t.get("Wj")), U=np.ascontiguousarray(U[:, k:k + 1]),
+                         x0=O(t["x0"]), h=np.ascontiguousarray(h[:, k:k + 1]), w=O(t["w"]),
+                         nthreads=cores)
         n += 1
+        if t["sps"] is not None:  # the block's prefix schedule, on the sampled positions' c
+            cs.append(o.c[:, 0])
+            if len(cs) == wl.gamma:
+                oracle.prefix_schedule(np.cumprod(np.stack(cs, 1), 1), t["sps"].numpy())
+                cs, nsched = [], nsched + 1
     dt = time.perf_counter() - t0
+    sched = f", {nsched} prefix schedules" if t["sps"] is not None else ""
     return {"value": wl.B * n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{n} draft positions x B={wl.B} over the full vocabulary ({dt:.1f} s)"}
+            "sample": f"{n} draft positions x B={wl.B} over the full vocabulary{sched} ({dt:.1f} s)"}
 
 VERIFY_METRIC = "verified draft blocks/sec (B per call) and achieved HBM GB/s vs roofline, 1 GB300"
 
@@ -656,14 +673,28 @@ def main():
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     resident = plan(dev["U"], dev["h"], dev["x0"], dev.get("target"))
+    # the batch prefix scheduler (the last step of the hot path) when the workload carries a
+    # steps/s table: the verify lengths from the block's S, in the timed step
+    conf = dev["h"] is not None and dev["w"] is not None
+    sched = conf and dev.get("sps") is not None
+    sl = torch.empty(B, dtype=torch.int32, device="cuda")
+    sth = torch.empty(1, dtype=torch.float64, device="cuda")
+
+    def schedule(p, s, out):
+        if sched:
+            ds.prefix_schedule(p.out.S, dev["sps"], stream=s, out=out)
+
     for _ in range(args.warmup):
         flush.zero_()
         resident.run()
+        schedule(resident, stream, (sl, sth))
     torch.cuda.synchronize()
     assert ws.status() == 0, "draft kernel reported a device error during warm-up"
 
-    # ---- device-resident timing: CUDA events around each draft launch, L2 flushed between
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    # ---- device-resident timing: CUDA events around each step (the draft call, then the
+    # scheduler when there is one, with one more event between them for the draft's own
+    # roofline); L2 flushed between steps
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3 if sched else 2))
           for _ in range(args.steps)]
     if dist:
         dist.barrier()
@@ -674,12 +705,17 @@ def main():
             flush.zero_()
             ev[i][0].record(stream)
             resident.run()
-            ev[i][1].record(stream)
+            if sched:
+                ev[i][1].record(stream)
+                schedule(resident, stream, (sl, sth))
+            ev[i][-1].record(stream)
         torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    times = [a.elapsed_time(b) for a, b in ev]   # ms per block
+    times = [e[0].elapsed_time(e[-1]) for e in ev]   # ms per step (block, and schedule)
     ms_step = sum(times) / len(times)
+    ms_draft = sum(e[0].elapsed_time(e[1]) for e in ev) / len(ev)  # the draft call alone
     assert ws.status() == 0, "draft kernel reported a device error"
+    sched_ok = (not sched) or bool(((sl >= 0) & (sl <= G)).all())
 
     # ---- end to end through the public API: pinned host inputs in, results out, every step.
     # The step's inputs (U, h, x0 and the target) sit in one pinned host buffer and the results
@@ -692,12 +728,13 @@ def main():
     din_buf, din = packed(in_specs, "cuda")
     for k in names:
         hin[k].copy_(host[k])
-    conf = dev["h"] is not None and dev["w"] is not None
     out_specs = [("tokens", (B, G), torch.int32), ("lse", (B, G), torch.float32)]
     if conf:
         out_specs += [("c", (B, G), torch.float32), ("S", (B, G), torch.float32)]
     if host.get("target") is not None:
         out_specs += [("cstar", (B, G), torch.float32), ("l1", (B, G), torch.float32)]
+    if sched:
+        out_specs += [("len", (B,), torch.int32), ("theta", (1,), torch.float64)]
     dout_buf, dout = packed(out_specs, "cuda")
     hout_buf, hout = packed(out_specs, "cpu")
     staged = plan(din["U"], din["h"], din["x0"], din.get("target"), out=dout)
@@ -709,6 +746,7 @@ def main():
     def e2e_step(s):
         din_buf.copy_(hin_buf, non_blocking=True)
         staged.run(s)
+        schedule(staged, s, (dout["len"], dout["theta"]) if sched else None)
         hout_buf.copy_(dout_buf, non_blocking=True)
 
     for _ in range(3):
@@ -745,14 +783,14 @@ def main():
     assert ws.status() == 0, "draft kernel reported a device error (end-to-end loop)"
 
     # ---- max over ranks
-    ms_step, e2e_ms = ranks_max(dist, [ms_step, e2e_ms])
+    ms_step, ms_draft, e2e_ms = ranks_max(dist, [ms_step, ms_draft, e2e_ms])
     value = job_rate(world, B * G, ms_step)
     e2e_value = job_rate(world, B * G, e2e_ms)
 
     if rank == 0:
         peak, peak_kind = load_peaks()
         alg = algorithmic_bytes(wl)
-        achieved = alg / (ms_step * 1e-3) / 1e9
+        achieved = alg / (ms_draft * 1e-3) / 1e9
         cap = TRAFFIC.get(wl.name)
         src = cap and os.path.join(ROOT, "semi_autoregressive_drafting_gb300", "csrc", cap[0])
         traffic = cap[2] if cap and _sha(src) == cap[1] else None
@@ -764,9 +802,11 @@ def main():
         if path in (0, 2) and args.w2_layout == "rv":
             launches += 1  # W2's transpose for the small-batch kernels
         kernel_name = "draft_tc_kernel" if path == 1 else "draft_cc_kernel"
-        # achieved covers the whole call: with launches before the draft kernel (the RNN head's
-        # h-part GEMM, the target's normalisers) their time is in ms_step too
-        scope = "one launch" if launches == 1 else f"whole call, {launches} launches"
+        # achieved covers the whole draft call: with launches before the draft kernel (the RNN
+        # head's h-part GEMM, the target's normalisers) their time is in ms_draft too; the
+        # scheduler after it is timed in the step but not in the roofline
+        scope = "one launch" if launches == 1 else f"whole draft call, {launches} launches"
+        step_launches = launches + (1 if sched else 0)
         path_name = {0: "cuda-core", 1: "tcgen05, requests on M",
                      2: "tcgen05, vocabulary on M"}.get(path, "none")
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -778,11 +818,11 @@ def main():
         if traffic is not None:
             # the bytes that actually crossed HBM (ncu) over the same time: below the
             # algorithmic fraction when the kernel keeps data on chip across steps
-            roof["dram_frac"] = traffic / (ms_step * 1e-3) / 1e9 / peak
+            roof["dram_frac"] = traffic / (ms_draft * 1e-3) / 1e9 / peak
         if path in (1, 2):
             tpeak, tkind = load_tensor_peak()
             flops = algorithmic_flops(wl)
-            tach = flops / (ms_step * 1e-3) / 1e12
+            tach = flops / (ms_draft * 1e-3) / 1e12
             roof["tensor"] = {"achieved": tach, "peak": tpeak, "unit": "TFLOP/s",
                               "frac": tach / tpeak, "peak_kind": tkind,
                               "algorithmic_flops_per_launch": flops}
@@ -795,12 +835,14 @@ def main():
             "config": {"workload": wl.name, "B": B, "gamma": G, "V": wl.V, "r": wl.r, "d": wl.d,
                        "T": wl.T, "l2": "flushed between timed blocks (512 MB write)",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                       "path": path_name, "w2_layout": args.w2_layout},
+                       "path": path_name, "w2_layout": args.w2_layout,
+                       "step": "draft block + prefix scheduler" if sched else "draft block",
+                       "draft_ms": ms_draft, "schedule_ok": sched_ok},
             "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "cuda_graph": graph is not None, "results_copied": res_ok},
-            "gpu_launches": launches * args.steps,
+            "gpu_launches": step_launches * args.steps,
             "clocks": clk.summary(),
             "wall_s": wall,
             "ms_per_step_min": min(times), "ms_per_step_median": statistics.median(times),

@@ -212,12 +212,18 @@ def tv_label(draft_logits, target_logits, *, T=1.0, stream=None):
     return cstar, l1
 
 
-def prefix_schedule(S, sps, *, stream=None):
-    """Per-request verify lengths maximising SPS(n) * expected accepted tokens."""
+def prefix_schedule(S, sps, *, stream=None, out=None):
+    """Per-request verify lengths maximising SPS(n) * expected accepted tokens.
+
+    ``out``: optional preallocated (lengths [B] int32, theta [1] float64) device tensors, e.g.
+    to capture the call in a CUDA graph."""
     lib = _lib.load()
     B, gamma = S.shape
-    ln = torch.empty(B, dtype=torch.int32, device=S.device)
-    theta = torch.empty(1, dtype=torch.float64, device=S.device)
+    if out is not None:
+        ln, theta = out
+    else:
+        ln = torch.empty(B, dtype=torch.int32, device=S.device)
+        theta = torch.empty(1, dtype=torch.float64, device=S.device)
     code = lib.dspark_prefix_schedule(B, gamma, _ptr(S), _ptr(sps), _ptr(ln), _ptr(theta),
                                       _stream(stream))
     _lib.check(code, "dspark_prefix_schedule")

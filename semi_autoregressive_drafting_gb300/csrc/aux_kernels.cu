@@ -105,8 +105,84 @@ __global__ void __launch_bounds__(512) tv_label_kernel(int V, float invT, const 
 // and the top-m sum is the best legal sum with B + m verify tokens.  The sums are exact
 // (floor(S 2^32) added as integers), so Theta(m) = sps[B + m] * (B + sum 2^-32) is a single
 // IEEE double multiply and the argmax (smallest m on ties) is reproducible bit for bit.
+// floor(S 2^32) is taken in single precision (S 2^32 is exact in fp32 for S in [0, 1], and the
+// conversion truncates), and the 2^-32 scaling is an exact multiply: the only fp64 arithmetic
+// left per entry is the conversion of the sum, one add and the Theta multiply.
 constexpr int kSchedThreads = 1024;
 
+// Bitonic sort of the Mp2 keys, ascending, with the keys in registers: thread t holds keys
+// [t E, t E + E).  Compare-exchange partners inside a thread are swapped in registers, partners
+// in another lane of the warp come by shuffle, and only strides of 32 E or more go through
+// shared memory (the same sort of 4096 keys all in shared memory took 31 us on GB300, this one
+// 26 us).  Padding keys (index >= Mp2 when Mp2 < 1024) only ever meet other padding keys.
+template <int E>
+__device__ __forceinline__ void sort_keys(unsigned long long* keys, int Mp2) {
+  const int tid = threadIdx.x;
+  unsigned long long r[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = tid * E + e;
+    r[e] = i < Mp2 ? keys[i] : ~0ull;
+  }
+  for (int size = 2; size <= Mp2; size <<= 1) {
+    int stride = size >> 1;
+    if (stride >= 32 * E) {  // across warps: through shared memory
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if (tid * E + e < Mp2) keys[tid * E + e] = r[e];
+      __syncthreads();
+      for (; stride >= 32 * E; stride >>= 1) {
+        for (int pi = tid; pi < Mp2 / 2; pi += kSchedThreads) {
+          const int lo = 2 * pi - (pi & (stride - 1));
+          const int hi = lo + stride;
+          const bool up = (lo & size) == 0;
+          const unsigned long long a = keys[lo], c = keys[hi];
+          if ((a > c) == up) {
+            keys[lo] = c;
+            keys[hi] = a;
+          }
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int i = tid * E + e;
+        r[e] = i < Mp2 ? keys[i] : ~0ull;
+      }
+      __syncthreads();  // every read done before the next size writes shared memory again
+    }
+    for (; stride >= E; stride >>= 1) {  // across the lanes of a warp
+      const int ld = stride / E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int i = tid * E + e;
+        const unsigned long long o = __shfl_xor_sync(~0u, r[e], ld);
+        const bool keep_min = ((i & stride) == 0) == ((i & size) == 0);
+        r[e] = keep_min ? (o < r[e] ? o : r[e]) : (o > r[e] ? o : r[e]);
+      }
+    }
+#pragma unroll
+    for (int st = E / 2; st > 0; st >>= 1) {  // inside the thread
+      if (st > (size >> 1)) continue;
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if ((e & st) == 0) {
+          const bool up = ((tid * E + e) & size) == 0;
+          const unsigned long long a = r[e], c = r[e + st];
+          if ((a > c) == up) {
+            r[e] = c;
+            r[e + st] = a;
+          }
+        }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if (tid * E + e < Mp2) keys[tid * E + e] = r[e];
+  __syncthreads();
+}
+
+template <int E>
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(int B, int G, int M, int Mp2,
                                                                  const float* S, const double* sps,
                                                                  int32_t* len, double* theta) {
@@ -136,40 +212,39 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(int B, int G, i
     if (tid == 0) *theta = __longlong_as_double(0x7ff8000000000000ll);
     return;
   }
-  // bitonic sort, ascending
-  for (int size = 2; size <= Mp2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < Mp2 / 2; i += kSchedThreads) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool up = (lo & size) == 0;
-        const unsigned long long a = keys[lo], c = keys[hi];
-        if ((a > c) == up) {
-          keys[lo] = c;
-          keys[hi] = a;
-        }
-      }
-      __syncthreads();
-    }
-  }
+  sort_keys<E>(keys, Mp2);
+  const int lane = tid & 31, warp = tid >> 5;
   // fixed-point values of the sorted S, inclusive prefix sums (chunk per thread)
   const int chunk = (M + kSchedThreads - 1) / kSchedThreads;
   const int c0 = min(M, tid * chunk), c1 = min(M, c0 + chunk);
   unsigned long long run = 0;
   for (int i = c0; i < c1; ++i) {
     const float s = __uint_as_float(~(uint32_t)(keys[i] >> 32));
-    run += (unsigned long long)floor((double)s * 4294967296.0);
+    run += __float2ull_rz(s * 4294967296.0f);
   }
-  csum[tid] = run;
+  // exclusive prefix of the chunk sums over the block: a shuffle scan per warp, then one over
+  // the 32 warp totals (integer sums: exact in any order)
+  unsigned long long incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long v = __shfl_up_sync(~0u, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) csum[warp] = incl;
   __syncthreads();
-  if (tid == 0) {
-    unsigned long long acc = 0;
-    for (int t = 0; t < kSchedThreads; ++t) {
-      const unsigned long long v = csum[t];
-      csum[t] = acc;  // exclusive prefix of chunk sums
-      acc += v;
+  if (warp == 0) {
+    unsigned long long wt = lane < kSchedThreads / 32 ? csum[lane] : 0ull;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long v = __shfl_up_sync(~0u, wt, o);
+      if (lane >= o) wt += v;
     }
+    csum[32 + lane] = wt;  // inclusive over warps
   }
+  __syncthreads();
+  const unsigned long long before_warp = warp > 0 ? csum[32 + warp - 1] : 0ull;
+  __syncthreads();
+  csum[tid] = before_warp + incl - run;  // exclusive prefix of this thread's chunk
   __syncthreads();
   // Theta(m) for this thread's m values; m = i + 1 covers the first i + 1 sorted entries
   double bv = -1.0;
@@ -181,8 +256,8 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(int B, int G, i
   run = csum[tid];
   for (int i = c0; i < c1; ++i) {
     const float s = __uint_as_float(~(uint32_t)(keys[i] >> 32));
-    run += (unsigned long long)floor((double)s * 4294967296.0);
-    const double tau = (double)B + (double)run / 4294967296.0;
+    run += __float2ull_rz(s * 4294967296.0f);
+    const double tau = (double)B + (double)run * 0x1p-32;
     const double th = __dmul_rn(sps[B + i + 1], tau);
     if (th > bv) {
       bv = th;
@@ -269,10 +344,14 @@ cudaError_t launch_prefix_schedule(int B, int G, const float* S, const double* s
   int Mp2 = 2;
   while (Mp2 < M) Mp2 <<= 1;
   const size_t smem = (size_t)(Mp2 + kSchedThreads) * 8;
-  cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  // keys per thread for the register sort: Mp2 / 1024, at least 1
+  const int E = Mp2 <= kSchedThreads ? 1 : Mp2 / kSchedThreads;
+  auto kern = E == 1 ? schedule_kernel<1> : E == 2 ? schedule_kernel<2> : E == 4 ? schedule_kernel<4>
+            : E == 8 ? schedule_kernel<8> : E == 16 ? schedule_kernel<16> : nullptr;
+  if (!kern) return cudaErrorInvalidValue;  // more than 16384 (b, k) keys
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  schedule_kernel<<<1, kSchedThreads, smem, stream>>>(B, G, M, Mp2, S, sps, len, theta);
+  kern<<<1, kSchedThreads, smem, stream>>>(B, G, M, Mp2, S, sps, len, theta);
   return cudaGetLastError();
 }
 

@@ -69,6 +69,21 @@ def test_prefix_schedule_bit_exact(B, G):
     assert th.item() == th_ref          # bit-exact
 
 
+@pytest.mark.parametrize("B,G", [(512, 7), (40, 3), (2048, 8)])
+def test_prefix_schedule_ties_bit_exact(B, G):
+    # S on a coarse grid: many equal values across requests and positions, so the order of
+    # equal keys (position, then request) decides which prefixes are taken
+    rng = np.random.default_rng(B + 7 * G)
+    c = rng.choice([0.5, 0.75, 1.0], size=(B, G))
+    S = np.cumprod(c, axis=1).astype(np.float32)
+    sps = inputs.sps_table(B, G).numpy()
+    ln_ref, th_ref, st = oracle.prefix_schedule(S, sps)
+    assert st == 0
+    ln, th = ds.prefix_schedule(torch.from_numpy(S).cuda(), torch.from_numpy(sps).cuda())
+    assert np.array_equal(ln.cpu().numpy(), ln_ref)
+    assert th.item() == th_ref
+
+
 def test_prefix_schedule_rejects_increasing_S():
     S = torch.tensor([[0.5, 0.6], [0.4, 0.3]], device="cuda")
     sps = torch.ones(7, dtype=torch.float64, device="cuda")
