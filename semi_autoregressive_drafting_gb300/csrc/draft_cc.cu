@@ -12,19 +12,26 @@
 //     flight while the grid agrees on x_k.  W2 is fetched with an L2 evict-last policy, so the
 //     steps after the first find it in L2 when it fits;
 //   * U_k and target rows of the slice arrive by bulk copy ahead of their step;
-//   * stages go round-robin to the consumer warps (16 for NB <= 2, else 8).  A warp takes
-//     32/NB rows at a time, every lane accumulating a 16-byte K-chunk of each row for each
-//     request (32 independent sums; bf16 operands go straight into mixed-precision FMAs),
-//     then one transposing shuffle reduction leaves lane l with the full dot product of
-//     (row l/NB, request l%NB), and every lane fuses +U_k, /T, the online (max, sum-exp), the
-//     Gumbel-max update and, with a target, the target's (max, sum-exp);
+//   * with 512-byte W2 rows the first 16 stages of the slice are copied into TMEM during the
+//     first step and read back from there afterwards, so the producer streams only the rest;
+//   * stages go round-robin to the consumer warps (24 for one request, 16 for two, 8 for four).
+//     A warp takes 32/NB rows at a time, every lane accumulating a 16-byte K-chunk of each row
+//     for each request (bf16 operands go straight into mixed-precision FMAs), then one
+//     transposing shuffle reduction leaves lane l with the full dot product of (row l/NB,
+//     request l%NB), and the lanes fuse +U_k, /T, the online (max, sum-exp), the Gumbel-max
+//     update and, with a target, the target's (max, sum-exp);
 //   * the Gumbel noise of step k+1 is computed while the block waits at the grid barrier of
 //     step k (it does not depend on the tokens);
-//   * the grid-wide argmax is one 64-bit atomicMax per (request, block) on an order-independent
-//     key; each block also prefetches its candidate's W1 row into L2 so the winner's row is
-//     warm when every block gathers it after the barrier;
+//   * grid barrier and argmax in one: each block merges its warps' results (warp reductions)
+//     and publishes a step-tagged 64-bit key in its own slot; every block polls all slots, so
+//     the barrier completes when the last key lands and its maximum is the drawn token.  Each
+//     block also prefetches its candidate's W1 row into L2 so the winner's row is warm when
+//     every block gathers it after the barrier.  (Opt-in: clusters of blocks first merge in
+//     distributed shared memory and publish one slot per cluster.)
 //   * the Eq 8 label needs both normalisers, so its L1 sum runs right after the barrier from y
-//     and target values kept in shared memory.
+//     and target values kept in shared memory;
+//   * the tensor-core variant (TCV, bf16, B = 3-4) computes the bias with tcgen05 MMAs, the
+//     vocabulary rows on M and the B conditioning vectors on N, from an MMA warp.
 #include <type_traits>
 
 #include <cstring>

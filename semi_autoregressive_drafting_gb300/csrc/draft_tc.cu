@@ -5,12 +5,15 @@
 // W1 rows, [B x r]) is a real dense contraction, so it runs on the 5th-generation tensor cores:
 //   * MMA tile: M = 128 requests (one batch chunk), N = 128 vocab entries, K = r in 64-wide
 //     slabs; A (the gathered W1 rows) is written into shared memory in the 128-byte-swizzled
-//     K-major layout by the epilogue warps, B (W2 rows, stored [V][r]) arrives by 2-D TMA;
-//     the fp32 accumulator lives in TMEM (4 buffers of 128 columns);
-//   * warp 0 produces W2 slabs (runs ahead across tiles, chunks and steps), warp 1 issues the
-//     MMAs from one thread and owns TMEM, warps 4..19 are the epilogue: four warps per TMEM
-//     lane quarter, each taking 32 of a tile's 128 columns for its 32 requests, with U and the
-//     target fetched as 16-byte vectors issued before the accumulator wait;
+//     K-major layout by the epilogue warps, B (W2, stored [V][r] or as the pages write it,
+//     [r][V]) arrives by 2-D TMA; the fp32 accumulator lives in TMEM (4 buffers of 128
+//     columns); with at most 64 requests two vocabulary tiles share one accumulator;
+//   * the blocks form one group per 128-request chunk and the blocks of a group split the
+//     vocabulary, walking their tiles in a serpentine order so that W2 is re-read from L2;
+//   * warp 0 produces W2 slabs and, when U is bf16 with 16-byte rows, U tiles by 3-D TMA (it
+//     runs ahead across tiles, chunks and steps), warp 1 issues the MMAs from one thread and
+//     owns TMEM, warps 4..19 are the epilogue: four warps per TMEM lane quarter, each taking 32
+//     of a tile's 128 columns for its 32 requests;
 //   * the epilogue fuses +U_k, /T, the online (max, sum-exp), and Gumbel-max sampling with an
 //     exact skip, in log2 units (y2 = y log2 e, exponentials by ex2): with w = 1 - u (exact
 //     from the Philox bits) and q = exp(y - best), an entry with w >= 1.001 q cannot beat the
