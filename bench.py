@@ -40,12 +40,12 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: every timed block starts with a cold
 # source file, the sha256 prefix of the source it was measured on, and the bytes.  A workload
 # without a capture, or whose kernel changed since, reports null.
 TRAFFIC = {
-    "qwen3_4b_markov": ("draft_cc.cu", "b7f16e7f9de10484", 81911552),           # 80.61 + 1.30 MB
-    "tiny_markov": ("draft_cc.cu", "b7f16e7f9de10484", 2327552),                # 2.33 + 0 MB
-    "high_concurrency_sched": ("draft_tc.cu", "417929313242095a", 2411431680),  # 2407 + 4.2 MB
+    "qwen3_4b_markov": ("draft_cc.cu", "cb8724e6c2d82289", 81708288),           # 80.61 + 1.10 MB
+    "tiny_markov": ("draft_cc.cu", "cb8724e6c2d82289", 2332160),                # 2.33 + 0 MB
+    "high_concurrency_sched": ("draft_tc.cu", "ec52e23d3affb2df", 2411139584),  # 2407 + 4.2 MB
     # draft_tc_kernel alone; the target's normalisers (272.4 MB) are a launch before it
-    "qwen3_8b_labels": ("draft_tc.cu", "417929313242095a", 628946176),         # 607.4 + 21.5 MB
-    "rnn_head": ("draft_tc.cu", "417929313242095a", 528982016),                 # 524.2 + 4.8 MB
+    "qwen3_8b_labels": ("draft_tc.cu", "ec52e23d3affb2df", 628756992),         # 607.2 + 21.5 MB
+    "rnn_head": ("draft_tc.cu", "ec52e23d3affb2df", 528002048),                 # 523.2 + 4.8 MB
     # the three verify kernels of one call (bench.py --op verify)
     "verify qwen3_8b_labels": ("verify.cu", "c5b18516acacc741", 661831424),
     # the four loss kernels of one call (bench.py --op loss)
