@@ -274,8 +274,13 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "source": self.source}
 
 
+REFERENCE_BUDGET_S = 150.0  # the whole reference run (warm-up and timed steps) stays within this
+
+
 def run_reference(args, wl):
-    """CPU oracle, one draft position (full vocabulary, all B requests) per step."""
+    """CPU oracle, one draft position over the full vocabulary per step, for all B requests, or
+    for the first Bs of them when all B would not let --steps K --warmup W finish within
+    REFERENCE_BUDGET_S (sized from one probe step; the rate is per request, so it compares)."""
     import numpy as np
 
     from oracle import oracle
@@ -286,29 +291,38 @@ def run_reference(args, wl):
     cores = os.cpu_count() or 1
     U = O(t["U"])
     h = O(t["h"])
+    x0 = O(t["x0"])
+    W1, W2, Wj, w = O(t["W1"]), O(t["W2"]), O(t.get("Wj")), O(t["w"])
+    sps = t["sps"].numpy() if t["sps"] is not None else None
 
     cs = []
 
-    def one(k):
-        o = oracle.draft(head=0 if wl.head == "markov" else 1, B=wl.B, gamma=1, V=wl.V,
-                         r=wl.r, d=wl.d, T=wl.T, seed=wl.seed, W1=O(t["W1"]), W2=O(t["W2"]),
-                         Wj=O(t.get("Wj")), U=np.ascontiguousarray(U[:, k:k + 1]),
-                         x0=O(t["x0"]), h=np.ascontiguousarray(h[:, k:k + 1]), w=O(t["w"]),
-                         nthreads=cores)
-        if t["sps"] is not None:  # the block's prefix schedule once gamma positions are in
+    def one(k, nb):
+        o = oracle.draft(head=0 if wl.head == "markov" else 1, B=nb, gamma=1, V=wl.V,
+                         r=wl.r, d=wl.d, T=wl.T, seed=wl.seed, W1=W1, W2=W2, Wj=Wj,
+                         U=np.ascontiguousarray(U[:nb, k:k + 1]), x0=np.ascontiguousarray(x0[:nb]),
+                         h=np.ascontiguousarray(h[:nb, k:k + 1]), w=w, nthreads=cores)
+        if sps is not None:  # the prefix schedule once gamma positions are in
             cs.append(o.c[:, 0])
             if len(cs) == wl.gamma:
-                oracle.prefix_schedule(np.cumprod(np.stack(cs, 1), 1), t["sps"].numpy())
+                oracle.prefix_schedule(np.cumprod(np.stack(cs, 1), 1), sps)
                 cs.clear()
 
-    for i in range(args.warmup):
-        one(i % wl.gamma)
+    t0 = time.perf_counter()
+    one(0, wl.B)  # probe step (also the first warm-up)
+    per_req = (time.perf_counter() - t0) / wl.B
+    nsteps = args.steps + max(0, args.warmup - 1)
+    nb = int(max(1, min(wl.B, REFERENCE_BUDGET_S / max(nsteps, 1) / max(per_req, 1e-9))))
+    for i in range(1, args.warmup):
+        one(i % wl.gamma, nb)
     cs.clear()
     t0 = time.perf_counter()
     for i in range(args.steps):
-        one(i % wl.gamma)
+        one(i % wl.gamma, nb)
     dt = time.perf_counter() - t0
-    value = wl.B * args.steps / dt
+    value = nb * args.steps / dt
+    sample = (f"one draft position over the full vocabulary per step, for {nb} of the "
+              f"{wl.B} requests" + (", the prefix schedule every gamma steps" if sps is not None else ""))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
@@ -316,9 +330,7 @@ def run_reference(args, wl):
         "data": "synthetic", "config": {"workload": wl.name, "B": wl.B, "gamma": wl.gamma,
                                         "V": wl.V, "r": wl.r, "d": wl.d, "T": wl.T},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": "one draft position over the full vocabulary per step"
-                                   + (", the prefix schedule every gamma steps"
-                                      if t["sps"] is not None else "")},
+                         "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
